@@ -1,0 +1,323 @@
+// Paged GQA decode attention and fused RoPE + KV-cache store: plain fp64 CPU oracle.
+//
+// TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only tests/, __graft_entry__.smoke() and the
+// CPU-baseline leg of bench.py may load, call or link this file.  It shares no code,
+// header, table or helper with the CUDA library under paged_kv_cache_244_gb300/, and the
+// library never calls it.
+//
+// Every function below is the plain definition of what the method computes, written out
+// with no blocking, fusion or reordering beyond what that definition states:
+//
+//  * Paged KV cache.  The cache is an array of fixed 16-token physical blocks; each
+//    sequence owns a block table that maps its logical block j to a physical block id,
+//    so token t of the sequence lives in physical block block_table[t / 16] at offset
+//    t % 16.  ("从零实现 LLM 推理引擎：深挖 vLLM 的六大核心优化", §3.1 Paged KV Cache:
+//    16 tokens per block, block_table as a page table; "nano-vllm：vLLM 极简实现与大模型
+//    推理流程解析", FAQ 2: logical-to-physical block mapping table.)
+//  * The new token's slot is (physical block of its position) * 16 + position % 16, the
+//    plain reading of append_slot (same page, §3.2 Continuous Batching).
+//  * GQA: consecutive groups of G = Hq / Hkv query heads share one KV head; query head h
+//    reads KV head h / G.  ("Pico-vLLM：从零手写的工业级LLM推理引擎实现", §核心技术架构解析
+//    1. 模型实现层: GQA.)
+//  * RoPE in the rotate_half form: for i < D/2, with (c, s) = (cos, sin) of the token's
+//    angle for frequency i,
+//        y[i]       = x[i] * c - x[i + D/2] * s
+//        y[i + D/2] = x[i + D/2] * c + x[i] * s
+//    (same page and section: RoPE, rotate_half computed in place; §2. Kernel层: fused
+//    RoPE + KV cache store).  The cos/sin values are an input table, one fp32 row of
+//    [cos(0..D/2-1) | sin(0..D/2-1)] per position.
+//  * Single-token decode: each query head attends over all context_len cached tokens of
+//    its sequence (the token just stored included): softmax(scale * q K^T) V
+//    (same page, §2. Kernel层: PagedAttention Decode Kernel).
+//  * Flash Decode: the context is cut into partitions; each gives (m_p, l_p, o_p) and an
+//    exp-weighted merge gives the same result as the unsplit softmax (same page, §H200上的
+//    详细对比 names Flash Decode; the merge is the standard log-sum-exp identity, the plain
+//    reading since the page gives no formula).
+//
+// Arithmetic: bf16 inputs are widened exactly to double; every sum, exp and product is in
+// double; results are rounded once to bf16 with round-to-nearest-even.
+//
+// Cache layout (the pages leave it open): k_cache and v_cache are each
+// [num_blocks][Hkv][block_size][D] bf16, row-major.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+double widen_bf16(uint16_t b) {
+  uint32_t u = static_cast<uint32_t>(b) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+// Round a double to the nearest bf16 (8 significant bits, exponent range of fp32), ties to
+// even, in one step.  The quantum of the binade of |x| is 2^(e-8) where |x| in
+// [2^(e-1), 2^e); below 2^-126 the quantum is fixed at 2^-133 (bf16 subnormals).
+uint16_t narrow_bf16(double x) {
+  if (std::isnan(x)) return 0x7FC0;
+  if (std::isinf(x)) return x > 0 ? 0x7F80 : 0xFF80;
+  if (x == 0.0) return std::signbit(x) ? 0x8000 : 0x0000;
+  int e = 0;
+  std::frexp(x, &e);  // |x| = m * 2^e, m in [0.5, 1)
+  int qexp = e - 8;
+  if (qexp < -133) qexp = -133;
+  double scaled = std::ldexp(x, -qexp);     // exact: power-of-two scaling
+  double r = std::nearbyint(scaled);        // default rounding mode: nearest, ties to even
+  double y = std::ldexp(r, qexp);           // exact, representable in bf16 or overflowing
+  const double max_bf16 = std::ldexp(255.0, 120);  // (2 - 2^-7) * 2^127
+  if (std::fabs(y) > max_bf16) return y > 0 ? 0x7F80 : 0xFF80;
+  float f = static_cast<float>(y);          // exact: y has at most 8 significant bits
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+size_t cache_index(int blk, int h, int off, int d, int Hkv, int B, int D) {
+  return ((static_cast<size_t>(blk) * Hkv + h) * B + off) * static_cast<size_t>(D) + d;
+}
+
+// Rotate one head vector of length D by the angles of one cos/sin table row.
+void rotate_half(const uint16_t* x, int D, const float* cs_row, double* y) {
+  const int half = D / 2;
+  for (int i = 0; i < half; ++i) {
+    const double c = static_cast<double>(cs_row[i]);
+    const double s = static_cast<double>(cs_row[half + i]);
+    const double a = widen_bf16(x[i]);
+    const double b = widen_bf16(x[half + i]);
+    y[i] = a * c - b * s;
+    y[half + i] = b * c + a * s;
+  }
+}
+
+bool shape_ok(int Hq, int Hkv, int D, int B) {
+  return Hq > 0 && Hkv > 0 && Hq % Hkv == 0 && D > 0 && D % 2 == 0 && B > 0;
+}
+
+int pick_threads(int nthreads, int units) {
+  int n = nthreads;
+  if (n <= 0) n = static_cast<int>(std::thread::hardware_concurrency());
+  if (n <= 0) n = 1;
+  return std::max(1, std::min(n, units));
+}
+
+// Run fn(unit) for unit in [0, units); unit u is always computed by exactly one thread
+// (thread u % n), so results do not depend on the thread count.
+template <class F>
+void parallel_units(int units, int nthreads, F fn) {
+  const int n = pick_threads(nthreads, units);
+  if (n == 1) {
+    for (int u = 0; u < units; ++u) fn(u);
+    return;
+  }
+  std::vector<std::thread> pool;
+  pool.reserve(n);
+  for (int t = 0; t < n; ++t)
+    pool.emplace_back([=] {
+      for (int u = t; u < units; u += n) fn(u);
+    });
+  for (auto& th : pool) th.join();
+}
+
+// Scores of one query head over tokens [t0, t1) of one sequence, in double.
+void head_scores(const uint16_t* qh, const uint16_t* k_cache, const int32_t* bt_row, int g,
+                 int t0, int t1, int Hkv, int B, int D, double scale, double* scores) {
+  for (int t = t0; t < t1; ++t) {
+    const int blk = bt_row[t / B];
+    const int off = t % B;
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d)
+      dot += widen_bf16(qh[d]) * widen_bf16(k_cache[cache_index(blk, g, off, d, Hkv, B, D)]);
+    scores[t - t0] = scale * dot;
+  }
+}
+
+bool table_ok(const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+              int num_seqs, int num_blocks, int B) {
+  for (int s = 0; s < num_seqs; ++s) {
+    const int ctx = context_lens[s];
+    if (ctx < 0 || ctx > max_blocks * B) return false;
+    const int nblk = (ctx + B - 1) / B;
+    for (int j = 0; j < nblk; ++j) {
+      const int blk = block_tables[static_cast<size_t>(s) * max_blocks + j];
+      if (blk < 0 || blk >= num_blocks) return false;
+    }
+  }
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+double orc_bf16_to_f64(uint16_t b) { return widen_bf16(b); }
+
+uint16_t orc_f64_to_bf16(double x) { return narrow_bf16(x); }
+
+// Rotated head vector in double, before rounding (for pinning the rotation itself).
+int orc_rope_rotate_f64(const uint16_t* x, int D, const float* cs_row, double* y) {
+  if (!x || !cs_row || !y || D <= 0 || D % 2) return -1;
+  rotate_half(x, D, cs_row, y);
+  return 0;
+}
+
+// Fused RoPE + KV-cache store for num_tokens new tokens.
+//   q [T][Hq][D] bf16, rotated in place;  k, v [T][Hkv][D] bf16 (read only)
+//   positions [T]; cos_sin [max_pos][D] fp32 = [cos | sin] halves
+//   slot_mapping [T]: slot = physical block * B + offset; a negative slot skips the store
+//   k_cache, v_cache [num_blocks][Hkv][B][D] bf16: rotated k and raw v written at the slot
+// Returns 0, or -1 on a bad argument (nothing is written then).
+int orc_rope_kv_store(int T, int Hq, int Hkv, int D, int B, uint16_t* q, const uint16_t* k,
+                      const uint16_t* v, const int32_t* positions, const float* cos_sin,
+                      int max_pos, const int64_t* slot_mapping, uint16_t* k_cache,
+                      uint16_t* v_cache, int num_blocks) {
+  if (T < 0 || !shape_ok(Hq, Hkv, D, B)) return -1;
+  if (T == 0) return 0;
+  if (!q || !k || !v || !positions || !cos_sin || !slot_mapping || !k_cache || !v_cache) return -1;
+  for (int t = 0; t < T; ++t) {
+    if (positions[t] < 0 || positions[t] >= max_pos) return -1;
+    if (slot_mapping[t] >= static_cast<int64_t>(num_blocks) * B) return -1;
+  }
+  std::vector<double> y(D);
+  for (int t = 0; t < T; ++t) {
+    const float* row = cos_sin + static_cast<size_t>(positions[t]) * D;
+    for (int h = 0; h < Hq; ++h) {
+      uint16_t* qh = q + (static_cast<size_t>(t) * Hq + h) * D;
+      rotate_half(qh, D, row, y.data());
+      for (int d = 0; d < D; ++d) qh[d] = narrow_bf16(y[d]);
+    }
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    const int blk = static_cast<int>(slot / B);
+    const int off = static_cast<int>(slot % B);
+    for (int h = 0; h < Hkv; ++h) {
+      const uint16_t* kh = k + (static_cast<size_t>(t) * Hkv + h) * D;
+      const uint16_t* vh = v + (static_cast<size_t>(t) * Hkv + h) * D;
+      rotate_half(kh, D, row, y.data());
+      for (int d = 0; d < D; ++d) {
+        k_cache[cache_index(blk, h, off, d, Hkv, B, D)] = narrow_bf16(y[d]);
+        v_cache[cache_index(blk, h, off, d, Hkv, B, D)] = vh[d];
+      }
+    }
+  }
+  return 0;
+}
+
+// Single-token paged decode attention, unsplit.
+//   q [S][Hq][D] bf16; block_tables [S][max_blocks]; context_lens [S]
+//   out_f64 [S][Hq][D] (may be null), out_bf16 [S][Hq][D] (may be null)
+// A sequence with context_len 0 gets an all-zero output.
+int orc_decode(int S, int Hq, int Hkv, int D, int B, const uint16_t* q, const uint16_t* k_cache,
+               const uint16_t* v_cache, int num_blocks, const int32_t* block_tables,
+               int max_blocks, const int32_t* context_lens, double scale, int nthreads,
+               double* out_f64, uint16_t* out_bf16) {
+  if (S < 0 || !shape_ok(Hq, Hkv, D, B) || max_blocks < 0) return -1;
+  if (S == 0) return 0;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens) return -1;
+  if (!table_ok(block_tables, max_blocks, context_lens, S, num_blocks, B)) return -1;
+  const int G = Hq / Hkv;
+  parallel_units(S * Hkv, nthreads, [&](int unit) {
+    const int s = unit / Hkv;
+    const int g = unit % Hkv;
+    const int ctx = context_lens[s];
+    const int32_t* bt_row = block_tables + static_cast<size_t>(s) * max_blocks;
+    std::vector<double> scores(std::max(ctx, 1));
+    std::vector<double> o(D);
+    for (int h = g * G; h < (g + 1) * G; ++h) {
+      const size_t obase = (static_cast<size_t>(s) * Hq + h) * D;
+      std::fill(o.begin(), o.end(), 0.0);
+      if (ctx > 0) {
+        head_scores(q + obase, k_cache, bt_row, g, 0, ctx, Hkv, B, D, scale, scores.data());
+        const double m = *std::max_element(scores.begin(), scores.begin() + ctx);
+        double l = 0.0;
+        for (int t = 0; t < ctx; ++t) {
+          const double p = std::exp(scores[t] - m);
+          l += p;
+          const int blk = bt_row[t / B];
+          const int off = t % B;
+          for (int d = 0; d < D; ++d)
+            o[d] += p * widen_bf16(v_cache[cache_index(blk, g, off, d, Hkv, B, D)]);
+        }
+        for (int d = 0; d < D; ++d) o[d] /= l;
+      }
+      for (int d = 0; d < D; ++d) {
+        if (out_f64) out_f64[obase + d] = o[d];
+        if (out_bf16) out_bf16[obase + d] = narrow_bf16(o[d]);
+      }
+    }
+  });
+  return 0;
+}
+
+// Flash Decode: the same attention, computed partition by partition and merged.
+// Partition p covers tokens [p*P, min((p+1)*P, ctx)).  Each gives
+//   m_p = max score,  l_p = sum exp(s - m_p),  o_p = sum exp(s - m_p) v / l_p
+// and the merge is
+//   M = max_p m_p,  out = sum_p exp(m_p - M) l_p o_p / sum_p exp(m_p - M) l_p.
+// The result equals orc_decode's up to rounding order.
+int orc_decode_partitioned(int S, int Hq, int Hkv, int D, int B, const uint16_t* q,
+                           const uint16_t* k_cache, const uint16_t* v_cache, int num_blocks,
+                           const int32_t* block_tables, int max_blocks,
+                           const int32_t* context_lens, double scale, int partition_tokens,
+                           int nthreads, double* out_f64) {
+  if (S < 0 || !shape_ok(Hq, Hkv, D, B) || partition_tokens <= 0 || max_blocks < 0) return -1;
+  if (S == 0) return 0;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out_f64) return -1;
+  if (!table_ok(block_tables, max_blocks, context_lens, S, num_blocks, B)) return -1;
+  const int G = Hq / Hkv;
+  const int P = partition_tokens;
+  parallel_units(S * Hkv, nthreads, [&](int unit) {
+    const int s = unit / Hkv;
+    const int g = unit % Hkv;
+    const int ctx = context_lens[s];
+    const int32_t* bt_row = block_tables + static_cast<size_t>(s) * max_blocks;
+    const int nparts = (ctx + P - 1) / P;
+    std::vector<double> scores(P), mp(nparts), lp(nparts), op(static_cast<size_t>(nparts) * D);
+    for (int h = g * G; h < (g + 1) * G; ++h) {
+      const size_t obase = (static_cast<size_t>(s) * Hq + h) * D;
+      for (int p = 0; p < nparts; ++p) {
+        const int t0 = p * P;
+        const int t1 = std::min(ctx, t0 + P);
+        head_scores(q + obase, k_cache, bt_row, g, t0, t1, Hkv, B, D, scale, scores.data());
+        const double m = *std::max_element(scores.begin(), scores.begin() + (t1 - t0));
+        double l = 0.0;
+        double* o = op.data() + static_cast<size_t>(p) * D;
+        std::fill(o, o + D, 0.0);
+        for (int t = t0; t < t1; ++t) {
+          const double w = std::exp(scores[t - t0] - m);
+          l += w;
+          const int blk = bt_row[t / B];
+          const int off = t % B;
+          for (int d = 0; d < D; ++d)
+            o[d] += w * widen_bf16(v_cache[cache_index(blk, g, off, d, Hkv, B, D)]);
+        }
+        for (int d = 0; d < D; ++d) o[d] /= l;
+        mp[p] = m;
+        lp[p] = l;
+      }
+      for (int d = 0; d < D; ++d) out_f64[obase + d] = 0.0;
+      if (nparts == 0) continue;
+      const double M = *std::max_element(mp.begin(), mp.end());
+      double L = 0.0;
+      for (int p = 0; p < nparts; ++p) L += std::exp(mp[p] - M) * lp[p];
+      for (int p = 0; p < nparts; ++p) {
+        const double w = std::exp(mp[p] - M) * lp[p] / L;
+        for (int d = 0; d < D; ++d) out_f64[obase + d] += w * op[static_cast<size_t>(p) * D + d];
+      }
+    }
+  });
+  return 0;
+}
+
+int orc_hardware_threads(void) {
+  const unsigned n = std::thread::hardware_concurrency();
+  return n ? static_cast<int>(n) : 1;
+}
+
+}  // extern "C"
