@@ -1,0 +1,468 @@
+"""Benchmark of one decode step of paged GQA attention: fused RoPE + KV store, then decode.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mix64] [--impl reference]
+
+A step is one pass of the whole hot path over one batch: pa_rope_kv_store of every
+sequence's new token, then pa_decode over every cached context, for each layer of the
+workload.  The metric is KV-cache bytes read per second: sum(context_lens) * Hkv * D * 2 B
+(K and V) per layer per step, over the step's device time.  L2 is flushed (a 512 MiB write)
+between timed steps, outside the timed events, because the workloads' caches fit in L2.
+
+The printed JSON line carries:
+  value / ms_per_step  from CUDA events around each step, inputs resident in HBM;
+  e2e                  the same metric when every step also copies its inputs (new-token
+                       q/k/v, positions, slots, block tables, lengths) from pinned host
+                       memory and reads the output back, all inside the timed region;
+  roofline             pa_decode (its partition kernel plus the merge kernel when the
+                       context is split) timed alone with CUDA events, against the
+                       measured HBM copy bandwidth;
+  cpu_baseline         the fp64 oracle on the host cores over a bounded sample.
+With --gpus N under torchrun each rank runs its own batch (weak scaling, no collective on
+the data path); value is all ranks' bytes over the slowest rank's time.
+`--impl reference` times the oracle instead, on the host cores (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from paged_kv_cache_244_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged GQA decode: KV-cache HBM GB/s (% of GB300 peak) and attention tokens/s"
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def hbm_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    try:
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------------ clocks ----
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the benchmark runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [r for t, r in self.rows if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            inside = [r for t, r in self.rows if t0 - 0.5 <= t <= t1 + 0.5]
+            note = "timed region shorter than the 100 ms sampling period; nearest samples"
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            try:
+                sm.append(float(r[2]))
+                smax.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, r[6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm), "note": note}
+
+
+# --------------------------------------------------------------------- GPU path ----
+
+class DeviceStep:
+    """A workload resident on the GPU and one step of the hot path over it."""
+
+    def __init__(self, w: W.Workload, torch, binding):
+        self.w, self.torch, self.pa = w, torch, binding
+        dev = torch.device("cuda")
+
+        def bf(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+        L = w.num_layers
+        self.q = [bf(w.q[i]) for i in range(L)]
+        self.q_src = [bf(w.q[i]) for i in range(L)]
+        self.k = [bf(w.k[i]) for i in range(L)]
+        self.v = [bf(w.v[i]) for i in range(L)]
+        self.k_cache = [bf(w.k_cache[i]) for i in range(L)]
+        self.v_cache = [bf(w.v_cache[i]) for i in range(L)]
+        self.positions = torch.from_numpy(w.positions).to(dev)
+        self.slots = torch.from_numpy(w.slot_mapping).to(dev)
+        self.cos_sin = torch.from_numpy(w.cos_sin).to(dev)
+        self.block_tables = torch.from_numpy(w.block_tables).to(dev)
+        self.context_lens = torch.from_numpy(w.context_lens).to(dev)
+        self.out = [torch.empty_like(self.q[i]) for i in range(L)]
+        self.P = binding.decode_partition_tokens(w.num_q_heads, w.num_kv_heads, w.num_seqs,
+                                                 w.max_context_len, w.partition_tokens)
+        self.workspace = binding.decode_workspace(self.q[0], self.k_cache[0], w.max_context_len, self.P)
+        self.max_parts = -(-w.max_context_len // self.P)
+        self.launches_per_step = L * (1 + 1 + (1 if self.max_parts > 1 else 0))
+
+    def rope_store(self, i):
+        self.pa.rope_kv_store(self.q[i], self.k[i], self.v[i], self.positions, self.cos_sin,
+                              self.slots, self.k_cache[i], self.v_cache[i])
+
+    def decode(self, i):
+        w = self.w
+        self.pa.decode(self.q[i], self.k_cache[i], self.v_cache[i], self.block_tables,
+                       self.context_lens, w.max_context_len, w.scale, partition_tokens=self.P,
+                       workspace=self.workspace, out=self.out[i])
+
+    def step(self):
+        for i in range(self.w.num_layers):
+            self.rope_store(i)
+            self.decode(i)
+
+
+def run_gpu(args, rank, world, dist):
+    import torch
+
+    from paged_kv_cache_244_gb300 import _build, binding
+
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local_rank)
+    if rank == 0:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    base = W.make(args.workload)
+    w = base if rank == 0 else W.make(args.workload, seed=base.seed + 1000 * rank)
+    st = DeviceStep(w, torch, binding)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    bytes_step = w.kv_bytes_per_layer() * w.num_layers
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def timed_loop(fn, steps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    # warm-up (also builds the library state and the kernels' shared-memory attributes)
+    for _ in range(args.warmup):
+        st.step()
+    rc, flags = binding.get_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after warm-up: {rc} flags {flags:#x}")
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    t_wall0 = time.time()
+    step_ms = timed_loop(st.step, args.steps)
+    barrier()
+    t_wall1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    total_ms = float(np.sum(step_ms))
+
+    # pa_decode alone (roofline of the dominant kernel), same flush discipline
+    dec_ms = timed_loop(lambda: st.decode(0), args.steps)
+    dec_avg = float(np.mean(dec_ms))
+    rope_ms = timed_loop(lambda: st.rope_store(0), max(3, args.steps // 4))
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, st, torch, binding, flush)
+
+    rc, flags = binding.get_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after timing: {rc} flags {flags:#x}")
+
+    # max over ranks of the timed device time; sum of bytes
+    t = torch.tensor([total_ms, e2e["ms"]], dtype=torch.float64, device="cuda")
+    b = torch.tensor([float(bytes_step)], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    total_ms_max, e2e_ms_max = float(t[0]), float(t[1])
+    all_bytes = float(b[0])
+    if rank != 0:
+        return None
+
+    peak, peak_kind = hbm_peak()
+    gbs = all_bytes * args.steps / (total_ms_max * 1e-3) / 1e9
+    dec_bytes = w.kv_bytes_per_layer()
+    achieved = dec_bytes / (dec_avg * 1e-3) / 1e9
+    tokens_per_s = world * w.num_seqs * args.steps / (total_ms_max * 1e-3)
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms_max / args.steps, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded splitmix64 -> Box-Muller -> bf16)",
+        "pct_of_peak": round(100.0 * gbs / peak, 2),
+        "tokens_per_s": round(tokens_per_s, 1),
+        "config": config_of(w, st, world),
+        "roofline": {
+            "kernel": "pa_decode (decode_partition_kernel + decode_merge_kernel)",
+            "bound": "hbm",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": args.traffic,
+            "algorithmic_bytes_per_launch": dec_bytes,
+            "avg_launch_ms": round(dec_avg, 6),
+        },
+        "rope_kv_store_us": round(1e3 * float(np.median(rope_ms)), 3),
+        "e2e": {"value": round(all_bytes * args.steps / (e2e_ms_max * 1e-3) / 1e9, 2),
+                "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": round(e2e_ms_max / args.steps, 6)},
+        "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    return line
+
+
+def run_e2e(args, st, torch, binding, flush):
+    """Every step: pinned host -> device copies of the step's inputs, the C-ABI calls, and
+    the device -> host read of the attention output, all between the CUDA events."""
+    w = st.w
+    stream = torch.cuda.current_stream()
+    L = w.num_layers
+
+    def pinned(t):
+        return t.detach().cpu().pin_memory()
+
+    h_q = [pinned(st.q_src[i]) for i in range(L)]
+    h_k = [pinned(st.k[i]) for i in range(L)]
+    h_v = [pinned(st.v[i]) for i in range(L)]
+    h_pos, h_slot = pinned(st.positions), pinned(st.slots)
+    h_bt, h_ctx = pinned(st.block_tables), pinned(st.context_lens)
+    h_out = [torch.empty(st.out[i].shape, dtype=torch.bfloat16).pin_memory() for i in range(L)]
+    h2d = sum(x.numel() * x.element_size() for x in h_q + h_k + h_v + [h_pos, h_slot, h_bt, h_ctx])
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+
+    def one():
+        st.positions.copy_(h_pos, non_blocking=True)
+        st.slots.copy_(h_slot, non_blocking=True)
+        st.block_tables.copy_(h_bt, non_blocking=True)
+        st.context_lens.copy_(h_ctx, non_blocking=True)
+        for i in range(L):
+            st.q[i].copy_(h_q[i], non_blocking=True)
+            st.k[i].copy_(h_k[i], non_blocking=True)
+            st.v[i].copy_(h_v[i], non_blocking=True)
+            st.rope_store(i)
+            st.decode(i)
+            h_out[i].copy_(st.out[i], non_blocking=True)
+
+    for _ in range(2):
+        one()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in evs:
+        flush.fill_(1)
+        a.record(stream)
+        one()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.sum([a.elapsed_time(b) for a, b in evs]))
+    return {"ms": ms, "h2d": int(h2d), "d2h": int(d2h)}
+
+
+def config_of(w, st, world):
+    c = {
+        "workload": w.name,
+        "num_seqs_per_gpu": w.num_seqs,
+        "num_layers": w.num_layers,
+        "context_lens": describe_ctx(w),
+        "num_q_heads": w.num_q_heads,
+        "num_kv_heads": w.num_kv_heads,
+        "head_dim": W.HEAD_DIM,
+        "block_size": W.BLOCK_SIZE,
+        "pool_blocks": w.num_blocks,
+        "partition_tokens": st.P if st is not None else w.partition_tokens,
+        "kv_bytes_per_step_per_gpu": w.kv_bytes_per_layer() * w.num_layers,
+        "l2": "flushed between timed steps (512 MiB write, outside the events)",
+        "parallelism": f"replicas x{world} (independent batches)",
+    }
+    if w.meta.get("shared_prefix_blocks"):
+        c["unique_kv_bytes_per_step_per_gpu"] = w.unique_kv_bytes_per_layer() * w.num_layers
+    return c
+
+
+def describe_ctx(w):
+    c = w.context_lens
+    if w.name == "mix64":
+        return f"uniform[64,4096] seeded: sum {int(c.sum())}, min {int(c.min())}, max {int(c.max())}"
+    return [int(x) for x in c[:8]] + (["..."] if len(c) > 8 else [])
+
+
+# ------------------------------------------------------------------ CPU oracle ----
+
+def oracle_step(orc, w, sample_seqs, nthreads):
+    """The oracle's RoPE + store and decode over the first `sample_seqs` sequences of every
+    layer.  Returns the KV bytes the decode read."""
+    n = min(sample_seqs, w.num_seqs)
+    total = 0
+    for layer in range(w.num_layers):
+        kc, vc = w.k_cache[layer].copy(), w.v_cache[layer].copy()
+        q = orc.rope_kv_store(w.q[layer, :n], w.k[layer, :n], w.v[layer, :n], w.positions[:n],
+                              w.cos_sin, w.slot_mapping[:n], kc, vc)
+        orc.decode(q, kc, vc, w.block_tables[:n], w.context_lens[:n], w.scale, nthreads=nthreads)
+        total += int(w.context_lens[:n].astype(np.int64).sum()) * w.num_kv_heads * W.HEAD_DIM * 4
+    return total
+
+
+def choose_sample(orc, w, budget_s, nthreads):
+    """Number of sequences whose oracle step takes about budget_s (at least 1)."""
+    n = max(1, min(w.num_seqs, 4))
+    t0 = time.perf_counter()
+    oracle_step(orc, w, n, nthreads)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    return max(1, min(w.num_seqs, int(n * budget_s / dt)))
+
+
+def cpu_baseline(w, budget_s=10.0):
+    import oracle
+    orc = oracle.default()
+    cores = orc.hardware_threads()
+    n = choose_sample(orc, w, budget_s, 0)
+    t0 = time.perf_counter()
+    nbytes = oracle_step(orc, w, n, 0)
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle RoPE+store and decode of the first {n} of {w.num_seqs} "
+                      f"sequences x {w.num_layers} layer(s), {dt:.1f} s on {cores} threads"}
+
+
+def run_reference(args, world):
+    import oracle
+    orc = oracle.default()
+    cores = orc.hardware_threads()
+    w = W.make(args.workload)
+    per_step = max(0.2, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    n = choose_sample(orc, w, per_step, 0)
+    for _ in range(args.warmup):
+        oracle_step(orc, w, n, 0)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += oracle_step(orc, w, n, 0)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    sample = (f"fp64 oracle RoPE+store and decode of the first {n} of {w.num_seqs} sequences x "
+              f"{w.num_layers} layer(s) per step, on {cores} host threads")
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * dt / max(1, args.steps), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference", "config": config_of(w, None, world),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="mix64", choices=W.WORKLOADS)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes read+written per pa_decode call from an ncu capture")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world)), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as td
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        td.init_process_group("nccl")
+        dist = td
+    line = run_gpu(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * pa.h -- paged GQA decode attention and the fused RoPE + KV-cache store, as a C ABI.
+ *
+ * Library: paged_kv_cache_244_gb300/libpa_gb300.so (CUDA, sm_103a).  Plain C: no CUDA,
+ * C++ or framework types appear here.  Streams are passed as `void*` and are CUDA stream
+ * handles (cudaStream_t); NULL means the legacy default stream.
+ *
+ * The operations follow these passages (page title, section):
+ *   [PV]  "Pico-vLLM：从零手写的工业级LLM推理引擎实现"
+ *         §1 模型实现层: RoPE computed with rotate_half in place; GQA, where groups of query
+ *            heads share one KV head.
+ *         §2 Kernel层: the PagedAttention decode kernel (one new token per sequence attends
+ *            over its cached context) and the fused RoPE + KV cache store.
+ *         §H200上的详细对比: Flash Decode, i.e. the context split into partitions whose
+ *            partial softmax results are merged.
+ *   [ME]  "从零实现 LLM 推理引擎：深挖 vLLM 的六大核心优化"
+ *         §3.1 Paged KV Cache: the cache is made of fixed blocks of 16 tokens, and each
+ *            sequence has a block_table mapping logical block index -> physical block id.
+ *         §3.2 Continuous Batching: append_slot gives every running sequence one new slot
+ *            per decode step.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Element types: q, k, v, caches and out are bf16 (16-bit, passed as void*).  cos_sin is
+ *    fp32.  All arithmetic inside is fp32 with fp32 accumulation.
+ *  - Layouts are dense row-major, with no strides:
+ *      q            [num_tokens or num_seqs][num_q_heads][head_dim]
+ *      k, v         [num_tokens][num_kv_heads][head_dim]
+ *      k_cache,
+ *      v_cache      [num_blocks][num_kv_heads][block_size][head_dim]   ("HND" blocks)
+ *      cos_sin      [max_pos][head_dim] fp32: row p = cos(p*w_0..w_{D/2-1}) | sin(...)
+ *      block_tables [num_seqs][max_blocks] int32 physical block ids
+ *      out          [num_seqs][num_q_heads][head_dim]
+ *    With block_size 16 and head_dim 128 each (block, KV head) tile is 4 KiB contiguous.
+ *  - Slot of a token: physical_block * block_size + offset_in_block.
+ *  - Supported shape: head_dim == 128, block_size == 16, num_q_heads a multiple of
+ *    num_kv_heads with group size num_q_heads / num_kv_heads in [1, 8].  Anything else
+ *    returns PA_ERR_SHAPE.
+ *  - Memory: every pointer is device memory owned by the caller (cudaMalloc, PyTorch, ...)
+ *    and must be 16-byte aligned (PA_ERR_ALIGN otherwise).  The library allocates nothing.
+ *    Its only global state is one 32-bit device status word per GPU.
+ *  - Asynchrony: calls enqueue work on `stream` and return at once.  Arguments the host can
+ *    check are checked before anything is enqueued; on error nothing is launched.
+ *  - Values only the device can see (block ids, positions, slots, per-sequence lengths) are
+ *    checked by the kernels: an out-of-range one is skipped (never dereferenced) and a flag
+ *    is raised in the device status word; read it with pa_get_device_status().
+ *  - Kernels launch with programmatic dependent launch: they wait for the previous kernel
+ *    on the stream before reading any input, so ordinary stream order holds.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pa_dims {
+  int32_t num_q_heads;   /* Hq, e.g. 12 */
+  int32_t num_kv_heads;  /* Hkv, e.g. 2; GQA group G = Hq / Hkv */
+  int32_t head_dim;      /* D, must be 128 */
+  int32_t block_size;    /* tokens per cache block, must be 16 */
+} pa_dims;
+
+/* Return codes (negative = error, nothing was enqueued unless noted). */
+enum {
+  PA_OK = 0,
+  PA_ERR_NULL = -1,        /* a required pointer is NULL */
+  PA_ERR_SHAPE = -2,       /* unsupported head_dim / block_size / head counts */
+  PA_ERR_RANGE = -3,       /* a count or length is out of range */
+  PA_ERR_WORKSPACE = -4,   /* workspace missing or smaller than pa_decode_workspace_size */
+  PA_ERR_CUDA = -5,        /* a CUDA runtime call failed (the launch itself, or a query) */
+  PA_ERR_DEVICE_OOB = -6,  /* pa_get_device_status: a kernel met an out-of-range value */
+  PA_ERR_TIMEOUT = -7,     /* pa_get_device_status: a kernel gave up a bounded wait */
+  PA_ERR_ALIGN = -8        /* a pointer is not 16-byte aligned */
+};
+
+/* Flags of the device status word (bitwise OR of everything seen since the last read). */
+#define PA_FLAG_BLOCK_ID_OOB    0x1u  /* block_tables entry outside [0, num_blocks) */
+#define PA_FLAG_CONTEXT_LEN_OOB 0x2u  /* context_lens[s] outside [0, max_context_len] */
+#define PA_FLAG_SLOT_OOB        0x4u  /* slot_mapping[t] >= num_blocks * block_size */
+#define PA_FLAG_POSITION_OOB    0x8u  /* positions[t] outside [0, max_pos) */
+#define PA_FLAG_TIMEOUT         0x10u /* a copy into shared memory did not land in time */
+
+/*
+ * pa_rope_kv_store -- fused RoPE + KV-cache store for `num_tokens` new tokens
+ * ([PV] §1 and §2: RoPE with rotate_half, fused with the KV cache store; [ME] §3.1/§3.2:
+ * the token's K and V go to the slot append_slot gave it).
+ *
+ * For each token t with p = positions[t], (c_i, s_i) = cos_sin[p][i], cos_sin[p][D/2 + i]:
+ *   every query head  q[t][h]:  q'[i] = q[i] c_i - q[i+D/2] s_i,  q'[i+D/2] = q[i+D/2] c_i + q[i] s_i
+ *                               written back into q (IN PLACE), rounded to bf16 (RNE);
+ *   every KV head g:            k_cache[slot][g] = rotate(k[t][g]) (same formula, bf16 RNE),
+ *                               v_cache[slot][g] = v[t][g] (bit copy),
+ *   where slot = slot_mapping[t] (block = slot / block_size, offset = slot % block_size).
+ * A negative slot means "padding token": q is rotated, nothing is stored.
+ * Device-side errors: p outside [0, max_pos) -> token skipped entirely (q left unrotated),
+ * PA_FLAG_POSITION_OOB; slot >= num_blocks * block_size -> store skipped, PA_FLAG_SLOT_OOB.
+ *
+ *   dims          shape (see conventions)
+ *   num_tokens    T >= 0 (0 is a no-op)
+ *   q             [T][Hq][D] bf16, read and overwritten
+ *   k, v          [T][Hkv][D] bf16, read only
+ *   positions     [T] int32
+ *   cos_sin       [max_pos][D] fp32, read only
+ *   max_pos       rows of cos_sin, >= 1
+ *   slot_mapping  [T] int64
+ *   k_cache, v_cache  [num_blocks][Hkv][block_size][D] bf16, written at the slots only
+ *   num_blocks    >= 1
+ *   stream        CUDA stream
+ * Returns PA_OK or a PA_ERR_* code (nothing launched on error).
+ */
+int pa_rope_kv_store(const pa_dims* dims, int num_tokens, void* q, const void* k, const void* v,
+                     const int32_t* positions, const float* cos_sin, int max_pos,
+                     const int64_t* slot_mapping, void* k_cache, void* v_cache, int num_blocks,
+                     void* stream);
+
+/*
+ * pa_decode_partition_tokens -- the context partition size pa_decode will use (Flash Decode,
+ * [PV] §H200上的详细对比).  `partition_tokens` > 0 is used as given (it must be a multiple
+ * of block_size); 0 asks the library to choose: the smallest power-of-two multiple of
+ * block_size for which num_seqs * num_kv_heads * ceil(max_context_len / P) <= 2048.
+ * Returns P >= block_size, or a negative PA_ERR_* code.
+ */
+int pa_decode_partition_tokens(const pa_dims* dims, int num_seqs, int max_context_len,
+                               int partition_tokens);
+
+/*
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for these
+ * arguments: num_seqs * Hq * ceil(max_context_len / P) * (D + 2) * 4 when the context is
+ * split into more than one partition, else 0.  Returns 0 for invalid arguments (pa_decode
+ * then reports the error).
+ */
+size_t pa_decode_workspace_size(const pa_dims* dims, int num_seqs, int max_context_len,
+                                int partition_tokens);
+
+/*
+ * pa_decode -- single-token paged GQA decode attention ([PV] §2: PagedAttention decode
+ * kernel; [ME] §3.1: block tables; [PV] §1: GQA; [PV] §H200上的详细对比: Flash Decode).
+ *
+ * For each sequence s with n = context_lens[s] (the new token, already stored, included)
+ * and each query head h, with g = h / (Hq / Hkv) and, for t < n,
+ *   K_t = k_cache[block_tables[s][t / 16]][g][t % 16],  V_t likewise,
+ *   out[s][h] = sum_t softmax_t(scale * q[s][h] . K_t) V_t      (bf16 RNE of the fp32 result)
+ * Table entries past ceil(n / 16) and cache slots past n are never read.  n == 0 gives an
+ * all-zero output row.  When ceil(max_context_len / P) > 1 the context is processed in
+ * partitions of P tokens whose partial (max, sum, weighted V) are merged by a second kernel;
+ * the result is the same softmax up to fp32 rounding order.
+ * Device-side errors: a block id outside [0, num_blocks) -> that block is skipped,
+ * PA_FLAG_BLOCK_ID_OOB; n outside [0, max_context_len] -> clamped, PA_FLAG_CONTEXT_LEN_OOB.
+ *
+ *   num_seqs          S >= 0 (0 is a no-op)
+ *   q                 [S][Hq][D] bf16 (already rotated), read only
+ *   k_cache, v_cache  [num_blocks][Hkv][16][D] bf16, read only
+ *   block_tables      [S][max_blocks] int32
+ *   context_lens      [S] int32 (device copy)
+ *   max_context_len   host-side upper bound of context_lens, 1 <= it <= max_blocks * 16
+ *   scale             softmax scale, finite and > 0 (1/sqrt(D) for standard attention)
+ *   partition_tokens  0 (library chooses) or a positive multiple of 16
+ *   workspace         device memory of >= pa_decode_workspace_size(...) bytes, or NULL
+ *                     when that size is 0; its contents need no initialisation
+ *   out               [S][Hq][D] bf16, written
+ * Returns PA_OK or a PA_ERR_* code (nothing launched on error).  Launches one kernel, plus
+ * one merge kernel when the context is split.
+ */
+int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_cache,
+              const void* v_cache, int num_blocks, const int32_t* block_tables, int max_blocks,
+              const int32_t* context_lens, int max_context_len, float scale,
+              int partition_tokens, void* workspace, size_t workspace_bytes, void* out,
+              void* stream);
+
+/*
+ * pa_get_device_status -- synchronise `stream`, then read and clear the calling thread's
+ * current GPU's status word.  *flags receives the PA_FLAG_* bits raised since the last
+ * read (may be NULL).  Returns PA_OK when no flag was set, PA_ERR_TIMEOUT when the timeout
+ * flag was set, PA_ERR_DEVICE_OOB when any other flag was set, PA_ERR_CUDA on a CUDA error.
+ */
+int pa_get_device_status(void* stream, uint32_t* flags);
+
+/* Human-readable name of a PA_* return code (static storage, never NULL). */
+const char* pa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,192 @@
+"""Thin Python binding of the C ABI in include/pa.h (argument marshalling only).
+
+Every function here checks tensor devices, dtypes, shapes and contiguity, passes raw
+device pointers and the current CUDA stream to libpa_gb300.so, and turns a negative return
+code into PaError.  All computation happens in the library's CUDA kernels: there is no
+fallback, and using any function without the compiled library raises at once.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+LIBRARY = Path(__file__).resolve().parent / "libpa_gb300.so"
+
+PA_OK = 0
+PA_ERR_NULL = -1
+PA_ERR_SHAPE = -2
+PA_ERR_RANGE = -3
+PA_ERR_WORKSPACE = -4
+PA_ERR_CUDA = -5
+PA_ERR_DEVICE_OOB = -6
+PA_ERR_TIMEOUT = -7
+PA_ERR_ALIGN = -8
+
+PA_FLAG_BLOCK_ID_OOB = 0x1
+PA_FLAG_CONTEXT_LEN_OOB = 0x2
+PA_FLAG_SLOT_OOB = 0x4
+PA_FLAG_POSITION_OOB = 0x8
+PA_FLAG_TIMEOUT = 0x10
+
+
+class PaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+class pa_dims(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded C library with argument types declared (raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not LIBRARY.exists():
+            raise RuntimeError(f"{LIBRARY.name} is not built: run __graft_entry__.build() "
+                               "(the CUDA kernels are the only implementation)")
+        L = ctypes.CDLL(str(LIBRARY))
+        p, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        pd = ctypes.POINTER(pa_dims)
+        L.pa_rope_kv_store.argtypes = [pd, i, p, p, p, p, p, i, p, p, p, i, p]
+        L.pa_rope_kv_store.restype = i
+        L.pa_decode_partition_tokens.argtypes = [pd, i, i, i]
+        L.pa_decode_partition_tokens.restype = i
+        L.pa_decode_workspace_size.argtypes = [pd, i, i, i]
+        L.pa_decode_workspace_size.restype = ctypes.c_size_t
+        L.pa_decode.argtypes = [pd, i, p, p, p, i, p, i, p, i, f, i, p, ctypes.c_size_t, p, p]
+        L.pa_decode.restype = i
+        L.pa_get_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
+        L.pa_get_device_status.restype = i
+        L.pa_status_string.argtypes = [i]
+        L.pa_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().pa_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != PA_OK:
+        raise PaError(code, what)
+
+
+def _dev_ptr(t: torch.Tensor | None, name: str, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_dims(num_q_heads: int, num_kv_heads: int, head_dim: int = 128, block_size: int = 16):
+    return pa_dims(num_q_heads, num_kv_heads, head_dim, block_size)
+
+
+def rope_kv_store(q, k, v, positions, cos_sin, slot_mapping, k_cache, v_cache, stream=None):
+    """Fused RoPE + KV-cache store (pa_rope_kv_store): rotates q in place, writes the caches.
+
+    q [T, Hq, D] bf16; k, v [T, Hkv, D] bf16; positions [T] int32; cos_sin [max_pos, D] fp32;
+    slot_mapping [T] int64; k_cache, v_cache [num_blocks, Hkv, B, D] bf16.
+    """
+    T, Hq, D = q.shape
+    nb, Hkv, B, D2 = k_cache.shape
+    if D2 != D or tuple(k.shape) != (T, Hkv, D) or tuple(v.shape) != (T, Hkv, D):
+        raise ValueError("shape mismatch between q, k, v and the caches")
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache differ in shape")
+    if positions.shape != (T,) or slot_mapping.shape != (T,) or cos_sin.shape[1] != D:
+        raise ValueError("positions / slot_mapping / cos_sin shape mismatch")
+    dims = make_dims(Hq, Hkv, D, B)
+    bf = torch.bfloat16
+    rc = lib().pa_rope_kv_store(
+        ctypes.byref(dims), T, _dev_ptr(q, "q", bf), _dev_ptr(k, "k", bf), _dev_ptr(v, "v", bf),
+        _dev_ptr(positions, "positions", torch.int32), _dev_ptr(cos_sin, "cos_sin", torch.float32),
+        cos_sin.shape[0], _dev_ptr(slot_mapping, "slot_mapping", torch.int64),
+        _dev_ptr(k_cache, "k_cache", bf), _dev_ptr(v_cache, "v_cache", bf), nb, _stream(stream))
+    _check(rc, "pa_rope_kv_store")
+
+
+def decode_partition_tokens(num_q_heads, num_kv_heads, num_seqs, max_context_len,
+                            partition_tokens=0, head_dim=128, block_size=16) -> int:
+    dims = make_dims(num_q_heads, num_kv_heads, head_dim, block_size)
+    rc = lib().pa_decode_partition_tokens(ctypes.byref(dims), num_seqs, max_context_len,
+                                          partition_tokens)
+    if rc < 0:
+        raise PaError(rc, "pa_decode_partition_tokens")
+    return rc
+
+
+def decode_workspace_size(num_q_heads, num_kv_heads, num_seqs, max_context_len,
+                          partition_tokens=0, head_dim=128, block_size=16) -> int:
+    dims = make_dims(num_q_heads, num_kv_heads, head_dim, block_size)
+    return int(lib().pa_decode_workspace_size(ctypes.byref(dims), num_seqs, max_context_len,
+                                              partition_tokens))
+
+
+def decode_workspace(q, k_cache, max_context_len, partition_tokens=0) -> torch.Tensor | None:
+    """Allocate the workspace pa_decode needs for these shapes (None when it needs none)."""
+    S, Hq, D = q.shape
+    _, Hkv, B, _ = k_cache.shape
+    n = decode_workspace_size(Hq, Hkv, S, max_context_len, partition_tokens, D, B)
+    if n == 0:
+        return None
+    return torch.empty((n + 3) // 4, dtype=torch.float32, device=q.device)
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
+           partition_tokens=0, workspace=None, out=None, stream=None):
+    """Paged GQA decode attention (pa_decode).  Returns out [S, Hq, D] bf16.
+
+    q [S, Hq, D] bf16; k_cache, v_cache [num_blocks, Hkv, B, D] bf16; block_tables
+    [S, max_blocks] int32; context_lens [S] int32; max_context_len a host int bounding them.
+    `workspace` (float32, from decode_workspace) is allocated here when None and needed.
+    """
+    S, Hq, D = q.shape
+    nb, Hkv, B, D2 = k_cache.shape
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables / context_lens shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = decode_workspace(q, k_cache, max_context_len, partition_tokens)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    dims = make_dims(Hq, Hkv, D, B)
+    bf = torch.bfloat16
+    rc = lib().pa_decode(
+        ctypes.byref(dims), S, _dev_ptr(q, "q", bf), _dev_ptr(k_cache, "k_cache", bf),
+        _dev_ptr(v_cache, "v_cache", bf), nb, _dev_ptr(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev_ptr(context_lens, "context_lens", torch.int32),
+        int(max_context_len), float(scale), int(partition_tokens), _dev_ptr(workspace, "workspace"),
+        ws_bytes, _dev_ptr(out, "out", bf), _stream(stream))
+    _check(rc, "pa_decode")
+    return out
+
+
+def get_device_status(stream=None) -> tuple[int, int]:
+    """Synchronise the stream and read+clear the device status word: (code, flags)."""
+    flags = ctypes.c_uint32(0)
+    rc = lib().pa_get_device_status(_stream(stream), ctypes.byref(flags))
+    return rc, int(flags.value)

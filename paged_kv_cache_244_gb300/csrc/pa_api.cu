@@ -1,0 +1,205 @@
+// C ABI of the paged decode attention library (declared in include/pa.h).
+//
+// Host side only: argument checks that need no device access, choice of the Flash-Decode
+// partition size, workspace carving, the device status word, and the kernel launches.
+// Nothing here allocates device memory.
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "pa.h"
+#include "pa_launch.h"
+
+namespace {
+
+// One status word per GPU that loads the library: kernels OR PA_FLAG_* bits into it.
+__device__ unsigned int g_pa_status;
+
+constexpr int kMaxDevices = 64;
+constexpr int kTargetUnits = 2048;  // auto partition size: at most this many (seq, kv, part)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const pa_dims* d) {
+  if (!d) return PA_ERR_NULL;
+  if (d->head_dim != 128 || d->block_size != 16) return PA_ERR_SHAPE;
+  if (d->num_q_heads <= 0 || d->num_kv_heads <= 0) return PA_ERR_SHAPE;
+  if (d->num_q_heads % d->num_kv_heads != 0) return PA_ERR_SHAPE;
+  const int G = d->num_q_heads / d->num_kv_heads;
+  if (G < 1 || G > 8) return PA_ERR_SHAPE;
+  return PA_OK;
+}
+
+// Resolve the partition size; negative = error.
+int resolve_partition(const pa_dims* d, int num_seqs, int max_context_len, int requested) {
+  if (const int rc = check_dims(d)) return rc;
+  if (num_seqs < 0 || max_context_len < 1) return PA_ERR_RANGE;
+  if (requested < 0 || requested % d->block_size != 0) return PA_ERR_RANGE;
+  if (requested > 0) return requested;
+  long long P = d->block_size;
+  const long long pairs = static_cast<long long>(num_seqs) * d->num_kv_heads;
+  while (P < max_context_len && pairs * ((max_context_len + P - 1) / P) > kTargetUnits) P *= 2;
+  return static_cast<int>(P);
+}
+
+int max_parts_for(int max_context_len, int P) { return (max_context_len + P - 1) / P; }
+
+size_t workspace_bytes_for(const pa_dims* d, int num_seqs, int max_parts) {
+  if (max_parts <= 1) return 0;
+  return static_cast<size_t>(num_seqs) * d->num_q_heads * max_parts *
+         (static_cast<size_t>(d->head_dim) + 2) * sizeof(float);
+}
+
+// Device address of this GPU's status word (looked up once per device).
+int status_word(unsigned** out) {
+  static std::mutex mu;
+  static unsigned* cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pa_status) != cudaSuccess) return PA_ERR_CUDA;
+    cache[dev] = static_cast<unsigned*>(p);
+  }
+  *out = cache[dev];
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_rope_kv_store(const pa_dims* dims, int num_tokens, void* q, const void* k, const void* v,
+                     const int32_t* positions, const float* cos_sin, int max_pos,
+                     const int64_t* slot_mapping, void* k_cache, void* v_cache, int num_blocks,
+                     void* stream) {
+  if (const int rc = check_dims(dims)) return rc;
+  if (num_tokens < 0) return PA_ERR_RANGE;
+  if (num_tokens == 0) return PA_OK;
+  if (!q || !k || !v || !positions || !cos_sin || !slot_mapping || !k_cache || !v_cache)
+    return PA_ERR_NULL;
+  if (max_pos < 1 || num_blocks < 1) return PA_ERR_RANGE;
+  const void* ptrs[] = {q, k, v, positions, cos_sin, slot_mapping, k_cache, v_cache};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return PA_ERR_ALIGN;
+  unsigned* status = nullptr;
+  if (const int rc = status_word(&status)) return rc;
+  pa::RopeArgs a;
+  a.q = static_cast<__nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.positions = positions;
+  a.cos_sin = cos_sin;
+  a.slot_mapping = slot_mapping;
+  a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  a.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  a.num_tokens = num_tokens;
+  a.num_q_heads = dims->num_q_heads;
+  a.num_kv_heads = dims->num_kv_heads;
+  a.max_pos = max_pos;
+  a.num_blocks = num_blocks;
+  a.status = status;
+  return pa::launch_rope_kv_store(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+int pa_decode_partition_tokens(const pa_dims* dims, int num_seqs, int max_context_len,
+                               int partition_tokens) {
+  return resolve_partition(dims, num_seqs, max_context_len, partition_tokens);
+}
+
+size_t pa_decode_workspace_size(const pa_dims* dims, int num_seqs, int max_context_len,
+                                int partition_tokens) {
+  const int P = resolve_partition(dims, num_seqs, max_context_len, partition_tokens);
+  if (P <= 0) return 0;
+  return workspace_bytes_for(dims, num_seqs, max_parts_for(max_context_len, P));
+}
+
+int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_cache,
+              const void* v_cache, int num_blocks, const int32_t* block_tables, int max_blocks,
+              const int32_t* context_lens, int max_context_len, float scale,
+              int partition_tokens, void* workspace, size_t workspace_bytes, void* out,
+              void* stream) {
+  if (const int rc = check_dims(dims)) return rc;
+  if (num_seqs < 0) return PA_ERR_RANGE;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
+  if (num_blocks < 1 || max_blocks < 1 || max_context_len < 1) return PA_ERR_RANGE;
+  if (static_cast<long long>(max_context_len) > static_cast<long long>(max_blocks) * dims->block_size)
+    return PA_ERR_RANGE;
+  if (static_cast<long long>(num_blocks) * dims->num_kv_heads * dims->block_size > (1ll << 31))
+    return PA_ERR_RANGE;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return PA_ERR_RANGE;
+  const int P = resolve_partition(dims, num_seqs, max_context_len, partition_tokens);
+  if (P < 0) return P;
+  const int max_parts = max_parts_for(max_context_len, P);
+  const size_t need = workspace_bytes_for(dims, num_seqs, max_parts);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return PA_ERR_WORKSPACE;
+  const void* ptrs[] = {q, k_cache, v_cache, block_tables, context_lens, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return PA_ERR_ALIGN;
+  if (need > 0 && !aligned16(workspace)) return PA_ERR_ALIGN;
+  unsigned* status = nullptr;
+  if (const int rc = status_word(&status)) return rc;
+
+  pa::DecodeArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  a.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  float* ws = static_cast<float*>(workspace);
+  const size_t o_floats = static_cast<size_t>(num_seqs) * dims->num_q_heads * max_parts * dims->head_dim;
+  a.ws_o = need ? ws : nullptr;
+  a.ws_ml = need ? reinterpret_cast<float2*>(ws + o_floats) : nullptr;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = dims->num_q_heads;
+  a.num_kv_heads = dims->num_kv_heads;
+  a.num_blocks = num_blocks;
+  a.max_blocks = max_blocks;
+  a.max_context_len = max_context_len;
+  a.partition_tokens = P;
+  a.max_parts = max_parts;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status;
+  return pa::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                 : PA_ERR_CUDA;
+}
+
+int pa_get_device_status(void* stream, uint32_t* flags) {
+  unsigned* status = nullptr;
+  if (const int rc = status_word(&status)) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned host = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaMemcpy(&host, status, sizeof host, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaMemset(status, 0, sizeof host) != cudaSuccess) return PA_ERR_CUDA;
+  if (flags) *flags = host;
+  if (host & PA_FLAG_TIMEOUT) return PA_ERR_TIMEOUT;
+  if (host) return PA_ERR_DEVICE_OOB;
+  return PA_OK;
+}
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_NULL: return "PA_ERR_NULL: a required pointer is NULL";
+    case PA_ERR_SHAPE: return "PA_ERR_SHAPE: unsupported head_dim, block_size or head counts";
+    case PA_ERR_RANGE: return "PA_ERR_RANGE: a count or length is out of range";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: a CUDA runtime call failed";
+    case PA_ERR_DEVICE_OOB: return "PA_ERR_DEVICE_OOB: a kernel met an out-of-range value";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a kernel gave up a bounded wait";
+    case PA_ERR_ALIGN: return "PA_ERR_ALIGN: a pointer is not 16-byte aligned";
+    default: return "unknown pa status";
+  }
+}
+
+}  // extern "C"

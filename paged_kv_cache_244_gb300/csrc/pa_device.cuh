@@ -1,0 +1,110 @@
+// Device helpers shared by the sm_103a kernels: inline PTX for mbarriers, bulk copies into
+// shared memory, programmatic dependent launch, the bounded wait and the status flags.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "pa.h"
+
+namespace pa {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlockSize = 16;
+constexpr int kTileBytes = kBlockSize * kHeadDim * 2;  // one (block, KV head) tile: 4 KiB
+constexpr unsigned kFullMask = 0xffffffffu;
+// A wait on a copy into shared memory gives up after this long (ns of %globaltimer) and
+// raises PA_FLAG_TIMEOUT instead of hanging the GPU.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ void raise_flag(unsigned* status, unsigned flag) {
+  atomicOr(status, flag);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- programmatic dependent launch --------------------------------------------------
+// Block until the grid this one depends on has completed and its writes are visible.
+__device__ __forceinline__ void pdl_wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allow the next grid on the stream to be scheduled (it still waits for our completion).
+__device__ __forceinline__ void pdl_allow_next_grid() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- mbarrier ------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Arrive once and announce `bytes` of incoming asynchronous copies on this phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait for phase `parity` of the barrier to complete, for at most kWaitLimitNs.
+// Returns false on timeout (the caller raises PA_FLAG_TIMEOUT and stops using the stage).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ---- bulk asynchronous copy global -> shared (no tensor map) -------------------------
+// `bytes` must be a multiple of 16 and both addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst_smem, const void* src_gmem,
+                                              uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst_smem), "l"(src_gmem), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Order this thread's earlier generic-proxy accesses to shared memory before later
+// async-proxy (bulk copy) writes to it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- bf16 ------------------------------------------------------------------------------
+// Widen a packed pair of bf16 (low half = element 0) to two floats: bf16 is the top half
+// of an fp32 bit pattern.
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Round two floats to bf16 (nearest even) and pack them, a in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+}  // namespace pa

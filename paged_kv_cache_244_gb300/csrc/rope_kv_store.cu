@@ -1,0 +1,88 @@
+// Fused RoPE + KV-cache store for sm_103a.
+//
+// "Pico-vLLM：从零手写的工业级LLM推理引擎实现", §1 模型实现层 (RoPE with rotate_half, in
+// place) and §2 Kernel层 (fused RoPE + KV cache store); "从零实现 LLM 推理引擎：深挖 vLLM 的
+// 六大核心优化", §3.1 (16-token blocks) and §3.2 (append_slot: one new slot per sequence).
+//
+// One warp per (token, head).  Warps for query heads rotate q in place; warps for KV heads
+// rotate k into its cache slot and copy v next to it.  Lane l owns the rotation pairs
+// (2l, 2l+64) and (2l+1, 2l+65): two 32-bit loads of bf16 pairs, two float2 loads of the
+// cos/sin row, two 32-bit stores, so each head vector moves as one 256-byte line.
+// Launch-bound (a few KiB per token): no shared memory, no staging.
+
+#include "pa_device.cuh"
+#include "pa_launch.h"
+
+namespace pa {
+namespace {
+
+constexpr int kRopeWarps = 8;
+
+__global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_store_kernel(const RopeArgs a) {
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+  const int lane = threadIdx.x & 31;
+  const int warp = blockIdx.x * kRopeWarps + (threadIdx.x >> 5);
+  const int heads = a.num_q_heads + a.num_kv_heads;
+  if (warp >= a.num_tokens * heads) return;
+  const int t = warp / heads;
+  const int h = warp - t * heads;
+
+  const int pos = a.positions[t];
+  if (pos < 0 || pos >= a.max_pos) {
+    if (lane == 0) raise_flag(a.status, PA_FLAG_POSITION_OOB);
+    return;
+  }
+  const uint32_t* src;
+  uint32_t* dst;
+  if (h < a.num_q_heads) {
+    dst = reinterpret_cast<uint32_t*>(a.q + (static_cast<size_t>(t) * a.num_q_heads + h) * kHeadDim);
+    src = dst;
+  } else {
+    const int g = h - a.num_q_heads;
+    const int64_t slot = a.slot_mapping[t];
+    if (slot < 0) return;  // padding token: nothing to store
+    if (slot >= static_cast<int64_t>(a.num_blocks) * kBlockSize) {
+      if (lane == 0) raise_flag(a.status, PA_FLAG_SLOT_OOB);
+      return;
+    }
+    const int64_t blk = slot / kBlockSize;
+    const int off = static_cast<int>(slot - blk * kBlockSize);
+    const size_t in_off = (static_cast<size_t>(t) * a.num_kv_heads + g) * kHeadDim;
+    const size_t cache_off = ((static_cast<size_t>(blk) * a.num_kv_heads + g) * kBlockSize + off) * kHeadDim;
+    src = reinterpret_cast<const uint32_t*>(a.k + in_off);
+    dst = reinterpret_cast<uint32_t*>(a.k_cache + cache_off);
+    reinterpret_cast<uint2*>(a.v_cache + cache_off)[lane] =
+        reinterpret_cast<const uint2*>(a.v + in_off)[lane];
+  }
+  const float* row = a.cos_sin + static_cast<size_t>(pos) * kHeadDim;
+  const float2 c = reinterpret_cast<const float2*>(row)[lane];        // cos of pairs 2l, 2l+1
+  const float2 s = reinterpret_cast<const float2*>(row + 64)[lane];   // sin of pairs 2l, 2l+1
+  const uint32_t lo = src[lane];        // x[2l], x[2l+1]
+  const uint32_t hi = src[32 + lane];   // x[2l+64], x[2l+65]
+  const float x0 = bf16lo(lo), x1 = bf16hi(lo), y0 = bf16lo(hi), y1 = bf16hi(hi);
+  const float r0 = __fmaf_rn(x0, c.x, -__fmul_rn(y0, s.x));
+  const float r1 = __fmaf_rn(x1, c.y, -__fmul_rn(y1, s.y));
+  const float r2 = __fmaf_rn(y0, c.x, __fmul_rn(x0, s.x));
+  const float r3 = __fmaf_rn(y1, c.y, __fmul_rn(x1, s.y));
+  dst[lane] = pack_bf16x2(r0, r1);
+  dst[32 + lane] = pack_bf16x2(r2, r3);
+}
+
+}  // namespace
+
+cudaError_t launch_rope_kv_store(const RopeArgs& a, cudaStream_t stream) {
+  const long long warps = static_cast<long long>(a.num_tokens) * (a.num_q_heads + a.num_kv_heads);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((warps + kRopeWarps - 1) / kRopeWarps));
+  cfg.blockDim = dim3(kRopeWarps * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, rope_kv_store_kernel, a);
+}
+
+}  // namespace pa

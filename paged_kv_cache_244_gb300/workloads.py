@@ -143,6 +143,14 @@ class Workload:
     meta: dict = field(default_factory=dict)
 
     @property
+    def num_q_heads(self) -> int:
+        return int(self.q.shape[2])
+
+    @property
+    def num_kv_heads(self) -> int:
+        return int(self.k_cache.shape[2])
+
+    @property
     def num_seqs(self) -> int:
         return int(self.context_lens.shape[0])
 
@@ -160,7 +168,7 @@ class Workload:
 
     def kv_bytes_per_layer(self) -> int:
         """K and V bytes one decode pass reads per layer: sum(ctx) * Hkv * D * 2 B * 2."""
-        return int(self.context_lens.astype(np.int64).sum()) * NUM_KV_HEADS * HEAD_DIM * 2 * 2
+        return int(self.context_lens.astype(np.int64).sum()) * self.num_kv_heads * HEAD_DIM * 2 * 2
 
     def unique_kv_bytes_per_layer(self) -> int:
         """Bytes of distinct (physical block, token) slots read, for shared-prefix tables."""
@@ -175,7 +183,7 @@ class Workload:
                     continue
                 seen.add(blk)
                 total += n
-        return total * NUM_KV_HEADS * HEAD_DIM * 2 * 2
+        return total * self.num_kv_heads * HEAD_DIM * 2 * 2
 
 
 def _slots_for(block_tables, positions):
@@ -185,7 +193,8 @@ def _slots_for(block_tables, positions):
 
 def build(name: str, context_lens, num_blocks: int, seed: int, *, sigma: float = 1.0,
           num_layers: int = 1, shared_prefix_blocks: int = 0, partition_tokens: int = 0,
-          max_blocks: int | None = None, canary: int = BF16_NAN) -> Workload:
+          max_blocks: int | None = None, canary: int = BF16_NAN,
+          num_q_heads: int = NUM_Q_HEADS, num_kv_heads: int = NUM_KV_HEADS) -> Workload:
     """General builder.
 
     Block allocation: one seeded shuffle of the pool's ids; the first `shared_prefix_blocks`
@@ -221,30 +230,31 @@ def build(name: str, context_lens, num_blocks: int, seed: int, *, sigma: float =
     cos_sin = rope_cos_sin_table(max_pos)
 
     L = num_layers
-    shape_cache = (L, num_blocks, NUM_KV_HEADS, BLOCK_SIZE, HEAD_DIM)
+    Hq, Hkv = num_q_heads, num_kv_heads
+    shape_cache = (L, num_blocks, Hkv, BLOCK_SIZE, HEAD_DIM)
     k_cache = np.full(shape_cache, canary, np.uint16)
     v_cache = np.full(shape_cache, canary, np.uint16)
-    tile = NUM_KV_HEADS * BLOCK_SIZE * HEAD_DIM
+    tile = Hkv * BLOCK_SIZE * HEAD_DIM
     for layer in range(L):
         for cache in (k_cache, v_cache):
             if shared_prefix_blocks:
                 ids = pool[:shared_prefix_blocks]
                 cache[layer, ids] = rng.normal_bf16(ids.shape[0] * tile, sigma).reshape(
-                    ids.shape[0], NUM_KV_HEADS, BLOCK_SIZE, HEAD_DIM)
+                    ids.shape[0], Hkv, BLOCK_SIZE, HEAD_DIM)
             for s in range(S):
                 ids = bt[s, shared_prefix_blocks:nblk[s]].astype(np.int64)
                 if ids.shape[0] == 0:
                     continue
                 cache[layer, ids] = rng.normal_bf16(ids.shape[0] * tile, sigma).reshape(
-                    ids.shape[0], NUM_KV_HEADS, BLOCK_SIZE, HEAD_DIM)
+                    ids.shape[0], Hkv, BLOCK_SIZE, HEAD_DIM)
                 # The new token's slot and everything after it in the last block are not
                 # past tokens: they keep the canary.
                 last = int(bt[s, nblk[s] - 1])
                 first_free = int(positions[s]) % BLOCK_SIZE
                 cache[layer, last, :, first_free:, :] = canary
-    q = rng.normal_bf16(L * S * NUM_Q_HEADS * HEAD_DIM, sigma).reshape(L, S, NUM_Q_HEADS, HEAD_DIM)
-    k = rng.normal_bf16(L * S * NUM_KV_HEADS * HEAD_DIM, sigma).reshape(L, S, NUM_KV_HEADS, HEAD_DIM)
-    v = rng.normal_bf16(L * S * NUM_KV_HEADS * HEAD_DIM, sigma).reshape(L, S, NUM_KV_HEADS, HEAD_DIM)
+    q = rng.normal_bf16(L * S * Hq * HEAD_DIM, sigma).reshape(L, S, Hq, HEAD_DIM)
+    k = rng.normal_bf16(L * S * Hkv * HEAD_DIM, sigma).reshape(L, S, Hkv, HEAD_DIM)
+    v = rng.normal_bf16(L * S * Hkv * HEAD_DIM, sigma).reshape(L, S, Hkv, HEAD_DIM)
     return Workload(name=name, num_layers=L, context_lens=ctx, block_tables=bt,
                     num_blocks=num_blocks, q=q, k=k, v=v, positions=positions,
                     slot_mapping=slots.astype(np.int64), cos_sin=cos_sin, k_cache=k_cache,

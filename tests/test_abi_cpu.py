@@ -1,0 +1,123 @@
+"""The C ABI library on a machine without a GPU: it loads, exports every declared entry
+point, and rejects bad arguments before touching the device (no compute calls here)."""
+
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from paged_kv_cache_244_gb300 import _build
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def L():
+    from paged_kv_cache_244_gb300 import binding
+    _build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    names = []
+    for header in sorted((ROOT / "include").glob("*.h")):
+        text = re.sub(r"/\*.*?\*/", "", header.read_text(), flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w ]*?\**\s*\**(pa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("pa_rope_kv_store", "pa_decode", "pa_decode_workspace_size",
+                 "pa_decode_partition_tokens", "pa_get_device_status", "pa_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in include/ but not exported"
+
+
+def dims(hq=12, hkv=2, d=128, b=16):
+    from paged_kv_cache_244_gb300 import binding
+    return binding.make_dims(hq, hkv, d, b)
+
+
+P = ctypes.c_void_p
+OK_PTR = P(0x10000)        # 16-byte aligned stand-in pointers: never dereferenced on error paths
+MIS_PTR = P(0x10008)
+
+
+def decode_call(L, d=None, S=2, q=OK_PTR, kc=OK_PTR, vc=OK_PTR, nb=16, bt=OK_PTR, maxb=4,
+                ctx=OK_PTR, maxctx=40, scale=0.088, part=0, ws=OK_PTR, wsb=1 << 30, out=OK_PTR):
+    d = dims() if d is None else d
+    return L.pa_decode(ctypes.byref(d) if d is not False else None, S, q, kc, vc, nb, bt, maxb,
+                       ctx, maxctx, scale, part, ws, wsb, out, None)
+
+
+def test_decode_rejects_bad_arguments_on_the_host(L):
+    from paged_kv_cache_244_gb300 import binding as b
+    assert decode_call(L, d=False) == b.PA_ERR_NULL
+    assert decode_call(L, d=dims(d=64)) == b.PA_ERR_SHAPE
+    assert decode_call(L, d=dims(b=32)) == b.PA_ERR_SHAPE
+    assert decode_call(L, d=dims(hq=12, hkv=5)) == b.PA_ERR_SHAPE
+    assert decode_call(L, d=dims(hq=18, hkv=2)) == b.PA_ERR_SHAPE      # group of 9 > 8
+    assert decode_call(L, S=-1) == b.PA_ERR_RANGE
+    assert decode_call(L, S=0) == b.PA_OK                              # no-op
+    for kw in ("q", "kc", "vc", "bt", "ctx", "out"):
+        assert decode_call(L, **{kw: None}) == b.PA_ERR_NULL, kw
+    assert decode_call(L, maxctx=0) == b.PA_ERR_RANGE
+    assert decode_call(L, maxctx=65, maxb=4) == b.PA_ERR_RANGE         # > max_blocks * 16
+    assert decode_call(L, part=24) == b.PA_ERR_RANGE                   # not a multiple of 16
+    assert decode_call(L, scale=0.0) == b.PA_ERR_RANGE
+    assert decode_call(L, scale=float("nan")) == b.PA_ERR_RANGE
+    assert decode_call(L, maxctx=40, maxb=4, part=16, wsb=100) == b.PA_ERR_WORKSPACE
+    assert decode_call(L, maxctx=40, maxb=4, part=16, ws=None) == b.PA_ERR_WORKSPACE
+    for kw in ("q", "kc", "vc", "bt", "ctx", "out"):
+        assert decode_call(L, **{kw: MIS_PTR}) == b.PA_ERR_ALIGN, kw
+
+
+def test_rope_kv_store_rejects_bad_arguments_on_the_host(L):
+    from paged_kv_cache_244_gb300 import binding as b
+
+    def call(d=None, T=3, maxpos=64, nb=16, **ptrs):
+        args = dict(q=OK_PTR, k=OK_PTR, v=OK_PTR, pos=OK_PTR, cs=OK_PTR, slot=OK_PTR,
+                    kc=OK_PTR, vc=OK_PTR)
+        args.update(ptrs)
+        d = dims() if d is None else d
+        return L.pa_rope_kv_store(ctypes.byref(d), T, args["q"], args["k"], args["v"], args["pos"],
+                                  args["cs"], maxpos, args["slot"], args["kc"], args["vc"], nb, None)
+
+    assert call(d=dims(d=96)) == b.PA_ERR_SHAPE
+    assert call(T=-1) == b.PA_ERR_RANGE
+    assert call(T=0) == b.PA_OK
+    for kw in ("q", "k", "v", "pos", "cs", "slot", "kc", "vc"):
+        assert call(**{kw: None}) == b.PA_ERR_NULL, kw
+        assert call(**{kw: MIS_PTR}) == b.PA_ERR_ALIGN, kw
+    assert call(maxpos=0) == b.PA_ERR_RANGE
+    assert call(nb=0) == b.PA_ERR_RANGE
+
+
+def test_partition_choice_and_workspace_size(L):
+    from paged_kv_cache_244_gb300 import binding as b
+    # auto: smallest power-of-two multiple of 16 with S * Hkv * ceil(ctx / P) <= 2048
+    assert b.decode_partition_tokens(12, 2, 2, 40) == 16
+    assert b.decode_partition_tokens(12, 2, 1, 2048) == 16
+    assert b.decode_partition_tokens(12, 2, 64, 4096) == 256
+    assert b.decode_partition_tokens(12, 2, 32, 2064) == 128
+    assert b.decode_partition_tokens(12, 2, 4, 32768) == 128
+    assert b.decode_partition_tokens(12, 2, 4, 32768, 512) == 512
+    with pytest.raises(b.PaError):
+        b.decode_partition_tokens(12, 2, 4, 32768, 100)
+    # workspace: S * Hq * parts * (D + 2) floats, 0 when one partition covers the context
+    assert b.decode_workspace_size(12, 2, 4, 32768, 512) == 4 * 12 * 64 * 130 * 4
+    assert b.decode_workspace_size(12, 2, 2, 40, 64) == 0
+    assert b.decode_workspace_size(12, 2, 2, 40) == 2 * 12 * 3 * 130 * 4
+
+
+def test_status_strings(L):
+    from paged_kv_cache_244_gb300 import binding as b
+    for code in range(0, -9, -1):
+        assert b.status_string(code).startswith("PA_")
+    assert b.status_string(7) == "unknown pa status"
