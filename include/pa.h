@@ -38,7 +38,8 @@
  *    returns PA_ERR_SHAPE.
  *  - Memory: every pointer is device memory owned by the caller (cudaMalloc, PyTorch, ...)
  *    and must be 16-byte aligned (PA_ERR_ALIGN otherwise).  The library allocates nothing.
- *    Its only global state is one 32-bit device status word per GPU.
+ *    Its only global state is one 32-bit device status word per GPU, and the fixed scratch
+ *    array of pa_decode_static_workspace (PA_STATIC_WORKSPACE_BYTES per GPU).
  *  - Asynchrony: calls enqueue work on `stream` and return at once.  Arguments the host can
  *    check are checked before anything is enqueued; on error nothing is launched.
  *  - Values only the device can see (block ids, positions, slots, per-sequence lengths) are
@@ -181,6 +182,36 @@ int pa_get_device_status(void* stream, uint32_t* flags);
 
 /* Human-readable name of a PA_* return code (static storage, never NULL). */
 const char* pa_status_string(int status);
+
+/*
+ * pa_decode_static_workspace -- pa_decode for callers that cannot allocate device memory.
+ *
+ * No counterpart in the source pages: this entry point exists for callers that may not call
+ * cudaMalloc or any allocator while a decode step runs -- for example an engine that has
+ * already handed all free HBM to its KV-cache pool, a plugin whose enqueue function is not
+ * allowed to allocate, or a real-time loop that must not take the allocator's locks.  It
+ * takes the same arguments as pa_decode minus the workspace, and uses instead a scratch
+ * array of PA_STATIC_WORKSPACE_BYTES that lives in the library itself (a file-scope
+ * __device__ array): every GPU that loads the library holds that much device memory until
+ * the process exits.  Neither this call nor anything it calls allocates.
+ *
+ *  - Limit: when pa_decode_workspace_size() for these arguments exceeds
+ *    PA_STATIC_WORKSPACE_BYTES the call returns PA_ERR_WORKSPACE and launches nothing
+ *    (use a larger partition_tokens, fewer sequences, or pa_decode with your own workspace).
+ *  - The scratch needs no clearing: each call writes every partial it later reads.
+ *  - All calls on a GPU share the one array and it keeps the last call's contents: two calls
+ *    whose kernels overlap on that GPU (different streams, no ordering between them) race on
+ *    it and give wrong results.  Order such calls on one stream or with events.
+ *  - The first call on each device looks up the array's device address (once per device,
+ *    with that device current); make that first call before any stream capture.
+ * Returns PA_OK or a PA_ERR_* code, with the same meaning as for pa_decode.
+ */
+#define PA_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)
+int pa_decode_static_workspace(const pa_dims* dims, int num_seqs, const void* q,
+                               const void* k_cache, const void* v_cache, int num_blocks,
+                               const int32_t* block_tables, int max_blocks,
+                               const int32_t* context_lens, int max_context_len, float scale,
+                               int partition_tokens, void* out, void* stream);
 
 #ifdef __cplusplus
 }
