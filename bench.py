@@ -5,8 +5,9 @@
 A step is one pass of the whole hot path over one batch: pa_rope_kv_store of every
 sequence's new token, then pa_decode over every cached context, for each layer of the
 workload.  The metric is KV-cache bytes read per second: sum(context_lens) * Hkv * D * 2 B
-(K and V) per layer per step, over the step's device time.  L2 is flushed (a 512 MiB write)
-between timed steps, outside the timed events, because the workloads' caches fit in L2.
+(K and V) per layer per step, over the step's device time.  L2 is flushed between timed steps,
+outside the timed events, because the workloads' caches fit in L2: a 512 MiB write, then a
+read of the same buffer so that no dirty flush lines are written back inside the timed step.
 
 The printed JSON line carries:
   value / ms_per_step  from CUDA events around each step, inputs resident in HBM;
@@ -145,8 +146,8 @@ class DeviceStep:
         self.P = binding.decode_partition_tokens(w.num_q_heads, w.num_kv_heads, w.num_seqs,
                                                  w.max_context_len, w.partition_tokens)
         self.workspace = binding.decode_workspace(self.q[0], self.k_cache[0], w.max_context_len, self.P)
-        self.max_parts = -(-w.max_context_len // self.P)
-        self.launches_per_step = L * (1 + 1 + (1 if self.max_parts > 1 else 0))
+        # per layer: the RoPE + store kernel, the decode kernel and the merge kernel
+        self.launches_per_step = L * 3
 
     def rope_store(self, i):
         self.pa.rope_kv_store(self.q[i], self.k[i], self.v[i], self.positions, self.cos_sin,
@@ -177,9 +178,19 @@ def run_gpu(args, rank, world, dist):
         dist.barrier()
     base = W.make(args.workload)
     w = base if rank == 0 else W.make(args.workload, seed=base.seed + 1000 * rank)
+    if args.partition_tokens is not None:
+        w.partition_tokens = args.partition_tokens
     st = DeviceStep(w, torch, binding)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    sink = torch.empty(1, dtype=torch.float32, device="cuda")
+
+    def flush_l2():
+        # Write a buffer larger than L2, then read it back: the write evicts the inputs, the
+        # read evicts the written (dirty) lines so that their write-back is not billed to
+        # the timed step.
+        flush.fill_(1.0)
+        torch.sum(flush.view(1, -1), dim=1, out=sink)
     bytes_step = w.kv_bytes_per_layer() * w.num_layers
 
     def barrier():
@@ -191,7 +202,7 @@ def run_gpu(args, rank, world, dist):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(steps)]
         for a, b in evs:
-            flush.fill_(1)
+            flush_l2()
             a.record(stream)
             fn()
             b.record(stream)
@@ -224,7 +235,7 @@ def run_gpu(args, rank, world, dist):
     rope_ms = timed_loop(lambda: st.rope_store(0), max(3, args.steps // 4))
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, st, torch, binding, flush)
+    e2e = run_e2e(args, st, torch, binding, flush_l2)
 
     rc, flags = binding.get_device_status()
     if rc != 0:
@@ -286,7 +297,7 @@ def run_gpu(args, rank, world, dist):
     return line
 
 
-def run_e2e(args, st, torch, binding, flush):
+def run_e2e(args, st, torch, binding, flush_l2):
     """Every step: pinned host -> device copies of the step's inputs, the C-ABI calls, and
     the device -> host read of the attention output, all between the CUDA events."""
     w = st.w
@@ -323,7 +334,7 @@ def run_e2e(args, st, torch, binding, flush):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     for a, b in evs:
-        flush.fill_(1)
+        flush_l2()
         a.record(stream)
         one()
         b.record(stream)
@@ -345,7 +356,7 @@ def config_of(w, st, world):
         "pool_blocks": w.num_blocks,
         "partition_tokens": st.P if st is not None else w.partition_tokens,
         "kv_bytes_per_step_per_gpu": w.kv_bytes_per_layer() * w.num_layers,
-        "l2": "flushed between timed steps (512 MiB write, outside the events)",
+        "l2": "flushed between timed steps (512 MiB write then read back, outside the events)",
         "parallelism": f"replicas x{world} (independent batches)",
     }
     if w.meta.get("shared_prefix_blocks"):
@@ -437,6 +448,8 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--partition-tokens", type=int, default=None,
+                    help="Flash-Decode partition size (default: the workload's, 0 = library choice)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes read+written per pa_decode call from an ncu capture")
     args = ap.parse_args()

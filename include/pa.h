@@ -119,20 +119,24 @@ int pa_rope_kv_store(const pa_dims* dims, int num_tokens, void* q, const void* k
                      void* stream);
 
 /*
- * pa_decode_partition_tokens -- the context partition size pa_decode will use (Flash Decode,
- * [PV] §H200上的详细对比).  `partition_tokens` > 0 is used as given (it must be a multiple
- * of block_size); 0 asks the library to choose: the smallest power-of-two multiple of
- * block_size for which num_seqs * num_kv_heads * ceil(max_context_len / P) <= 2048.
- * Returns P >= block_size, or a negative PA_ERR_* code.
+ * pa_decode_partition_tokens -- validate a partition request for pa_decode (Flash Decode,
+ * [PV] §H200上的详细对比).  pa_decode lays the (sequence, KV head, block) jobs of the batch
+ * on one axis and cuts it into contiguous ranges, one warp of its persistent grid at a time:
+ * `partition_tokens` == 0 cuts the axis into equal ranges, one per warp (every warp gets the
+ * same number of blocks +-1); > 0 cuts it every partition_tokens / block_size blocks.  Where a
+ * range boundary falls inside a sequence, that sequence's pieces are merged by a second
+ * kernel.  Returns the request (0 or a positive multiple of block_size) or a negative
+ * PA_ERR_* code (PA_ERR_RANGE also for num_seqs > 8192 or max_context_len < 1).
  */
 int pa_decode_partition_tokens(const pa_dims* dims, int num_seqs, int max_context_len,
                                int partition_tokens);
 
 /*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for these
- * arguments: num_seqs * Hq * ceil(max_context_len / P) * (D + 2) * 4 when the context is
- * split into more than one partition, else 0.  Returns 0 for invalid arguments (pa_decode
- * then reports the error).
+ * arguments: (R + num_seqs * Hkv) * (Hq / Hkv) * (D + 2) * 4, where R bounds the number of
+ * ranges: min(2048, J) for partition_tokens == 0, ceil(J / (partition_tokens / 16)) otherwise,
+ * with J = num_seqs * Hkv * ceil(max_context_len / 16).  Returns 0 for invalid arguments
+ * (pa_decode then reports the error).
  */
 size_t pa_decode_workspace_size(const pa_dims* dims, int num_seqs, int max_context_len,
                                 int partition_tokens);
@@ -146,25 +150,26 @@ size_t pa_decode_workspace_size(const pa_dims* dims, int num_seqs, int max_conte
  *   K_t = k_cache[block_tables[s][t / 16]][g][t % 16],  V_t likewise,
  *   out[s][h] = sum_t softmax_t(scale * q[s][h] . K_t) V_t      (bf16 RNE of the fp32 result)
  * Table entries past ceil(n / 16) and cache slots past n are never read.  n == 0 gives an
- * all-zero output row.  When ceil(max_context_len / P) > 1 the context is processed in
- * partitions of P tokens whose partial (max, sum, weighted V) are merged by a second kernel;
+ * all-zero output row.  The work is split as pa_decode_partition_tokens describes; pieces
+ * of a split sequence give partial (max, sum, weighted V) that a second kernel merges, and
  * the result is the same softmax up to fp32 rounding order.
  * Device-side errors: a block id outside [0, num_blocks) -> that block is skipped,
  * PA_FLAG_BLOCK_ID_OOB; n outside [0, max_context_len] -> clamped, PA_FLAG_CONTEXT_LEN_OOB.
  *
- *   num_seqs          S >= 0 (0 is a no-op)
+ *   num_seqs          0 <= S <= 8192 (0 is a no-op)
  *   q                 [S][Hq][D] bf16 (already rotated), read only
  *   k_cache, v_cache  [num_blocks][Hkv][16][D] bf16, read only
  *   block_tables      [S][max_blocks] int32
  *   context_lens      [S] int32 (device copy)
  *   max_context_len   host-side upper bound of context_lens, 1 <= it <= max_blocks * 16
  *   scale             softmax scale, finite and > 0 (1/sqrt(D) for standard attention)
- *   partition_tokens  0 (library chooses) or a positive multiple of 16
- *   workspace         device memory of >= pa_decode_workspace_size(...) bytes, or NULL
- *                     when that size is 0; its contents need no initialisation
+ *   partition_tokens  0 (even split over the grid) or a positive multiple of 16
+ *   workspace         device memory of >= pa_decode_workspace_size(...) bytes, 16-byte
+ *                     aligned; its contents need no initialisation.  Two calls whose kernels
+ *                     overlap on the GPU must not share a workspace.
  *   out               [S][Hq][D] bf16, written
  * Returns PA_OK or a PA_ERR_* code (nothing launched on error).  Launches one kernel, plus
- * one merge kernel when the context is split.
+ * one merge kernel.
  */
 int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_cache,
               const void* v_cache, int num_blocks, const int32_t* block_tables, int max_blocks,

@@ -144,13 +144,13 @@ def decode_workspace_size(num_q_heads, num_kv_heads, num_seqs, max_context_len,
                                               partition_tokens))
 
 
-def decode_workspace(q, k_cache, max_context_len, partition_tokens=0) -> torch.Tensor | None:
-    """Allocate the workspace pa_decode needs for these shapes (None when it needs none)."""
+def decode_workspace(q, k_cache, max_context_len, partition_tokens=0) -> torch.Tensor:
+    """Allocate the workspace pa_decode needs for these shapes (no initialisation needed)."""
     S, Hq, D = q.shape
     _, Hkv, B, _ = k_cache.shape
     n = decode_workspace_size(Hq, Hkv, S, max_context_len, partition_tokens, D, B)
     if n == 0:
-        return None
+        raise PaError(PA_ERR_RANGE, "pa_decode_workspace_size")
     return torch.empty((n + 3) // 4, dtype=torch.float32, device=q.device)
 
 
@@ -160,7 +160,7 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len, sca
 
     q [S, Hq, D] bf16; k_cache, v_cache [num_blocks, Hkv, B, D] bf16; block_tables
     [S, max_blocks] int32; context_lens [S] int32; max_context_len a host int bounding them.
-    `workspace` (float32, from decode_workspace) is allocated here when None and needed.
+    `workspace` (from decode_workspace) is allocated here when None.
     """
     S, Hq, D = q.shape
     nb, Hkv, B, D2 = k_cache.shape

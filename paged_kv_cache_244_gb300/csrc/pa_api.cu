@@ -1,8 +1,7 @@
 // C ABI of the paged decode attention library (declared in include/pa.h).
 //
-// Host side only: argument checks that need no device access, choice of the Flash-Decode
-// partition size, workspace carving, the device status word, and the kernel launches.
-// Nothing here allocates device memory.
+// Host side only: argument checks that need no device access, workspace sizing and carving,
+// the device status word, and the kernel launches.  Nothing here allocates device memory.
 
 #include <cmath>
 #include <cstdint>
@@ -19,7 +18,6 @@ namespace {
 __device__ unsigned int g_pa_status;
 
 constexpr int kMaxDevices = 64;
-constexpr int kTargetUnits = 2048;  // auto partition size: at most this many (seq, kv, part)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -33,24 +31,29 @@ int check_dims(const pa_dims* d) {
   return PA_OK;
 }
 
-// Resolve the partition size; negative = error.
-int resolve_partition(const pa_dims* d, int num_seqs, int max_context_len, int requested) {
+// Validate a partition request: 0 (even split over the warps) or a positive multiple of the
+// block size.  Returns it, or a negative PA_ERR_* code.
+int check_partition(const pa_dims* d, int num_seqs, int max_context_len, int requested) {
   if (const int rc = check_dims(d)) return rc;
-  if (num_seqs < 0 || max_context_len < 1) return PA_ERR_RANGE;
+  if (num_seqs < 0 || num_seqs > pa::kMaxDecodeSeqs || max_context_len < 1) return PA_ERR_RANGE;
   if (requested < 0 || requested % d->block_size != 0) return PA_ERR_RANGE;
-  if (requested > 0) return requested;
-  long long P = d->block_size;
-  const long long pairs = static_cast<long long>(num_seqs) * d->num_kv_heads;
-  while (P < max_context_len && pairs * ((max_context_len + P - 1) / P) > kTargetUnits) P *= 2;
-  return static_cast<int>(P);
+  return requested;
 }
 
-int max_parts_for(int max_context_len, int P) { return (max_context_len + P - 1) / P; }
-
-size_t workspace_bytes_for(const pa_dims* d, int num_seqs, int max_parts) {
-  if (max_parts <= 1) return 0;
-  return static_cast<size_t>(num_seqs) * d->num_q_heads * max_parts *
-         (static_cast<size_t>(d->head_dim) + 2) * sizeof(float);
+// Partial rows: G per piece, one piece per (range, segment) pair that meets, so at most
+// (#ranges + #segments) pieces.  Each row is D partial sums plus a (max, sum) pair.
+size_t workspace_bytes_for(const pa_dims* d, int num_seqs, int max_context_len, int partition_tokens) {
+  const long long segs = static_cast<long long>(num_seqs) * d->num_kv_heads;
+  const long long jobs = segs * ((max_context_len + d->block_size - 1) / d->block_size);
+  long long ranges;
+  if (partition_tokens > 0) {
+    const long long chunk = partition_tokens / d->block_size;
+    ranges = (jobs + chunk - 1) / chunk;
+  } else {
+    ranges = jobs < pa::kMaxDecodeWarps ? jobs : pa::kMaxDecodeWarps;
+  }
+  const long long rows = (ranges + segs) * (d->num_q_heads / d->num_kv_heads);
+  return static_cast<size_t>(rows) * (static_cast<size_t>(d->head_dim) + 2) * sizeof(float);
 }
 
 // Device address of this GPU's status word (looked up once per device).
@@ -110,14 +113,14 @@ int pa_rope_kv_store(const pa_dims* dims, int num_tokens, void* q, const void* k
 
 int pa_decode_partition_tokens(const pa_dims* dims, int num_seqs, int max_context_len,
                                int partition_tokens) {
-  return resolve_partition(dims, num_seqs, max_context_len, partition_tokens);
+  return check_partition(dims, num_seqs, max_context_len, partition_tokens);
 }
 
 size_t pa_decode_workspace_size(const pa_dims* dims, int num_seqs, int max_context_len,
                                 int partition_tokens) {
-  const int P = resolve_partition(dims, num_seqs, max_context_len, partition_tokens);
-  if (P <= 0) return 0;
-  return workspace_bytes_for(dims, num_seqs, max_parts_for(max_context_len, P));
+  const int P = check_partition(dims, num_seqs, max_context_len, partition_tokens);
+  if (P < 0 || num_seqs == 0) return 0;
+  return workspace_bytes_for(dims, num_seqs, max_context_len, P);
 }
 
 int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_cache,
@@ -126,7 +129,7 @@ int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_ca
               int partition_tokens, void* workspace, size_t workspace_bytes, void* out,
               void* stream) {
   if (const int rc = check_dims(dims)) return rc;
-  if (num_seqs < 0) return PA_ERR_RANGE;
+  if (num_seqs < 0 || num_seqs > pa::kMaxDecodeSeqs) return PA_ERR_RANGE;
   if (num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
   if (num_blocks < 1 || max_blocks < 1 || max_context_len < 1) return PA_ERR_RANGE;
@@ -135,15 +138,13 @@ int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_ca
   if (static_cast<long long>(num_blocks) * dims->num_kv_heads * dims->block_size > (1ll << 31))
     return PA_ERR_RANGE;
   if (!(scale > 0.f) || !std::isfinite(scale)) return PA_ERR_RANGE;
-  const int P = resolve_partition(dims, num_seqs, max_context_len, partition_tokens);
+  const int P = check_partition(dims, num_seqs, max_context_len, partition_tokens);
   if (P < 0) return P;
-  const int max_parts = max_parts_for(max_context_len, P);
-  const size_t need = workspace_bytes_for(dims, num_seqs, max_parts);
-  if (need > 0 && (!workspace || workspace_bytes < need)) return PA_ERR_WORKSPACE;
-  const void* ptrs[] = {q, k_cache, v_cache, block_tables, context_lens, out};
+  const size_t need = workspace_bytes_for(dims, num_seqs, max_context_len, P);
+  if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+  const void* ptrs[] = {q, k_cache, v_cache, block_tables, context_lens, out, workspace};
   for (const void* p : ptrs)
     if (!aligned16(p)) return PA_ERR_ALIGN;
-  if (need > 0 && !aligned16(workspace)) return PA_ERR_ALIGN;
   unsigned* status = nullptr;
   if (const int rc = status_word(&status)) return rc;
 
@@ -154,18 +155,19 @@ int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_ca
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   a.out = static_cast<__nv_bfloat16*>(out);
+  // [rows][D] partial sums, then [rows] (max, sum) pairs; rows = need / ((D + 2) * 4).
   float* ws = static_cast<float*>(workspace);
-  const size_t o_floats = static_cast<size_t>(num_seqs) * dims->num_q_heads * max_parts * dims->head_dim;
-  a.ws_o = need ? ws : nullptr;
-  a.ws_ml = need ? reinterpret_cast<float2*>(ws + o_floats) : nullptr;
+  const size_t rows = need / ((static_cast<size_t>(dims->head_dim) + 2) * sizeof(float));
+  a.ws_o = ws;
+  a.ws_ml = reinterpret_cast<float2*>(ws + rows * dims->head_dim);
   a.num_seqs = num_seqs;
   a.num_q_heads = dims->num_q_heads;
   a.num_kv_heads = dims->num_kv_heads;
   a.num_blocks = num_blocks;
   a.max_blocks = max_blocks;
   a.max_context_len = max_context_len;
-  a.partition_tokens = P;
-  a.max_parts = max_parts;
+  a.chunk_blocks = P / dims->block_size;
+  a.num_warps = 0;  // set by the launcher from the grid it picks
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   return pa::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK

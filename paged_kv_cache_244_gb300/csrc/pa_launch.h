@@ -6,7 +6,20 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+// Decode kernel shape: warps per CTA and shared-memory stages per warp.
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 8
+#endif
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 2
+#endif
+
 namespace pa {
+
+// Decode limits: sequences per call (their block-count prefix lives in shared memory) and
+// warps of the persistent grid (bounds the partial slots the workspace must hold).
+constexpr int kMaxDecodeSeqs = 8192;
+constexpr int kMaxDecodeWarps = 2048;
 
 struct RopeArgs {
   __nv_bfloat16* q;                 // [T][Hq][128], rotated in place
@@ -28,10 +41,11 @@ struct DecodeArgs {
   const int32_t* block_tables;      // [S][max_blocks]
   const int32_t* context_lens;      // [S]
   __nv_bfloat16* out;               // [S][Hq][128]
-  float* ws_o;                      // [S][Hq][max_parts][128]   partial sum_t p_t V_t
-  float2* ws_ml;                    // [S][Hq][max_parts]        partial (max, sum p) log2 domain
+  float* ws_o;                      // [slots][G][128]  partial sum_t p_t V_t of each piece
+  float2* ws_ml;                    // [slots][G]       partial (max, sum p), log2 domain
   int num_seqs, num_q_heads, num_kv_heads, num_blocks, max_blocks, max_context_len;
-  int partition_tokens, max_parts;
+  int chunk_blocks;                 // 0: even split over the grid's warps; else blocks per range
+  int num_warps;                    // warps of the partition kernel's grid (set at launch)
   float scale_log2;                 // softmax scale * log2(e)
   unsigned* status;
 };

@@ -46,8 +46,7 @@ extern "C" int pa_decode_static_workspace(const pa_dims* dims, int num_seqs, con
                                           int max_blocks, const int32_t* context_lens,
                                           int max_context_len, float scale,
                                           int partition_tokens, void* out, void* stream) {
-  // 0 both when no partials are needed and when the arguments are invalid; pa_decode then
-  // reports the invalid argument itself.
+  // 0 when the arguments are invalid; pa_decode then reports the invalid argument itself.
   const size_t need = pa_decode_workspace_size(dims, num_seqs, max_context_len, partition_tokens);
   if (need > PA_STATIC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE;
   void* scratch = nullptr;

@@ -1,27 +1,48 @@
-// Single-token paged GQA decode attention for sm_103a, with Flash-Decode partitions.
+// Single-token paged GQA decode attention for sm_103a, with Flash-Decode splitting.
 //
 // "Pico-vLLM：从零手写的工业级LLM推理引擎实现": §2 Kernel层 (PagedAttention decode kernel),
 // §1 模型实现层 (GQA), §H200上的详细对比 (Flash Decode); "从零实现 LLM 推理引擎：深挖 vLLM 的
 // 六大核心优化", §3.1 Paged KV Cache (16-token blocks reached through a block table).
 //
-// Work unit = (partition, sequence, KV head), one warp each; a CTA holds kWarps units.  The
-// warp serves all G query heads of its KV head, so each (block, KV head) tile of K and V is
-// read from HBM exactly once.  Per block the warp:
-//   1. has the 4 KiB K tile and 4 KiB V tile in shared memory, brought by two bulk async
-//      copies (cp.async.bulk, completion on an mbarrier) issued kStages blocks ahead, the
-//      physical id coming from the block table;
-//   2. computes the 16 x G scores in fp32 (lane l owns dims 4l..4l+3 for every head, then a
-//      butterfly that halves the live values each step turns 32 partial sums per score into
-//      G/2 finished scores per lane: lane l ends with token l/2, heads (l&1)*G/2 + i);
-//   3. updates the online softmax (running max m, running sum l, rescale factor
-//      exp2(m_old - m_new)) in the log2 domain, scale * log2(e) folded into q;
-//   4. accumulates p * V into 4 dims x G heads per lane.
-// A unit whose sequence fits in one partition writes bf16 `out`; otherwise it writes its
-// partial (sum p V, (m, l)) to the workspace and decode_merge_kernel combines partitions:
+// Work.  Segment i = s * Hkv + g is the block list of sequence s for KV head g: n_s =
+// ceil(len_s / 16) blocks, starting at X_i = Hkv * N_s + g * n_s on one flattened axis of
+// T = Hkv * N_S block jobs (N_s = sum of n over the sequences before s).  The axis is cut into
+// V equal contiguous ranges ("virtual warps"): V = min(#warps, T) so that every warp of the
+// persistent grid gets the same number of blocks +-1, or ranges of a fixed C = P / 16 blocks
+// when the caller asks for P-token partitions.  A range cut by segment boundaries gives
+// pieces; piece (v, i) covers the part of segment i inside range v and owns partial slot v + i.
+// A warp serves all G <= 8 query heads of a segment's KV head, so each (block, KV head) tile of
+// K and V is read from HBM exactly once.
+//
+// Each warp is its own producer and consumer over a ring of kStages shared-memory stages that
+// runs straight through piece boundaries:
+//   lookahead  the lanes of the warp resolve 32 jobs at a time -- segment (binary search over
+//              the CTA's shared prefix of block counts), block id from the block table, valid
+//              tokens, first / last / whole-segment flags -- one window ahead of use;
+//   producer   per job, lane 0 writes a small descriptor and issues four TMA tensor loads (two
+//              64-column halves of the K tile and of the V tile, 128-byte swizzle) on the
+//              stage's mbarrier, plus on a piece's first block a bulk copy of the q rows;
+//   consumer   waits on the stage (bounded), on a first block loads q^T fragments from the
+//              stage and resets the softmax state, computes S^T = K q^T (16 tokens x 8 head
+//              columns) with 8 m16n8k16 bf16 MMAs (A = K via ldmatrix), updates the online
+//              softmax in the log2 domain (scale * log2(e) applied to S), rounds P to bf16 and
+//              transposes it with movmatrix into the B operand, and accumulates O^T += V^T P^T
+//              (128 dims x 8 heads, fp32) with 8 MMAs (A = V via transposing ldmatrix); on a
+//              piece's last block it writes bf16 `out` (the piece is the whole segment) or the
+//              partial (sum p V, (m, l)) to slot v + i.
+// decode_merge_kernel combines the pieces of split segments:
 //   M = max_p m_p,  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
+//
+// Shared memory per stage: [K cols 0-63 | K cols 64-127 | V cols 0-63 | V cols 64-127 | q rows],
+// the four tile halves 16 rows x 128 B each, swizzled so that 16-byte chunk c of row r sits at
+// chunk c ^ (r % 8); the ldmatrix row addresses apply the same XOR, so all eight rows of a
+// matrix hit distinct banks.
 
 #include <cmath>
 #include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "pa_device.cuh"
 #include "pa_launch.h"
@@ -29,326 +50,646 @@
 namespace pa {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kStages = 3;
-constexpr int kStageBytes = 2 * kTileBytes;              // K tile + V tile
-constexpr int kSmemBytes = kWarps * kStages * kStageBytes + kWarps * kStages * 8;
+constexpr int kWarps = PA_DECODE_WARPS;
+constexpr int kStages = PA_DECODE_STAGES;
+constexpr int kHalfBytes = kBlockSize * 128;                // 16 rows x 64 bf16
+constexpr int kQBytes = 8 * kHeadDim * 2;                   // q rows of up to 8 heads
+constexpr int kStageBytes = 2 * kTileBytes + kQBytes;       // K tile + V tile + q rows
+constexpr int kDescOffset = kWarps * kStages * 8;           // after the mbarriers
+constexpr int kPrefixOffset = kDescOffset + kWarps * kStages * 16;
+constexpr int kTileBytesAll = kWarps * kStages * kStageBytes;
 
-template <int GP>
-__global__ void __launch_bounds__(kWarps * 32) decode_partition_kernel(const DecodeArgs a) {
-  constexpr int HPL = GP / 2;       // heads per lane after the butterfly
-  constexpr int NV = 16 * GP;       // partial scores per block (token-major: t * GP + h)
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  unsigned char* tiles = smem + warp * kStages * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * kStageBytes) + warp * kStages;
-  if (lane == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(smem_addr(&bars[st]), 1);
-    fence_mbar_init();
+constexpr uint32_t kFirst = 1u, kLast = 2u, kWhole = 4u, kHasData = 8u;
+
+__host__ __device__ inline int prefix_bytes(int num_seqs) { return ((num_seqs + 1) * 4 + 15) & ~15; }
+__host__ __device__ inline int smem_bytes(int num_seqs) {
+  return kPrefixOffset + prefix_bytes(num_seqs) + 1024 + kTileBytesAll;  // + 1024: alignment pad
+}
+
+// Flattened-axis ranges.  chunk > 0: range v = [v*chunk, (v+1)*chunk) clipped to T.  chunk == 0:
+// V = min(num_warps, T) ranges, range v = [floor(v T / V), floor((v+1) T / V)).
+struct Ranges {
+  long long T;
+  int V, chunk;
+  __device__ __forceinline__ long long begin(int v) const {
+    if (chunk) return min(static_cast<long long>(v) * chunk, T);
+    return (static_cast<long long>(v) * T) / V;
   }
-  __syncwarp();
+  __device__ __forceinline__ int owner(long long x) const {
+    if (chunk) return static_cast<int>(x / chunk);
+    return static_cast<int>(((x + 1) * V - 1) / T);
+  }
+};
+
+__device__ __forceinline__ Ranges make_ranges(long long T, const DecodeArgs& a) {
+  Ranges r;
+  r.T = T;
+  r.chunk = a.chunk_blocks;
+  if (r.chunk) r.V = static_cast<int>((T + r.chunk - 1) / r.chunk);
+  else r.V = static_cast<int>(min(static_cast<long long>(a.num_warps), T));
+  return r;
+}
+
+__device__ __forceinline__ int clamp_len(int len, int max_len) {
+  return len < 0 ? 0 : (len > max_len ? max_len : len);
+}
+
+__global__ void __launch_bounds__(kWarps * 32, 1)
+decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t bars = raw + warp * kStages * 8;
+  int4* descs = reinterpret_cast<int4*>(smem_raw + kDescOffset) + warp * kStages;
+  int* prefix = reinterpret_cast<int*>(smem_raw + kPrefixOffset);  // N_s, s = 0..S
+  // 128-byte swizzled TMA destinations must sit on 1024-byte boundaries.
+  const uint32_t tiles =
+      ((raw + kPrefixOffset + prefix_bytes(a.num_seqs) + 1023u) & ~1023u) + warp * kStages * kStageBytes;
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(bars + 8 * st, 1);
+    fence_mbar_init();
+    prefetch_tensor_map(&tm_k);
+    prefetch_tensor_map(&tm_v);
+  }
   pdl_wait_prior_grid();
   pdl_allow_next_grid();
 
-  const int units_per_part = a.num_seqs * a.num_kv_heads;
-  const int unit = blockIdx.x * kWarps + warp;
-  if (unit >= units_per_part * a.max_parts) return;
-  const int part = unit / units_per_part;
-  const int rem = unit - part * units_per_part;
-  const int s = rem / a.num_kv_heads;
-  const int g = rem - s * a.num_kv_heads;
-  const int G = a.num_q_heads / a.num_kv_heads;
-  const int P = a.partition_tokens;
+  const int S = a.num_seqs;
+  const int Hkv = a.num_kv_heads;
+  const int G = a.num_q_heads / Hkv;
 
-  int ctx = a.context_lens[s];
-  if (ctx < 0 || ctx > a.max_context_len) {
-    if (lane == 0 && part == 0 && g == 0) raise_flag(a.status, PA_FLAG_CONTEXT_LEN_OOB);
-    ctx = ctx < 0 ? 0 : a.max_context_len;
-  }
-  const int t0 = part * P;
-  const size_t head0 = static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(g) * G;
-  if (t0 >= ctx) {
-    if (part == 0) {  // empty context: zero rows
-      for (int h = 0; h < G; ++h)
-        reinterpret_cast<uint2*>(a.out + (head0 + h) * kHeadDim)[lane] = make_uint2(0u, 0u);
+  // ---- CTA prologue: exclusive prefix N_s of per-sequence block counts in shared memory ----
+  {
+    __shared__ int warp_sums[kWarps];
+    const int per = (S + kWarps * 32 - 1) / (kWarps * 32);
+    const int lo = min(S, tid * per), hi = min(S, lo + per);
+    int sum = 0;
+    for (int s = lo; s < hi; ++s) {
+      const int len = a.context_lens[s];
+      if ((len < 0 || len > a.max_context_len) && blockIdx.x == 0)
+        raise_flag(a.status, PA_FLAG_CONTEXT_LEN_OOB);
+      sum += (clamp_len(len, a.max_context_len) + kBlockSize - 1) / kBlockSize;
     }
-    return;
-  }
-  const int t1 = min(ctx, t0 + P);
-  const int j0 = t0 / kBlockSize;
-  const int nblk = (t1 + kBlockSize - 1) / kBlockSize - j0;
-  const int nparts = (ctx + P - 1) / P;
-
-  // q for every head of the group: lane owns dims 4*lane .. 4*lane+3, pre-scaled.
-  float qr[GP][4];
+    int incl = sum;
 #pragma unroll
-  for (int h = 0; h < GP; ++h) {
-    uint2 w = make_uint2(0u, 0u);
-    if (h < G) w = reinterpret_cast<const uint2*>(a.q + (head0 + h) * kHeadDim)[lane];
-    qr[h][0] = bf16lo(w.x) * a.scale_log2;
-    qr[h][1] = bf16hi(w.x) * a.scale_log2;
-    qr[h][2] = bf16lo(w.y) * a.scale_log2;
-    qr[h][3] = bf16hi(w.y) * a.scale_log2;
+    for (int x = 1; x < 32; x <<= 1) {
+      const int y = __shfl_up_sync(kFullMask, incl, x);
+      if (lane >= x) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    int run = incl - sum;
+    for (int w = 0; w < warp; ++w) run += warp_sums[w];
+    for (int s = lo; s < hi; ++s) {
+      prefix[s] = run;
+      run += (clamp_len(a.context_lens[s], a.max_context_len) + kBlockSize - 1) / kBlockSize;
+    }
+    if (tid == kWarps * 32 - 1) {
+      int total = 0;
+      for (int w = 0; w < kWarps; ++w) total += warp_sums[w];
+      prefix[S] = total;
+    }
+    __syncthreads();
   }
+  const long long T = static_cast<long long>(Hkv) * prefix[S];
+  const Ranges R = make_ranges(T, a);
+  const int NW = gridDim.x * kWarps;
+  const int gq = lane >> 2;  // fragment row group
+  const int cq = lane & 3;   // fragment column pair
+  const int mi = lane >> 3;  // ldmatrix: matrix this lane addresses
+  const int r = lane & 7;    // ldmatrix: row of that matrix
 
-  const int32_t* bt = a.block_tables + static_cast<size_t>(s) * a.max_blocks;
-  int blk_chunk = -1;           // block ids of the 32-block chunk the producer is in
-  uint32_t issued = 0;          // bit st: a copy is in flight into stage st
-  uint32_t parity = 0;          // bit st: phase parity to wait for on stage st
+  // ---------------------------------------------------------------- lookahead windows --
+  // Window = up to 32 consecutive jobs of one range; lane j resolves job j.  Fields per lane:
+  // physical block id, segment, flags | valid << 8, partial slot.
+  struct Window {
+    int v;                // range
+    long long x;          // first position
+    int n;                // jobs in the window (0: none left)
+    int blk, seg, fl, slot;
+  };
+  auto resolve = [&](Window& W) {
+    W.blk = -1;
+    W.seg = W.fl = W.slot = 0;
+    if (W.n == 0 || lane >= W.n) return;
+    const long long x0 = R.begin(W.v), x1 = R.begin(W.v + 1);
+    const long long p = W.x + lane;
+    // largest s with Hkv * N_s <= p (N_0 = 0 <= p < Hkv * N_S = T)
+    int lo = 0, hi = S;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (static_cast<long long>(Hkv) * prefix[mid] <= p) lo = mid;
+      else hi = mid;
+    }
+    const int s = lo;
+    const int ns = prefix[s + 1] - prefix[s];
+    const long long off = p - static_cast<long long>(Hkv) * prefix[s];
+    const int g = static_cast<int>(off / ns);
+    const int j = static_cast<int>(off - static_cast<long long>(g) * ns);
+    const long long Xi = static_cast<long long>(Hkv) * prefix[s] + static_cast<long long>(g) * ns;
+    const int len = clamp_len(a.context_lens[s], a.max_context_len);
+    W.blk = a.block_tables[static_cast<size_t>(s) * a.max_blocks + j];
+    W.seg = s * Hkv + g;
+    const int valid = min(kBlockSize, len - j * kBlockSize);
+    const uint32_t flags = ((p == x0 || j == 0) ? kFirst : 0u) | ((p == x1 - 1 || j == ns - 1) ? kLast : 0u) |
+                           ((Xi >= x0 && Xi + ns <= x1) ? kWhole : 0u);
+    W.fl = static_cast<int>(flags | (static_cast<uint32_t>(valid) << 8));
+    W.slot = W.v + W.seg;
+  };
+  // The window after W: the rest of W's range, else the start of this warp's next range.
+  auto next_of = [&](const Window& W, Window& N) {
+    N.v = W.v;
+    N.x = W.x + W.n;
+    if (W.n == 0 || N.x >= R.begin(W.v + 1)) {
+      N.v = W.v + NW;
+      N.x = N.v < R.V ? R.begin(N.v) : 0;
+    }
+    N.n = N.v < R.V ? static_cast<int>(min(32ll, R.begin(N.v + 1) - N.x)) : 0;
+  };
 
-  // Whole warp calls; lane 0 issues the two copies of block (j0 + jj) into stage st.
-  auto issue = [&](int jj, int st) {
-    if ((jj & 31) == 0) {
-      const int j = j0 + jj + lane;
-      blk_chunk = (jj + lane < nblk) ? bt[j] : -1;
+  Window cur, nxt;
+  cur.v = blockIdx.x * kWarps + warp;
+  cur.x = cur.v < R.V ? R.begin(cur.v) : 0;
+  cur.n = cur.v < R.V ? static_cast<int>(min(32ll, R.begin(cur.v + 1) - cur.x)) : 0;
+  resolve(cur);
+  next_of(cur, nxt);
+  resolve(nxt);
+  int pk = 0;  // next job of `cur`
+
+  // Emit the next job into stage st; false when the warp has no work left.
+  auto produce = [&](int st) -> bool {
+    if (pk == cur.n) {
+      if (nxt.n == 0) return false;
+      cur = nxt;
+      pk = 0;
+      next_of(cur, nxt);
+      resolve(nxt);
     }
-    const int blk = __shfl_sync(kFullMask, blk_chunk, jj & 31);
-    if (blk < 0 || blk >= a.num_blocks) {
-      if (lane == 0) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
-      issued &= ~(1u << st);
-      return;
-    }
-    issued |= 1u << st;
+    const int blk = __shfl_sync(kFullMask, cur.blk, pk);
+    const int seg = __shfl_sync(kFullMask, cur.seg, pk);
+    const int fl = __shfl_sync(kFullMask, cur.fl, pk);
+    const int slot = __shfl_sync(kFullMask, cur.slot, pk);
+    ++pk;
+    const bool ok = blk >= 0 && blk < a.num_blocks;
+    const bool first = (fl & kFirst) != 0;
     if (lane == 0) {
-      const uint32_t bar = smem_addr(&bars[st]);
-      const size_t tile = (static_cast<size_t>(blk) * a.num_kv_heads + g) * (kBlockSize * kHeadDim);
+      if (!ok) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
+      descs[st] = make_int4(seg, fl | (ok ? static_cast<int>(kHasData) : 0), slot, 0);
+      const uint32_t bar = bars + 8 * st;
+      const uint32_t dst = tiles + st * kStageBytes;
+      const uint32_t bytes = (ok ? 2u * kTileBytes : 0u) + (first ? static_cast<uint32_t>(G) * 256u : 0u);
+      const int s = seg / Hkv;
+      const int g = seg - s * Hkv;
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, kStageBytes);
-      bulk_copy_g2s(smem_addr(tiles + st * kStageBytes), a.k_cache + tile, kTileBytes, bar);
-      bulk_copy_g2s(smem_addr(tiles + st * kStageBytes + kTileBytes), a.v_cache + tile, kTileBytes, bar);
+      if (bytes) {
+        mbar_arrive_expect_tx(bar, bytes);
+        if (ok) {
+          const int y = (blk * Hkv + g) * kBlockSize;
+          tma_load_2d(dst, &tm_k, 0, y, bar);
+          tma_load_2d(dst + kHalfBytes, &tm_k, 64, y, bar);
+          tma_load_2d(dst + 2 * kHalfBytes, &tm_v, 0, y, bar);
+          tma_load_2d(dst + 3 * kHalfBytes, &tm_v, 64, y, bar);
+        }
+        if (first) {
+          const size_t head0 = static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(g) * G;
+          bulk_copy_g2s(dst + 2 * kTileBytes, a.q + head0 * kHeadDim, static_cast<uint32_t>(G) * 256u, bar);
+        }
+      } else {
+        mbar_arrive(bar);
+      }
+    }
+    return true;
+  };
+
+  // ---------------------------------------------------------------- consumer state --
+  const uint32_t k_row = static_cast<uint32_t>((r + 8 * (mi & 1)) * 128);   // K: rows 0-7 / 8-15
+  const int k_col = mi >> 1;                                                 // K: chunk 2kk / 2kk+1
+  const uint32_t v_row = static_cast<uint32_t>((r + 8 * (mi >> 1)) * 128);  // V: tokens 0-7 / 8-15
+  const int v_col = mi & 1;                                                  // V: chunk 2mt / 2mt+1
+  uint32_t qb[8][2];                     // B operand q^T: head gq, dims 16kk + 2cq (+1), +8
+  float m0 = -INFINITY, m1 = -INFINITY;  // running max of head columns 2cq, 2cq+1
+  float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
+  float o[8][4];                         // O^T: dims 16mt + gq (+8), heads 2cq, 2cq+1
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+  auto consume = [&](int st) {
+    const int4 d = descs[st];
+    const uint32_t fl = static_cast<uint32_t>(d.y);
+    const uint32_t kt = tiles + st * kStageBytes;
+    const uint32_t vt = kt + 2 * kHalfBytes;
+    if (fl & kFirst) {
+      // q rows sit unswizzled at 256-byte stride; rows >= G are not real heads.
+      const uint32_t qt = kt + 2 * kTileBytes + static_cast<uint32_t>(r * 256);
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2)
+        ldsm_x4(qt + (4 * k2 + mi) * 16, qb[2 * k2][0], qb[2 * k2][1], qb[2 * k2 + 1][0],
+                qb[2 * k2 + 1][1]);
+      if (gq >= G) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) qb[kk][0] = qb[kk][1] = 0u;
+      }
+      m0 = m1 = -INFINITY;
+      l0 = l1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    }
+    if (fl & kHasData) {
+      const int valid = static_cast<int>(fl >> 8);
+      // S^T = K q^T: rows = tokens, columns = heads.
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        const int chunk = (2 * kk + k_col) & 7;
+        ldsm_x4(kt + (kk >> 2) * kHalfBytes + k_row + ((chunk ^ r) << 4), a0, a1, a2, a3);
+        mma_bf16_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+      }
+      // sc: [0] = (token gq, head 2cq), [1] = (gq, 2cq+1), [2] = (gq+8, 2cq), [3] = (gq+8, 2cq+1)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc[i] *= a.scale_log2;
+      uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+      if (valid < kBlockSize) {
+        if (gq >= valid) sc[0] = sc[1] = -INFINITY;
+        if (gq + 8 >= valid) sc[2] = sc[3] = -INFINITY;
+        // V rows past the context may hold anything (even NaN): zero them in the operand.
+        vmask_lo = (2 * cq < valid ? 0x0000ffffu : 0u) | (2 * cq + 1 < valid ? 0xffff0000u : 0u);
+        vmask_hi = (2 * cq + 8 < valid ? 0x0000ffffu : 0u) | (2 * cq + 9 < valid ? 0xffff0000u : 0u);
+      }
+      float bm0 = fmaxf(sc[0], sc[2]);
+      float bm1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+      for (int x = 4; x < 32; x <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(kFullMask, bm0, x));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(kFullMask, bm1, x));
+      }
+      const float mn0 = fmaxf(m0, bm0);
+      const float mn1 = fmaxf(m1, bm1);
+      const float al0 = exp2f(m0 - mn0);
+      const float al1 = exp2f(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      // P rounded to bf16 (the MMA operand); the running sums add the same rounded values.
+      const uint32_t p_lo = pack_bf16x2(exp2f(sc[0] - mn0), exp2f(sc[1] - mn1));  // token gq
+      const uint32_t p_hi = pack_bf16x2(exp2f(sc[2] - mn0), exp2f(sc[3] - mn1));  // token gq+8
+      l0 = fmaf(l0, al0, bf16lo(p_lo) + bf16lo(p_hi));
+      l1 = fmaf(l1, al1, bf16hi(p_lo) + bf16hi(p_hi));
+      // B operand P^T: tokens 2cq, 2cq+1 (and +8) of head gq.
+      const uint32_t pb0 = movmatrix_trans(p_lo);
+      const uint32_t pb1 = movmatrix_trans(p_hi);
+      if (__any_sync(kFullMask, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][0] *= al0;
+          o[mt][1] *= al1;
+          o[mt][2] *= al0;
+          o[mt][3] *= al1;
+        }
+      }
+      // O^T += V^T P^T, one 16-dim slab at a time.
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t v0, v1, v2, v3;
+        const int chunk = (2 * mt + v_col) & 7;
+        ldsm_x4_trans(vt + (mt >> 2) * kHalfBytes + v_row + ((chunk ^ r) << 4), v0, v1, v2, v3);
+        mma_bf16_16816(o[mt], v0 & vmask_lo, v1 & vmask_lo, v2 & vmask_hi, v3 & vmask_hi, pb0, pb1);
+      }
+    }
+    if (fl & kLast) {
+      const int seg = d.x;
+      const int s = seg / Hkv;
+      const int g = seg - s * Hkv;
+      const size_t head0 = static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(g) * G;
+      // Full row sums: the 8 lanes sharing cq hold disjoint token shares of the same heads.
+      float L0 = l0, L1 = l1;
+#pragma unroll
+      for (int x = 4; x < 32; x <<= 1) {
+        L0 += __shfl_xor_sync(kFullMask, L0, x);
+        L1 += __shfl_xor_sync(kFullMask, L1, x);
+      }
+      if (fl & kWhole) {
+        const float i0 = 1.f / L0;
+        const float i1 = 1.f / L1;
+        uint32_t* orow = reinterpret_cast<uint32_t*>(a.out + (head0 + gq) * kHeadDim);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          // (dim, head pair) -> transpose -> (head gq, dim pair): one 32-bit store per half.
+          const uint32_t lo = movmatrix_trans(pack_bf16x2(o[mt][0] * i0, o[mt][1] * i1));
+          const uint32_t hi = movmatrix_trans(pack_bf16x2(o[mt][2] * i0, o[mt][3] * i1));
+          if (gq < G) {
+            orow[8 * mt + cq] = lo;
+            orow[8 * mt + 4 + cq] = hi;
+          }
+        }
+      } else {
+        const size_t slot = static_cast<size_t>(d.z);
+        const size_t row0 = slot * G + 2 * cq;  // head 2cq of the group
+        const bool h0 = 2 * cq < G;
+        const bool h1 = 2 * cq + 1 < G;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const int dd = 16 * mt + gq;
+          if (h0) {
+            a.ws_o[row0 * kHeadDim + dd] = o[mt][0];
+            a.ws_o[row0 * kHeadDim + dd + 8] = o[mt][2];
+          }
+          if (h1) {
+            a.ws_o[(row0 + 1) * kHeadDim + dd] = o[mt][1];
+            a.ws_o[(row0 + 1) * kHeadDim + dd + 8] = o[mt][3];
+          }
+        }
+        if (gq == 0) {
+          if (h0) a.ws_ml[row0] = make_float2(m0, L0);
+          if (h1) a.ws_ml[row0 + 1] = make_float2(m1, L1);
+        }
+      }
     }
   };
 
-#pragma unroll
-  for (int st = 0; st < kStages; ++st)
-    if (st < nblk) issue(st, st);
-
-  float m[HPL], l[HPL];
-#pragma unroll
-  for (int i = 0; i < HPL; ++i) {
-    m[i] = -INFINITY;
-    l[i] = 0.f;
+  // ---------------------------------------------------------------- pipeline --------
+  int produced = 0, consumed = 0;
+  bool more = true;
+  while (more && produced < kStages) {
+    if (produce(produced % kStages)) ++produced;
+    else more = false;
   }
-  float acc[GP][4];
-#pragma unroll
-  for (int h = 0; h < GP; ++h)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[h][i] = 0.f;
-
-  for (int jj = 0; jj < nblk; ++jj) {
-    const int st = jj % kStages;
-    if (issued & (1u << st)) {
-      if (!mbar_wait_bounded(smem_addr(&bars[st]), (parity >> st) & 1u)) {
-        if (lane == 0) raise_flag(a.status, PA_FLAG_TIMEOUT);
-        // Let the other copies in flight land (bounded) before the CTA can exit.
-        for (int o = 0; o < kStages; ++o)
-          if (o != st && (issued & (1u << o))) mbar_wait_bounded(smem_addr(&bars[o]), (parity >> o) & 1u);
-        return;
-      }
-      parity ^= 1u << st;
-      const int valid = min(kBlockSize, t1 - (j0 + jj) * kBlockSize);
-      const uint2* K2 = reinterpret_cast<const uint2*>(tiles + st * kStageBytes);
-      const uint2* V2 = reinterpret_cast<const uint2*>(tiles + st * kStageBytes + kTileBytes);
-
-      // Scores: partial dot products over this lane's 4 dims.
-      float vals[NV];
-#pragma unroll
-      for (int t = 0; t < kBlockSize; ++t) {
-        const uint2 w = K2[t * 32 + lane];
-        const float k0 = bf16lo(w.x), k1 = bf16hi(w.x), k2 = bf16lo(w.y), k3 = bf16hi(w.y);
-#pragma unroll
-        for (int h = 0; h < GP; ++h)
-          vals[t * GP + h] = fmaf(qr[h][3], k3, fmaf(qr[h][2], k2, fmaf(qr[h][1], k1, qr[h][0] * k0)));
-      }
-      // Butterfly: at each step a lane keeps the half of its live values selected by its
-      // lane bit and adds its partner's copy of that half.
-#pragma unroll
-      for (int step = 0; step < 5; ++step) {
-        const int msk = 16 >> step;
-        const int half = (NV >> step) / 2;
-        const bool upper = (lane & msk) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-          const float send = upper ? vals[i] : vals[i + half];
-          const float keep = upper ? vals[i + half] : vals[i];
-          vals[i] = keep + __shfl_xor_sync(kFullMask, send, msk);
-        }
-      }
-      // lane holds token lane/2, heads (lane&1)*HPL + i.
-      const bool tok_ok = (lane >> 1) < valid;
-      float p[HPL], alpha[HPL];
-#pragma unroll
-      for (int i = 0; i < HPL; ++i) {
-        const float sc = tok_ok ? vals[i] : -INFINITY;
-        float bm = sc;
-        bm = fmaxf(bm, __shfl_xor_sync(kFullMask, bm, 2));
-        bm = fmaxf(bm, __shfl_xor_sync(kFullMask, bm, 4));
-        bm = fmaxf(bm, __shfl_xor_sync(kFullMask, bm, 8));
-        bm = fmaxf(bm, __shfl_xor_sync(kFullMask, bm, 16));
-        const float mn = fmaxf(m[i], bm);
-        alpha[i] = exp2f(m[i] - mn);
-        m[i] = mn;
-        p[i] = tok_ok ? exp2f(sc - mn) : 0.f;
-        l[i] = l[i] * alpha[i] + p[i];
-      }
-#pragma unroll
-      for (int h = 0; h < GP; ++h) {
-        const float ah = __shfl_sync(kFullMask, alpha[h % HPL], h / HPL);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[h][i] *= ah;
-      }
-#pragma unroll
-      for (int t = 0; t < kBlockSize; ++t) {
-        if (t < valid) {
-          const uint2 w = V2[t * 32 + lane];
-          const float v0 = bf16lo(w.x), v1 = bf16hi(w.x), v2 = bf16lo(w.y), v3 = bf16hi(w.y);
-#pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            const float pt = __shfl_sync(kFullMask, p[h % HPL], 2 * t + h / HPL);
-            acc[h][0] = fmaf(pt, v0, acc[h][0]);
-            acc[h][1] = fmaf(pt, v1, acc[h][1]);
-            acc[h][2] = fmaf(pt, v2, acc[h][2]);
-            acc[h][3] = fmaf(pt, v3, acc[h][3]);
-          }
-        }
-      }
+  while (consumed < produced) {
+    const int st = consumed % kStages;
+    if (!mbar_wait_bounded(bars + 8 * st, (consumed / kStages) & 1)) {
+      if (lane == 0) raise_flag(a.status, PA_FLAG_TIMEOUT);
+      // Let the other copies in flight land (bounded) before the CTA can exit.
+      for (int j = consumed + 1; j < produced; ++j)
+        mbar_wait_bounded(bars + 8 * (j % kStages), (j / kStages) & 1);
+      break;
     }
+    consume(st);
+    ++consumed;
     __syncwarp();
-    if (jj + kStages < nblk) issue(jj + kStages, st);
-  }
-
-  // Row sums: lanes of equal parity hold the same heads' per-token sums.
-#pragma unroll
-  for (int i = 0; i < HPL; ++i) {
-    l[i] += __shfl_xor_sync(kFullMask, l[i], 2);
-    l[i] += __shfl_xor_sync(kFullMask, l[i], 4);
-    l[i] += __shfl_xor_sync(kFullMask, l[i], 8);
-    l[i] += __shfl_xor_sync(kFullMask, l[i], 16);
-  }
-  if (nparts == 1) {
-#pragma unroll
-    for (int h = 0; h < GP; ++h) {
-      if (h < G) {
-        const float inv = 1.f / __shfl_sync(kFullMask, l[h % HPL], h / HPL);
-        const uint2 o = make_uint2(pack_bf16x2(acc[h][0] * inv, acc[h][1] * inv),
-                                   pack_bf16x2(acc[h][2] * inv, acc[h][3] * inv));
-        reinterpret_cast<uint2*>(a.out + (head0 + h) * kHeadDim)[lane] = o;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int h = 0; h < GP; ++h) {
-      if (h < G) {
-        const size_t row = (head0 + h) * a.max_parts + part;
-        reinterpret_cast<float4*>(a.ws_o + row * kHeadDim)[lane] =
-            make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-        if (lane == h / HPL) a.ws_ml[row] = make_float2(m[h % HPL], l[h % HPL]);
-      }
+    if (more) {
+      if (produce(produced % kStages)) ++produced;
+      else more = false;
     }
   }
 }
 
-// Merge of the partitions of one (sequence, query head) per warp.
-constexpr int kMergeWarps = 4;
+// Merge of the pieces of one (sequence, query head) per CTA of 8 warps.  The block counts
+// (inputs of the partition kernel, not outputs) are summed before waiting for it: N_s and the
+// total T locate the segment's pieces.  Then, in one round of loads: thread t reads (m_p, l_p)
+// of pieces p = t, t + 256, ..., and warp w reads the partial rows of pieces p = w, w + 8, ...
+// (lane owns dims 4l..4l+3).  The CTA finds M = max m_p, each warp weights its rows by
+// 2^(m_p - M) and the eight warp sums are added in shared memory.  Empty sequences get zero rows.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeRows = 8;  // rows per warp held in registers per round
 
-__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeArgs a) {
-  pdl_wait_prior_grid();
-  const int lane = threadIdx.x & 31;
-  const int w = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
-  if (w >= a.num_seqs * a.num_q_heads) return;
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeArgs a) {
+  __shared__ int red_i[2][kMergeWarps];
+  __shared__ float red[kMergeWarps];
+  __shared__ float lsum[kMergeWarps];
+  __shared__ float4 accs[kMergeWarps][32];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int w = blockIdx.x;  // (sequence, query head)
+  const int S = a.num_seqs;
+  const int Hkv = a.num_kv_heads;
+  const int G = a.num_q_heads / Hkv;
   const int s = w / a.num_q_heads;
-  int ctx = a.context_lens[s];
-  ctx = ctx < 0 ? 0 : (ctx > a.max_context_len ? a.max_context_len : ctx);
-  const int nparts = (ctx + a.partition_tokens - 1) / a.partition_tokens;
-  if (nparts <= 1) return;  // written directly by the partition kernel
-  const size_t row0 = static_cast<size_t>(w) * a.max_parts;
-  const float2* ml = a.ws_ml + row0;
-  float M = -INFINITY;
-  for (int p = lane; p < nparts; p += 32) M = fmaxf(M, ml[p].x);
+  const int h = w - s * a.num_q_heads;
+  const int g = h / G;
+  const int hl = h - g * G;
+
+  // N_s (blocks before s) and N_S, over all sequences.
+  int before = 0, total = 0;
+  for (int t = tid; t < S; t += kMergeThreads) {
+    const int n = (clamp_len(a.context_lens[t], a.max_context_len) + kBlockSize - 1) / kBlockSize;
+    total += n;
+    if (t < s) before += n;
+  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
+  for (int x = 16; x > 0; x >>= 1) {
+    before += __shfl_xor_sync(kFullMask, before, x);
+    total += __shfl_xor_sync(kFullMask, total, x);
+  }
+  if (lane == 0) {
+    red_i[0][warp] = before;
+    red_i[1][warp] = total;
+  }
+  __syncthreads();
+  before = total = 0;
+#pragma unroll
+  for (int i = 0; i < kMergeWarps; ++i) {
+    before += red_i[0][i];
+    total += red_i[1][i];
+  }
+  const int ns = (clamp_len(a.context_lens[s], a.max_context_len) + kBlockSize - 1) / kBlockSize;
+  const long long T = static_cast<long long>(Hkv) * total;
+  if (ns == 0) {  // empty context: zero row (after the partition kernel, which may read `out`)
+    pdl_wait_prior_grid();
+    if (warp == 0)
+      reinterpret_cast<uint2*>(a.out + static_cast<size_t>(w) * kHeadDim)[lane] = make_uint2(0u, 0u);
+    return;
+  }
+  const Ranges R = make_ranges(T, a);
+  const long long Xi = static_cast<long long>(Hkv) * before + static_cast<long long>(g) * ns;
+  const int v_first = R.owner(Xi);
+  const int npieces = R.owner(Xi + ns - 1) - v_first + 1;
+  if (npieces <= 1) return;  // written directly by the partition kernel
+  pdl_wait_prior_grid();
+  const int seg = s * Hkv + g;
+  // piece p lives in slot v_first + p + seg; its row for this head is slot * G + hl
+  const size_t row_base = (static_cast<size_t>(v_first) + seg) * G + hl;
+  const float2* ml = a.ws_ml + row_base;                   // stride G per piece
+  const float4* rows = reinterpret_cast<const float4*>(a.ws_o + row_base * kHeadDim) + lane;
+  const size_t row_stride4 = static_cast<size_t>(G) * 32;  // float4s per piece
+
+  float2 mine = make_float2(-INFINITY, 0.f);
+  if (tid < npieces) mine = ml[static_cast<size_t>(tid) * G];
+  float4 rr[kMergeRows];
+#pragma unroll
+  for (int u = 0; u < kMergeRows; ++u) {
+    const int p = warp + u * kMergeWarps;
+    rr[u] = p < npieces ? rows[p * row_stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float M = mine.x;
+  for (int p = tid + kMergeThreads; p < npieces; p += kMergeThreads)
+    M = fmaxf(M, ml[static_cast<size_t>(p) * G].x);
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, x));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int i = 1; i < kMergeWarps; ++i) M = fmaxf(M, red[i]);
+
   float L = 0.f;
+  for (int p = tid; p < npieces; p += kMergeThreads) {
+    const float2 v = p == tid ? mine : ml[static_cast<size_t>(p) * G];
+    L = fmaf(exp2f(v.x - M), v.y, L);
+  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int pb = 0; pb < nparts; pb += 32) {
-    float wmine = 0.f;
-    if (pb + lane < nparts) {
-      const float2 v = ml[pb + lane];
-      wmine = exp2f(v.x - M);
-      L = fmaf(wmine, v.y, L);
+  for (int base = 0; base < npieces; base += kMergeRows * kMergeWarps) {
+    if (base > 0) {
+#pragma unroll
+      for (int u = 0; u < kMergeRows; ++u) {
+        const int p = base + warp + u * kMergeWarps;
+        rr[u] = p < npieces ? rows[p * row_stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
-    const int n = min(32, nparts - pb);
-    for (int k = 0; k < n; ++k) {
-      const float wk = __shfl_sync(kFullMask, wmine, k);
-      const float4 o = reinterpret_cast<const float4*>(a.ws_o + (row0 + pb + k) * kHeadDim)[lane];
-      acc.x = fmaf(wk, o.x, acc.x);
-      acc.y = fmaf(wk, o.y, acc.y);
-      acc.z = fmaf(wk, o.z, acc.z);
-      acc.w = fmaf(wk, o.w, acc.w);
+#pragma unroll
+    for (int u = 0; u < kMergeRows; ++u) {
+      const int p = base + warp + u * kMergeWarps;
+      if (p < npieces) {
+        const float wk = exp2f(ml[static_cast<size_t>(p) * G].x - M);
+        acc.x = fmaf(wk, rr[u].x, acc.x);
+        acc.y = fmaf(wk, rr[u].y, acc.y);
+        acc.z = fmaf(wk, rr[u].z, acc.z);
+        acc.w = fmaf(wk, rr[u].w, acc.w);
+      }
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(kFullMask, L, o);
-  const float inv = 1.f / L;
-  reinterpret_cast<uint2*>(a.out + static_cast<size_t>(w) * kHeadDim)[lane] =
-      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  for (int x = 16; x > 0; x >>= 1) L += __shfl_xor_sync(kFullMask, L, x);
+  if (lane == 0) lsum[warp] = L;
+  accs[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    float Lt = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kMergeWarps; ++i) {
+      Lt += lsum[i];
+      o.x += accs[i][lane].x;
+      o.y += accs[i][lane].y;
+      o.z += accs[i][lane].z;
+      o.w += accs[i][lane].w;
+    }
+    const float inv = 1.f / Lt;
+    reinterpret_cast<uint2*>(a.out + static_cast<size_t>(w) * kHeadDim)[lane] =
+        make_uint2(pack_bf16x2(o.x * inv, o.y * inv), pack_bf16x2(o.z * inv, o.w * inv));
+  }
 }
 
-template <int GP>
-cudaError_t launch_partition(const DecodeArgs& a, cudaStream_t stream) {
+// ---- host side ------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map of one cache viewed as a 2-D bf16 array [num_blocks * Hkv * 16 rows][128 cols],
+// box 64 cols x 16 rows, 128-byte swizzle.  Encoded maps are cached by (address, rows).
+bool cache_tensor_map(const void* cache, long long rows, CUtensorMap* out) {
+  struct Entry {
+    const void* ptr;
+    long long rows;
+    CUtensorMap map;
+  };
   static std::mutex mu;
-  static bool configured[64] = {};
+  static Entry table[16];
+  static int used = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (table[i].ptr == cache && table[i].rows == rows) {
+      *out = table[i].map;
+      return true;
+    }
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return false;
+  CUtensorMap m;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
+  cuuint32_t estr[2] = {1, 1};
+  if (encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const int slot = used < 16 ? used++ : (next++ & 15);
+  table[slot] = Entry{cache, rows, m};
+  *out = m;
+  return true;
+}
+
+// Persistent grid size for this device: SMs x resident CTAs per SM, capped so that the grid
+// has at most kMaxDecodeWarps warps (looked up once per device, at the largest shared-memory
+// footprint the kernel can ask for).
+cudaError_t persistent_ctas(int* ctas) {
+  static std::mutex mu;
+  static int cached[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-      err = cudaFuncSetAttribute(decode_partition_kernel<GP>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (err != cudaSuccess) return err;
-      configured[dev] = true;
-    }
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    const int smem = smem_bytes(kMaxDecodeSeqs);
+    err = cudaFuncSetAttribute(decode_partition_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    int sms = 0, per_sm = 0;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_partition_kernel, kWarps * 32, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    cached[dev] = min(sms * per_sm, kMaxDecodeWarps / kWarps);
   }
-  const long long units = static_cast<long long>(a.num_seqs) * a.num_kv_heads * a.max_parts;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((units + kWarps - 1) / kWarps));
-  cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_partition_kernel<GP>, a);
+  *ctas = cached[dev];
+  return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
+  DecodeArgs a = args;
   const int G = a.num_q_heads / a.num_kv_heads;
-  cudaError_t err;
-  switch ((G + 1) & ~1) {
-    case 2: err = launch_partition<2>(a, stream); break;
-    case 4: err = launch_partition<4>(a, stream); break;
-    case 6: err = launch_partition<6>(a, stream); break;
-    case 8: err = launch_partition<8>(a, stream); break;
-    default: return cudaErrorInvalidValue;
-  }
-  if (err != cudaSuccess || a.max_parts <= 1) return err;
-  const long long warps = static_cast<long long>(a.num_seqs) * a.num_q_heads;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((warps + kMergeWarps - 1) / kMergeWarps));
-  cfg.blockDim = dim3(kMergeWarps * 32);
-  cfg.stream = stream;
+  if (G < 1 || G > 8 || a.num_seqs > kMaxDecodeSeqs) return cudaErrorInvalidValue;
+  const long long rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * kBlockSize;
+  CUtensorMap tm_k, tm_v;
+  if (!cache_tensor_map(a.k_cache, rows, &tm_k) || !cache_tensor_map(a.v_cache, rows, &tm_v))
+    return cudaErrorInvalidValue;
+  int max_ctas = 0;
+  cudaError_t err = persistent_ctas(&max_ctas);
+  if (err != cudaSuccess) return err;
+  // No more CTAs than there can be ranges.
+  const long long jobs_bound = static_cast<long long>(a.num_seqs) * a.num_kv_heads *
+                               ((a.max_context_len + kBlockSize - 1) / kBlockSize);
+  const long long want = a.chunk_blocks ? (jobs_bound + a.chunk_blocks - 1) / a.chunk_blocks : jobs_bound;
+  const long long ctas = min(static_cast<long long>(max_ctas), (want + kWarps - 1) / kWarps);
+  a.num_warps = static_cast<int>(ctas) * kWarps;
+
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = smem_bytes(a.num_seqs);
+  cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_merge_kernel, a);
+  err = cudaLaunchKernelEx(&cfg, decode_partition_kernel, tm_k, tm_v, a);
+  if (err != cudaSuccess) return err;
+
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.num_seqs) * a.num_q_heads));
+  mcfg.blockDim = dim3(kMergeThreads);
+  mcfg.stream = stream;
+  mcfg.attrs = attr;
+  mcfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&mcfg, decode_merge_kernel, a);
 }
 
 }  // namespace pa

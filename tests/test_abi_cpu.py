@@ -74,7 +74,10 @@ def test_decode_rejects_bad_arguments_on_the_host(L):
     assert decode_call(L, scale=float("nan")) == b.PA_ERR_RANGE
     assert decode_call(L, maxctx=40, maxb=4, part=16, wsb=100) == b.PA_ERR_WORKSPACE
     assert decode_call(L, maxctx=40, maxb=4, part=16, ws=None) == b.PA_ERR_WORKSPACE
-    for kw in ("q", "kc", "vc", "bt", "ctx", "out"):
+    assert decode_call(L, maxctx=40, maxb=4, part=64, ws=None) == b.PA_ERR_WORKSPACE
+    assert decode_call(L, maxctx=40, maxb=4, part=64, wsb=(3 + 4) * 6 * 520 - 1) == b.PA_ERR_WORKSPACE
+    assert decode_call(L, S=8193) == b.PA_ERR_RANGE
+    for kw in ("q", "kc", "vc", "bt", "ctx", "out", "ws"):
         assert decode_call(L, **{kw: MIS_PTR}) == b.PA_ERR_ALIGN, kw
 
 
@@ -101,19 +104,21 @@ def test_rope_kv_store_rejects_bad_arguments_on_the_host(L):
 
 def test_partition_choice_and_workspace_size(L):
     from paged_kv_cache_244_gb300 import binding as b
-    # auto: smallest power-of-two multiple of 16 with S * Hkv * ceil(ctx / P) <= 2048
-    assert b.decode_partition_tokens(12, 2, 2, 40) == 16
-    assert b.decode_partition_tokens(12, 2, 1, 2048) == 16
-    assert b.decode_partition_tokens(12, 2, 64, 4096) == 256
-    assert b.decode_partition_tokens(12, 2, 32, 2064) == 128
-    assert b.decode_partition_tokens(12, 2, 4, 32768) == 128
+    # the request is validated and echoed: 0 = even split, else a multiple of 16 tokens
+    assert b.decode_partition_tokens(12, 2, 2, 40) == 0
     assert b.decode_partition_tokens(12, 2, 4, 32768, 512) == 512
+    for bad in (100, -16):
+        with pytest.raises(b.PaError):
+            b.decode_partition_tokens(12, 2, 4, 32768, bad)
     with pytest.raises(b.PaError):
-        b.decode_partition_tokens(12, 2, 4, 32768, 100)
-    # workspace: S * Hq * parts * (D + 2) floats, 0 when one partition covers the context
-    assert b.decode_workspace_size(12, 2, 4, 32768, 512) == 4 * 12 * 64 * 130 * 4
-    assert b.decode_workspace_size(12, 2, 2, 40, 64) == 0
-    assert b.decode_workspace_size(12, 2, 2, 40) == 2 * 12 * 3 * 130 * 4
+        b.decode_partition_tokens(12, 2, 8193, 64)              # more sequences than supported
+    # workspace: (ranges + segments) * G rows of (D + 2) floats
+    row = 130 * 4
+    assert b.decode_workspace_size(12, 2, 4, 32768, 512) == (512 + 8) * 6 * row
+    assert b.decode_workspace_size(12, 2, 2, 40, 64) == (3 + 4) * 6 * row
+    assert b.decode_workspace_size(12, 2, 2, 40) == (12 + 4) * 6 * row
+    assert b.decode_workspace_size(12, 2, 64, 4096) == (2048 + 128) * 6 * row
+    assert b.decode_workspace_size(12, 2, 4, 32768, 100) == 0
 
 
 def test_status_strings(L):

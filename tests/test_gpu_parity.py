@@ -163,13 +163,25 @@ def test_decode_zero_context_gives_zero_rows(pa, orc):
     check_status_clean(pa)
 
 
-def test_decode_is_deterministic(pa, orc):
+def test_decode_is_deterministic_with_a_reused_workspace(pa, orc):
+    """Repeated calls on one workspace give identical results (the workspace carries nothing
+    from one call to the next)."""
     w = workload("mix64")
     q, kc, vc = oracle_store(orc, w)
     d = DeviceLayer(w, q=q, k_cache=kc, v_cache=vc)
-    a = run_decode(pa, d, w)
-    b = run_decode(pa, d, w)
-    assert np.array_equal(a, b)
+    ref, _ = orc.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    outs = []
+    for P in (0, 64, 0):
+        ws = pa.decode_workspace(d.q, d.k_cache, w.max_context_len, P)
+        ws.fill_(float("nan"))
+        for _ in range(3):
+            out = pa.decode(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens,
+                            w.max_context_len, w.scale, partition_tokens=P, workspace=ws)
+            torch.cuda.synchronize()
+            outs.append((P, host_bits(out)))
+    for P, o in outs:
+        assert_out_close(o, ref, f"P={P}")
+        assert np.array_equal(o, [x for p2, x in outs if p2 == P][0])
 
 
 # --------------------------------------------------------- device-side range checks ----

@@ -60,8 +60,7 @@ def test_static_workspace_matches_decode_on_two_calls(pa):
     orc = oracle.default()
     for name in ("mix64", "long4"):               # two calls in a row, different shapes
         w, d = prepared(name, orc)
-        P = pa.decode_partition_tokens(w.num_q_heads, w.num_kv_heads, w.num_seqs,
-                                       w.max_context_len, w.partition_tokens)
+        P = w.partition_tokens            # mix64: even split; long4: 512-token partitions
         need = pa.decode_workspace_size(w.num_q_heads, w.num_kv_heads, w.num_seqs,
                                         w.max_context_len, P)
         assert 0 < need <= STATIC_BYTES
@@ -84,7 +83,7 @@ def test_static_workspace_refuses_oversized_requests(pa):
     orc = oracle.default()
     w, d = prepared("mix64", orc)
     need = pa.decode_workspace_size(w.num_q_heads, w.num_kv_heads, w.num_seqs,
-                                    w.max_context_len, 16)
+                                    w.max_context_len, 16)     # one range per block: too many
     assert need > STATIC_BYTES
     out = torch.zeros_like(d.q)
     assert call_static(pa, d, w, 16, out) == pa.PA_ERR_WORKSPACE
