@@ -216,12 +216,29 @@ def run_gpu(args, rank, world, dist):
     if rc != 0:
         raise RuntimeError(f"device status after warm-up: {rc} flags {flags:#x}")
 
+    # The step as a CUDA graph (all its launches recorded once, replayed per step), as a serving
+    # engine runs a decode step; --no-graph launches every call from Python instead.
+    step_fn, graph_note = st.step, "eager launches"
+    if not args.no_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                st.step()
+            graph.replay()
+            torch.cuda.synchronize()
+            step_fn, graph_note = graph.replay, "CUDA graph of the step's launches"
+        except Exception as e:  # capture unsupported here: keep eager launches
+            graph_note = f"eager launches (graph capture failed: {type(e).__name__})"
+    rc, flags = binding.get_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after capture: {rc} flags {flags:#x}")
+
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
     barrier()
     t_wall0 = time.time()
-    step_ms = timed_loop(st.step, args.steps)
+    step_ms = timed_loop(step_fn, args.steps)
     barrier()
     t_wall1 = time.time()
     time.sleep(0.25)
@@ -257,6 +274,8 @@ def run_gpu(args, rank, world, dist):
     dec_bytes = w.kv_bytes_per_layer()
     achieved = dec_bytes / (dec_avg * 1e-3) / 1e9
     tokens_per_s = world * w.num_seqs * args.steps / (total_ms_max * 1e-3)
+    cfg = config_of(w, st, world)
+    cfg["launch"] = graph_note
     line = {
         "metric": METRIC,
         "value": round(gbs, 2),
@@ -272,7 +291,7 @@ def run_gpu(args, rank, world, dist):
         "data": "synthetic (seeded splitmix64 -> Box-Muller -> bf16)",
         "pct_of_peak": round(100.0 * gbs / peak, 2),
         "tokens_per_s": round(tokens_per_s, 1),
-        "config": config_of(w, st, world),
+        "config": cfg,
         "roofline": {
             "kernel": "pa_decode (decode_partition_kernel + decode_merge_kernel)",
             "bound": "hbm",
@@ -354,7 +373,7 @@ def config_of(w, st, world):
         "head_dim": W.HEAD_DIM,
         "block_size": W.BLOCK_SIZE,
         "pool_blocks": w.num_blocks,
-        "partition_tokens": st.P if st is not None else w.partition_tokens,
+        "partition_tokens": (st.P if st is not None else w.partition_tokens) or "0 (even split)",
         "kv_bytes_per_step_per_gpu": w.kv_bytes_per_layer() * w.num_layers,
         "l2": "flushed between timed steps (512 MiB write then read back, outside the events)",
         "parallelism": f"replicas x{world} (independent batches)",
@@ -448,6 +467,7 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch each call instead of a CUDA graph")
     ap.add_argument("--partition-tokens", type=int, default=None,
                     help="Flash-Decode partition size (default: the workload's, 0 = library choice)")
     ap.add_argument("--traffic", type=float, default=None,

@@ -13,6 +13,10 @@
 #ifndef PA_DECODE_STAGES
 #define PA_DECODE_STAGES 2
 #endif
+// Shortest range of the even split, in blocks.
+#ifndef PA_DECODE_MIN_RANGE
+#define PA_DECODE_MIN_RANGE 4
+#endif
 
 namespace pa {
 

@@ -7,8 +7,8 @@
 // Work.  Segment i = s * Hkv + g is the block list of sequence s for KV head g: n_s =
 // ceil(len_s / 16) blocks, starting at X_i = Hkv * N_s + g * n_s on one flattened axis of
 // T = Hkv * N_S block jobs (N_s = sum of n over the sequences before s).  The axis is cut into
-// V equal contiguous ranges ("virtual warps"): V = min(#warps, T) so that every warp of the
-// persistent grid gets the same number of blocks +-1, or ranges of a fixed C = P / 16 blocks
+// V equal contiguous ranges ("virtual warps"): V = min(#warps, ceil(T / 4)) so that every warp of
+// the persistent grid gets the same number of blocks +-1, or ranges of a fixed C = P / 16 blocks
 // when the caller asks for P-token partitions.  A range cut by segment boundaries gives
 // pieces; piece (v, i) covers the part of segment i inside range v and owns partial slot v + i.
 // A warp serves all G <= 8 query heads of a segment's KV head, so each (block, KV head) tile of
@@ -60,6 +60,7 @@ constexpr int kPrefixOffset = kDescOffset + kWarps * kStages * 16;
 constexpr int kTileBytesAll = kWarps * kStages * kStageBytes;
 
 constexpr uint32_t kFirst = 1u, kLast = 2u, kWhole = 4u, kHasData = 8u;
+constexpr int kMinRangeBlocks = PA_DECODE_MIN_RANGE;
 
 __host__ __device__ inline int prefix_bytes(int num_seqs) { return ((num_seqs + 1) * 4 + 15) & ~15; }
 __host__ __device__ inline int smem_bytes(int num_seqs) {
@@ -67,7 +68,9 @@ __host__ __device__ inline int smem_bytes(int num_seqs) {
 }
 
 // Flattened-axis ranges.  chunk > 0: range v = [v*chunk, (v+1)*chunk) clipped to T.  chunk == 0:
-// V = min(num_warps, T) ranges, range v = [floor(v T / V), floor((v+1) T / V)).
+// V = min(num_warps, ceil(T / kMinRangeBlocks)) ranges, range v = [floor(v T / V),
+// floor((v+1) T / V)): equal ranges, none shorter than kMinRangeBlocks blocks unless T is, so
+// that a small batch is not cut into one-block pieces that the merge must then gather.
 struct Ranges {
   long long T;
   int V, chunk;
@@ -86,7 +89,7 @@ __device__ __forceinline__ Ranges make_ranges(long long T, const DecodeArgs& a) 
   r.T = T;
   r.chunk = a.chunk_blocks;
   if (r.chunk) r.V = static_cast<int>((T + r.chunk - 1) / r.chunk);
-  else r.V = static_cast<int>(min(static_cast<long long>(a.num_warps), T));
+  else r.V = static_cast<int>(min(static_cast<long long>(a.num_warps), (T + kMinRangeBlocks - 1) / kMinRangeBlocks));
   return r;
 }
 
@@ -435,26 +438,21 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
   }
 }
 
-// Merge of the pieces of one (sequence, query head) per CTA of 8 warps.  The block counts
-// (inputs of the partition kernel, not outputs) are summed before waiting for it: N_s and the
-// total T locate the segment's pieces.  Then, in one round of loads: thread t reads (m_p, l_p)
-// of pieces p = t, t + 256, ..., and warp w reads the partial rows of pieces p = w, w + 8, ...
-// (lane owns dims 4l..4l+3).  The CTA finds M = max m_p, each warp weights its rows by
-// 2^(m_p - M) and the eight warp sums are added in shared memory.  Empty sequences get zero rows.
-constexpr int kMergeThreads = 256;
-constexpr int kMergeWarps = kMergeThreads / 32;
-constexpr int kMergeRows = 8;  // rows per warp held in registers per round
+// Merge of the pieces of one (sequence, query head) per warp.  The kernel is small enough
+// (registers, no shared memory) to sit on the SMs next to the partition kernel, so it starts as
+// soon as that kernel lets dependents launch and does everything that needs no partial result
+// first: where the segment's pieces are comes from N_s and N_S, computed from the sequence
+// lengths (inputs of the partition kernel, not outputs).  After the wait, one round of loads:
+// lane p reads (m_p, l_p) of piece p while every lane reads its 4 dims of the first kMergeBatch
+// piece rows.  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.  Empty sequences get zeros.
+constexpr int kMergeWarps = 8;
+constexpr int kMergeBatch = 8;
 
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeArgs a) {
-  __shared__ int red_i[2][kMergeWarps];
-  __shared__ float red[kMergeWarps];
-  __shared__ float lsum[kMergeWarps];
-  __shared__ float4 accs[kMergeWarps][32];
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const int w = blockIdx.x;  // (sequence, query head)
+__global__ void __launch_bounds__(kMergeWarps * 32, 2) decode_merge_kernel(const DecodeArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);  // (sequence, query head)
   const int S = a.num_seqs;
+  if (w >= S * a.num_q_heads) return;
   const int Hkv = a.num_kv_heads;
   const int G = a.num_q_heads / Hkv;
   const int s = w / a.num_q_heads;
@@ -462,9 +460,8 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   const int g = h / G;
   const int hl = h - g * G;
 
-  // N_s (blocks before s) and N_S, over all sequences.
   int before = 0, total = 0;
-  for (int t = tid; t < S; t += kMergeThreads) {
+  for (int t = lane; t < S; t += 32) {
     const int n = (clamp_len(a.context_lens[t], a.max_context_len) + kBlockSize - 1) / kBlockSize;
     total += n;
     if (t < s) before += n;
@@ -474,76 +471,50 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     before += __shfl_xor_sync(kFullMask, before, x);
     total += __shfl_xor_sync(kFullMask, total, x);
   }
-  if (lane == 0) {
-    red_i[0][warp] = before;
-    red_i[1][warp] = total;
-  }
-  __syncthreads();
-  before = total = 0;
-#pragma unroll
-  for (int i = 0; i < kMergeWarps; ++i) {
-    before += red_i[0][i];
-    total += red_i[1][i];
-  }
   const int ns = (clamp_len(a.context_lens[s], a.max_context_len) + kBlockSize - 1) / kBlockSize;
-  const long long T = static_cast<long long>(Hkv) * total;
+  uint2* orow = reinterpret_cast<uint2*>(a.out + static_cast<size_t>(w) * kHeadDim) + lane;
   if (ns == 0) {  // empty context: zero row (after the partition kernel, which may read `out`)
     pdl_wait_prior_grid();
-    if (warp == 0)
-      reinterpret_cast<uint2*>(a.out + static_cast<size_t>(w) * kHeadDim)[lane] = make_uint2(0u, 0u);
+    *orow = make_uint2(0u, 0u);
     return;
   }
-  const Ranges R = make_ranges(T, a);
+  const Ranges R = make_ranges(static_cast<long long>(Hkv) * total, a);
   const long long Xi = static_cast<long long>(Hkv) * before + static_cast<long long>(g) * ns;
   const int v_first = R.owner(Xi);
   const int npieces = R.owner(Xi + ns - 1) - v_first + 1;
   if (npieces <= 1) return;  // written directly by the partition kernel
-  pdl_wait_prior_grid();
-  const int seg = s * Hkv + g;
-  // piece p lives in slot v_first + p + seg; its row for this head is slot * G + hl
-  const size_t row_base = (static_cast<size_t>(v_first) + seg) * G + hl;
+  // piece p lives in slot v_first + p + segment; its row for this head is slot * G + hl
+  const size_t row_base = (static_cast<size_t>(v_first) + s * Hkv + g) * G + hl;
   const float2* ml = a.ws_ml + row_base;                   // stride G per piece
   const float4* rows = reinterpret_cast<const float4*>(a.ws_o + row_base * kHeadDim) + lane;
-  const size_t row_stride4 = static_cast<size_t>(G) * 32;  // float4s per piece
+  const size_t stride4 = static_cast<size_t>(G) * 32;      // float4s per piece
+  pdl_wait_prior_grid();
 
-  float2 mine = make_float2(-INFINITY, 0.f);
-  if (tid < npieces) mine = ml[static_cast<size_t>(tid) * G];
-  float4 rr[kMergeRows];
+  float2 mine = lane < npieces ? ml[lane * G] : make_float2(-INFINITY, 0.f);
+  float4 rr[kMergeBatch];
 #pragma unroll
-  for (int u = 0; u < kMergeRows; ++u) {
-    const int p = warp + u * kMergeWarps;
-    rr[u] = p < npieces ? rows[p * row_stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+  for (int u = 0; u < kMergeBatch; ++u)
+    rr[u] = u < npieces ? rows[u * stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
   float M = mine.x;
-  for (int p = tid + kMergeThreads; p < npieces; p += kMergeThreads)
-    M = fmaxf(M, ml[static_cast<size_t>(p) * G].x);
+  for (int p = lane + 32; p < npieces; p += 32) M = fmaxf(M, ml[p * G].x);
 #pragma unroll
   for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, x));
-  if (lane == 0) red[warp] = M;
-  __syncthreads();
-  M = red[0];
-#pragma unroll
-  for (int i = 1; i < kMergeWarps; ++i) M = fmaxf(M, red[i]);
-
   float L = 0.f;
-  for (int p = tid; p < npieces; p += kMergeThreads) {
-    const float2 v = p == tid ? mine : ml[static_cast<size_t>(p) * G];
-    L = fmaf(exp2f(v.x - M), v.y, L);
-  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int base = 0; base < npieces; base += kMergeRows * kMergeWarps) {
-    if (base > 0) {
+  for (int base = 0; base < npieces; base += 32) {
+    const float2 v = base == 0 ? mine : (base + lane < npieces ? ml[(base + lane) * G] : make_float2(-INFINITY, 0.f));
+    const float wmine = exp2f(v.x - M);  // 0 for lanes past the last piece
+    L = fmaf(wmine, v.y, L);
+    const int n = min(32, npieces - base);
+    for (int k = 0; k < n; k += kMergeBatch) {
+      if (base + k > 0) {
 #pragma unroll
-      for (int u = 0; u < kMergeRows; ++u) {
-        const int p = base + warp + u * kMergeWarps;
-        rr[u] = p < npieces ? rows[p * row_stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < kMergeBatch; ++u)
+          rr[u] = k + u < n ? rows[(base + k + u) * stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kMergeRows; ++u) {
-      const int p = base + warp + u * kMergeWarps;
-      if (p < npieces) {
-        const float wk = exp2f(ml[static_cast<size_t>(p) * G].x - M);
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const float wk = __shfl_sync(kFullMask, wmine, (k + u) & 31);
         acc.x = fmaf(wk, rr[u].x, acc.x);
         acc.y = fmaf(wk, rr[u].y, acc.y);
         acc.z = fmaf(wk, rr[u].z, acc.z);
@@ -553,24 +524,8 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   }
 #pragma unroll
   for (int x = 16; x > 0; x >>= 1) L += __shfl_xor_sync(kFullMask, L, x);
-  if (lane == 0) lsum[warp] = L;
-  accs[warp][lane] = acc;
-  __syncthreads();
-  if (warp == 0) {
-    float Lt = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < kMergeWarps; ++i) {
-      Lt += lsum[i];
-      o.x += accs[i][lane].x;
-      o.y += accs[i][lane].y;
-      o.z += accs[i][lane].z;
-      o.w += accs[i][lane].w;
-    }
-    const float inv = 1.f / Lt;
-    reinterpret_cast<uint2*>(a.out + static_cast<size_t>(w) * kHeadDim)[lane] =
-        make_uint2(pack_bf16x2(o.x * inv, o.y * inv), pack_bf16x2(o.z * inv, o.w * inv));
-  }
+  const float inv = 1.f / L;
+  *orow = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
 }
 
 // ---- host side ------------------------------------------------------------------------
@@ -683,9 +638,10 @@ cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
   err = cudaLaunchKernelEx(&cfg, decode_partition_kernel, tm_k, tm_v, a);
   if (err != cudaSuccess) return err;
 
+  const long long heads = static_cast<long long>(a.num_seqs) * a.num_q_heads;
   cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(a.num_seqs) * a.num_q_heads));
-  mcfg.blockDim = dim3(kMergeThreads);
+  mcfg.gridDim = dim3(static_cast<unsigned>((heads + kMergeWarps - 1) / kMergeWarps));
+  mcfg.blockDim = dim3(kMergeWarps * 32);
   mcfg.stream = stream;
   mcfg.attrs = attr;
   mcfg.numAttrs = 1;
