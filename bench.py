@@ -259,13 +259,8 @@ def run_gpu(args, rank, world, dist):
         raise RuntimeError(f"device status after timing: {rc} flags {flags:#x}")
 
     # max over ranks of the timed device time; sum of bytes
-    t = torch.tensor([total_ms, e2e["ms"]], dtype=torch.float64, device="cuda")
-    b = torch.tensor([float(bytes_step)], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dist.all_reduce(b, op=dist.ReduceOp.SUM)
-    total_ms_max, e2e_ms_max = float(t[0]), float(t[1])
-    all_bytes = float(b[0])
+    (total_ms_max, e2e_ms_max), (all_bytes,) = reduce_over_ranks(
+        [total_ms, e2e["ms"]], [float(bytes_step)], dist, torch.device("cuda"))
     if rank != 0:
         return None
 
@@ -316,37 +311,55 @@ def run_gpu(args, rank, world, dist):
     return line
 
 
+def reduce_over_ranks(maxes, sums, dist, device):
+    """Max of `maxes` and sum of `sums` over all ranks (no-op on one rank).  Only timings and
+    byte counts cross ranks: the decode itself has no collective."""
+    import torch
+    t = torch.tensor(maxes, dtype=torch.float64, device=device)
+    b = torch.tensor(sums, dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return [float(x) for x in t.cpu()], [float(x) for x in b.cpu()]
+
+
 def run_e2e(args, st, torch, binding, flush_l2):
-    """Every step: pinned host -> device copies of the step's inputs, the C-ABI calls, and
-    the device -> host read of the attention output, all between the CUDA events."""
+    """Every step: one host -> device copy of all the step's inputs (new-token q/k/v of every
+    layer, positions, slots, block tables, lengths), packed in one pinned buffer, then the C-ABI
+    calls on views of the device copy, then one device -> host copy of every layer's output,
+    all between the CUDA events.  The KV caches stay resident, as in a serving engine."""
     w = st.w
     stream = torch.cuda.current_stream()
     L = w.num_layers
-
-    def pinned(t):
-        return t.detach().cpu().pin_memory()
-
-    h_q = [pinned(st.q_src[i]) for i in range(L)]
-    h_k = [pinned(st.k[i]) for i in range(L)]
-    h_v = [pinned(st.v[i]) for i in range(L)]
-    h_pos, h_slot = pinned(st.positions), pinned(st.slots)
-    h_bt, h_ctx = pinned(st.block_tables), pinned(st.context_lens)
-    h_out = [torch.empty(st.out[i].shape, dtype=torch.bfloat16).pin_memory() for i in range(L)]
-    h2d = sum(x.numel() * x.element_size() for x in h_q + h_k + h_v + [h_pos, h_slot, h_bt, h_ctx])
-    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    items = [st.positions, st.slots, st.block_tables, st.context_lens]
+    for i in range(L):
+        items += [st.q_src[i], st.k[i], st.v[i]]
+    offs, total = [], 0
+    for t in items:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(total, dtype=torch.uint8, device="cuda")
+    views = []
+    for t, o in zip(items, offs):
+        n = t.numel() * t.element_size()
+        h_in[o:o + n].copy_(t.detach().reshape(-1).view(torch.uint8).cpu())
+        views.append(d_in[o:o + n].view(t.dtype).view(t.shape))
+    pos, slots, bt, ctx = views[:4]
+    q = [views[4 + 3 * i] for i in range(L)]
+    k = [views[5 + 3 * i] for i in range(L)]
+    v = [views[6 + 3 * i] for i in range(L)]
+    d_out = torch.empty((L,) + tuple(st.out[0].shape), dtype=torch.bfloat16, device="cuda")
+    h_out = torch.empty(d_out.shape, dtype=torch.bfloat16).pin_memory()
 
     def one():
-        st.positions.copy_(h_pos, non_blocking=True)
-        st.slots.copy_(h_slot, non_blocking=True)
-        st.block_tables.copy_(h_bt, non_blocking=True)
-        st.context_lens.copy_(h_ctx, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         for i in range(L):
-            st.q[i].copy_(h_q[i], non_blocking=True)
-            st.k[i].copy_(h_k[i], non_blocking=True)
-            st.v[i].copy_(h_v[i], non_blocking=True)
-            st.rope_store(i)
-            st.decode(i)
-            h_out[i].copy_(st.out[i], non_blocking=True)
+            binding.rope_kv_store(q[i], k[i], v[i], pos, st.cos_sin, slots, st.k_cache[i],
+                                  st.v_cache[i])
+            binding.decode(q[i], st.k_cache[i], st.v_cache[i], bt, ctx, w.max_context_len, w.scale,
+                           partition_tokens=st.P, workspace=st.workspace, out=d_out[i])
+        h_out.copy_(d_out, non_blocking=True)
 
     for _ in range(2):
         one()
@@ -359,7 +372,7 @@ def run_e2e(args, st, torch, binding, flush_l2):
         b.record(stream)
     torch.cuda.synchronize()
     ms = float(np.sum([a.elapsed_time(b) for a, b in evs]))
-    return {"ms": ms, "h2d": int(h2d), "d2h": int(d2h)}
+    return {"ms": ms, "h2d": int(total), "d2h": int(h_out.numel() * h_out.element_size())}
 
 
 def config_of(w, st, world):

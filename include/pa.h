@@ -185,6 +185,17 @@ int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_ca
  */
 int pa_get_device_status(void* stream, uint32_t* flags);
 
+/*
+ * pa_selftest_wait_timeout -- exercise the bounded wait that guards every copy into shared
+ * memory.  Launches one warp that waits on an mbarrier nothing ever arrives on, for
+ * `limit_us` microseconds (1 .. 1,000,000); the wait gives up and raises PA_FLAG_TIMEOUT in
+ * the device status word, which pa_get_device_status() then reports as PA_ERR_TIMEOUT.  The
+ * GPU stays usable: nothing traps, faults or spins without limit.  (The decode kernel uses the
+ * same wait with a 1 s limit.)  No counterpart in the source pages: failure detection support.
+ * Returns PA_OK once launched, PA_ERR_RANGE for a bad limit, PA_ERR_CUDA on a launch error.
+ */
+int pa_selftest_wait_timeout(uint32_t limit_us, void* stream);
+
 /* Human-readable name of a PA_* return code (static storage, never NULL). */
 const char* pa_status_string(int status);
 

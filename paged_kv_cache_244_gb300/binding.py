@@ -66,6 +66,8 @@ def lib():
         L.pa_decode.restype = i
         L.pa_get_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
         L.pa_get_device_status.restype = i
+        L.pa_selftest_wait_timeout.argtypes = [ctypes.c_uint32, p]
+        L.pa_selftest_wait_timeout.restype = i
         L.pa_status_string.argtypes = [i]
         L.pa_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -183,6 +185,12 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len, sca
         ws_bytes, _dev_ptr(out, "out", bf), _stream(stream))
     _check(rc, "pa_decode")
     return out
+
+
+def selftest_wait_timeout(limit_us: int = 1000, stream=None):
+    """Launch the bounded-wait self-test (a wait that must run out); read the result with
+    get_device_status(), which then reports PA_ERR_TIMEOUT with PA_FLAG_TIMEOUT set."""
+    _check(lib().pa_selftest_wait_timeout(int(limit_us), _stream(stream)), "pa_selftest_wait_timeout")
 
 
 def get_device_status(stream=None) -> tuple[int, int]:

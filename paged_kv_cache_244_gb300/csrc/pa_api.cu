@@ -189,6 +189,16 @@ int pa_get_device_status(void* stream, uint32_t* flags) {
   return PA_OK;
 }
 
+int pa_selftest_wait_timeout(uint32_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return PA_ERR_RANGE;
+  unsigned* status = nullptr;
+  if (const int rc = status_word(&status)) return rc;
+  return pa::launch_wait_selftest(status, static_cast<uint64_t>(limit_us) * 1000ull,
+                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
 const char* pa_status_string(int status) {
   switch (status) {
     case PA_OK: return "PA_OK";

@@ -73,14 +73,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Wait for phase `parity` of the barrier to complete, for at most kWaitLimitNs.
+// Wait for phase `parity` of the barrier to complete, for at most limit_ns of %globaltimer.
 // Returns false on timeout (the caller raises PA_FLAG_TIMEOUT and stops using the stage).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 255u) == 0u && global_ns() - t0 > limit_ns) return false;
   }
 }
 

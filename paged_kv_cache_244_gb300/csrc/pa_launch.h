@@ -55,6 +55,7 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_rope_kv_store(const RopeArgs& a, cudaStream_t stream);
+cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace pa

@@ -69,7 +69,27 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_store_kernel(const Ro
   dst[32 + lane] = pack_bf16x2(r2, r3);
 }
 
+// Self-test of the bounded wait every kernel here uses on its shared-memory copies: one warp
+// initialises an mbarrier that nothing will ever arrive on and waits on it with the given
+// limit.  The wait must give up and raise PA_FLAG_TIMEOUT; nothing faults and nothing hangs.
+__global__ void wait_selftest_kernel(unsigned* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool done = mbar_wait_bounded(b, 0u, limit_ns);
+  if (!done && threadIdx.x == 0) raise_flag(status, PA_FLAG_TIMEOUT);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope_kv_store(const RopeArgs& a, cudaStream_t stream) {
   const long long warps = static_cast<long long>(a.num_tokens) * (a.num_q_heads + a.num_kv_heads);

@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for must in ("pa_rope_kv_store", "pa_decode", "pa_decode_workspace_size",
-                 "pa_decode_partition_tokens", "pa_get_device_status", "pa_status_string"):
+                 "pa_decode_partition_tokens", "pa_get_device_status", "pa_status_string",
+                 "pa_selftest_wait_timeout", "pa_decode_static_workspace"):
         assert must in names
 
 
@@ -119,6 +120,12 @@ def test_partition_choice_and_workspace_size(L):
     assert b.decode_workspace_size(12, 2, 2, 40) == (12 + 4) * 6 * row
     assert b.decode_workspace_size(12, 2, 64, 4096) == (2048 + 128) * 6 * row
     assert b.decode_workspace_size(12, 2, 4, 32768, 100) == 0
+
+
+def test_selftest_rejects_bad_limits_on_the_host(L):
+    from paged_kv_cache_244_gb300 import binding as b
+    assert L.pa_selftest_wait_timeout(0, None) == b.PA_ERR_RANGE
+    assert L.pa_selftest_wait_timeout(2000000, None) == b.PA_ERR_RANGE
 
 
 def test_status_strings(L):

@@ -230,3 +230,19 @@ def test_bad_slot_and_position_are_flagged(pa, orc):
     assert flags & pa.PA_FLAG_SLOT_OOB and flags & pa.PA_FLAG_POSITION_OOB
     assert np.array_equal(host_bits(d.v_cache), before_v)   # nothing was stored
     check_status_clean(pa)
+
+
+def test_bounded_wait_times_out_and_reports(pa):
+    """A wait on a barrier that nothing completes gives up, raises the timeout flag, and the
+    GPU keeps working afterwards (a decode right after still matches the oracle)."""
+    check_status_clean(pa)
+    pa.selftest_wait_timeout(2000)          # 2 ms
+    rc, flags = pa.get_device_status()
+    assert rc == pa.PA_ERR_TIMEOUT and flags == pa.PA_FLAG_TIMEOUT
+    check_status_clean(pa)
+    orc = oracle.default()
+    w = W.build("after_timeout", [40, 17], 16, 84)
+    q, kc, vc = oracle_store(orc, w)
+    ref, _ = orc.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    d = DeviceLayer(w, q=q, k_cache=kc, v_cache=vc)
+    assert_out_close(run_decode(pa, d, w), ref)
