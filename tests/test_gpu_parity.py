@@ -163,25 +163,29 @@ def test_decode_zero_context_gives_zero_rows(pa, orc):
     check_status_clean(pa)
 
 
-def test_decode_is_deterministic_with_a_reused_workspace(pa, orc):
-    """Repeated calls on one workspace give identical results (the workspace carries nothing
-    from one call to the next)."""
-    w = workload("mix64")
-    q, kc, vc = oracle_store(orc, w)
-    d = DeviceLayer(w, q=q, k_cache=kc, v_cache=vc)
-    ref, _ = orc.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale)
-    outs = []
-    for P in (0, 64, 0):
-        ws = pa.decode_workspace(d.q, d.k_cache, w.max_context_len, P)
-        ws.fill_(float("nan"))
-        for _ in range(3):
-            out = pa.decode(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens,
-                            w.max_context_len, w.scale, partition_tokens=P, workspace=ws)
-            torch.cuda.synchronize()
-            outs.append((P, host_bits(out)))
-    for P, o in outs:
-        assert_out_close(o, ref, f"P={P}")
-        assert np.array_equal(o, [x for p2, x in outs if p2 == P][0])
+def test_decode_reuses_one_workspace_across_shapes(pa, orc):
+    """One zero-filled workspace serves calls of different shapes and split modes in a row;
+    repeated calls give identical results."""
+    big = workload("mix64")
+    need = max(pa.decode_workspace_size(12, 2, big.num_seqs, big.max_context_len, P) for P in (0, 64))
+    ws = torch.zeros((need + 3) // 4, dtype=torch.float32, device="cuda")
+    cases = [("mix64", 0), ("tiny", 0), ("mix64", 64), ("long4", 512), ("mix64", 0)]
+    seen = {}
+    for name, P in cases:
+        w = workload(name)
+        q, kc, vc = oracle_store(orc, w)
+        ref, _ = orc.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale)
+        d = DeviceLayer(w, q=q, k_cache=kc, v_cache=vc)
+        assert pa.decode_workspace_size(12, 2, w.num_seqs, w.max_context_len, P) <= ws.numel() * 4
+        out = pa.decode(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens,
+                        w.max_context_len, w.scale, partition_tokens=P, workspace=ws)
+        torch.cuda.synchronize()
+        got = host_bits(out)
+        assert_out_close(got, ref, f"{name} P={P}")
+        if (name, P) in seen:
+            assert np.array_equal(got, seen[(name, P)])
+        seen[(name, P)] = got
+    check_status_clean(pa)
 
 
 # --------------------------------------------------------- device-side range checks ----
@@ -246,3 +250,34 @@ def test_bounded_wait_times_out_and_reports(pa):
     ref, _ = orc.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale)
     d = DeviceLayer(w, q=q, k_cache=kc, v_cache=vc)
     assert_out_close(run_decode(pa, d, w), ref)
+
+
+@pytest.mark.parametrize("P", [0, 16])
+def test_decode_replayed_from_a_cuda_graph(pa, orc, P):
+    """A graph freezes the call's arguments; every replay must still merge only its own
+    pieces (the workspace counters carry a per-call epoch that the kernel itself advances)."""
+    w = W.build("graph", [40, 300, 700, 17], 200, 85)
+    q, kc, vc = oracle_store(orc, w)
+    d = DeviceLayer(w, q=q, k_cache=kc, v_cache=vc)
+    ws = pa.decode_workspace(d.q, d.k_cache, w.max_context_len, P)
+    out = torch.empty_like(d.q)
+
+    def call():
+        pa.decode(d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, w.max_context_len,
+                  w.scale, partition_tokens=P, workspace=ws, out=out)
+
+    call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    rng = W.SplitMix64(86 + P)
+    for _ in range(3):
+        q2 = rng.normal_bf16(q.size, 1.0).reshape(q.shape)
+        d.q.copy_(dev_bf16(q2))
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref, _ = orc.decode(q2, kc, vc, w.block_tables, w.context_lens, w.scale)
+        assert_out_close(host_bits(out), ref, f"P={P}")
+    check_status_clean(pa)
