@@ -1,10 +1,13 @@
-"""Benchmark of one decode step of paged GQA attention: fused RoPE + KV store, then decode.
+"""Benchmark of one decode step of paged GQA attention: RoPE + KV store of the new token, then
+decode over the paged cache.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mix64] [--impl reference]
+                    [--split-step]
 
-A step is one pass of the whole hot path over one batch: pa_rope_kv_store of every
-sequence's new token, then pa_decode over every cached context, for each layer of the
-workload.  The metric is KV-cache bytes read per second: sum(context_lens) * Hkv * D * 2 B
+A step is one pass of the whole hot path over one batch, for each layer of the workload:
+pa_decode_step, which rotates and stores every sequence's new token and attends over every
+cached context in one launch (plus the merge of split contexts); or, with --split-step,
+pa_rope_kv_store followed by pa_decode.  The metric is KV-cache bytes read per second: sum(context_lens) * Hkv * D * 2 B
 (K and V) per layer per step, over the step's device time.  L2 is flushed between timed steps,
 outside the timed events, because the workloads' caches fit in L2: a 512 MiB write, then a
 read of the same buffer so that no dirty flush lines are written back inside the timed step.
@@ -14,9 +17,9 @@ The printed JSON line carries:
   e2e                  the same metric when every step also copies its inputs (new-token
                        q/k/v, positions, slots, block tables, lengths) from pinned host
                        memory and reads the output back, all inside the timed region;
-  roofline             pa_decode (its partition kernel plus the merge kernel when the
-                       context is split) timed alone with CUDA events, against the
-                       measured HBM copy bandwidth;
+  roofline             the step's decode call (its partition kernel plus the merge kernel)
+                       on one layer, timed alone with CUDA events, against the measured HBM
+                       copy bandwidth;
   cpu_baseline         the fp64 oracle on the host cores over a bounded sample.
 With --gpus N under torchrun each rank runs its own batch (weak scaling, no collective on
 the data path); value is all ranks' bytes over the slowest rank's time.
@@ -123,8 +126,8 @@ class ClockSampler:
 class DeviceStep:
     """A workload resident on the GPU and one step of the hot path over it."""
 
-    def __init__(self, w: W.Workload, torch, binding):
-        self.w, self.torch, self.pa = w, torch, binding
+    def __init__(self, w: W.Workload, torch, binding, fused: bool = True):
+        self.w, self.torch, self.pa, self.fused = w, torch, binding, fused
         dev = torch.device("cuda")
 
         def bf(a):
@@ -146,8 +149,9 @@ class DeviceStep:
         self.P = binding.decode_partition_tokens(w.num_q_heads, w.num_kv_heads, w.num_seqs,
                                                  w.max_context_len, w.partition_tokens)
         self.workspace = binding.decode_workspace(self.q[0], self.k_cache[0], w.max_context_len, self.P)
-        # per layer: the RoPE + store kernel, the decode kernel and the merge kernel
-        self.launches_per_step = L * 3
+        # per layer: the (fused) decode kernel and the merge kernel, plus the RoPE + store
+        # kernel when it runs apart
+        self.launches_per_step = L * (2 if fused else 3)
 
     def rope_store(self, i):
         self.pa.rope_kv_store(self.q[i], self.k[i], self.v[i], self.positions, self.cos_sin,
@@ -159,10 +163,20 @@ class DeviceStep:
                        self.context_lens, w.max_context_len, w.scale, partition_tokens=self.P,
                        workspace=self.workspace, out=self.out[i])
 
+    def decode_step(self, i):
+        w = self.w
+        self.pa.decode_step(self.q[i], self.k[i], self.v[i], self.cos_sin, self.k_cache[i],
+                            self.v_cache[i], self.block_tables, self.context_lens,
+                            w.max_context_len, w.scale, partition_tokens=self.P,
+                            workspace=self.workspace, out=self.out[i])
+
     def step(self):
         for i in range(self.w.num_layers):
-            self.rope_store(i)
-            self.decode(i)
+            if self.fused:
+                self.decode_step(i)
+            else:
+                self.rope_store(i)
+                self.decode(i)
 
 
 def run_gpu(args, rank, world, dist):
@@ -180,7 +194,7 @@ def run_gpu(args, rank, world, dist):
     w = base if rank == 0 else W.make(args.workload, seed=base.seed + 1000 * rank)
     if args.partition_tokens is not None:
         w.partition_tokens = args.partition_tokens
-    st = DeviceStep(w, torch, binding)
+    st = DeviceStep(w, torch, binding, fused=not args.split_step)
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     sink = torch.empty(1, dtype=torch.float32, device="cuda")
@@ -246,10 +260,12 @@ def run_gpu(args, rank, world, dist):
     clocks = sampler.summary(t_wall0, t_wall1)
     total_ms = float(np.sum(step_ms))
 
-    # pa_decode alone (roofline of the dominant kernel), same flush discipline
-    dec_ms = timed_loop(lambda: st.decode(0), args.steps)
+    # the step's decode call on one layer alone (roofline of the dominant kernel), same flush
+    # discipline; then the unfused calls for comparison
+    dec_ms = timed_loop(lambda: (st.decode_step(0) if st.fused else st.decode(0)), args.steps)
     dec_avg = float(np.mean(dec_ms))
     rope_ms = timed_loop(lambda: st.rope_store(0), max(3, args.steps // 4))
+    plain_ms = timed_loop(lambda: st.decode(0), max(3, args.steps // 4))
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, st, torch, binding, flush_l2)
@@ -288,7 +304,8 @@ def run_gpu(args, rank, world, dist):
         "tokens_per_s": round(tokens_per_s, 1),
         "config": cfg,
         "roofline": {
-            "kernel": "pa_decode (decode_partition_kernel + decode_merge_kernel)",
+            "kernel": ("pa_decode_step (decode_partition_kernel<fused> + decode_merge_kernel)"
+                       if st.fused else "pa_decode (decode_partition_kernel + decode_merge_kernel)"),
             "bound": "hbm",
             "achieved": round(achieved, 2),
             "peak": peak,
@@ -300,6 +317,7 @@ def run_gpu(args, rank, world, dist):
             "avg_launch_ms": round(dec_avg, 6),
         },
         "rope_kv_store_us": round(1e3 * float(np.median(rope_ms)), 3),
+        "pa_decode_us": round(1e3 * float(np.mean(plain_ms)), 3),
         "e2e": {"value": round(all_bytes * args.steps / (e2e_ms_max * 1e-3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e_ms_max / args.steps, 6)},
@@ -325,23 +343,30 @@ def reduce_over_ranks(maxes, sums, dist, device):
 
 def run_e2e(args, st, torch, binding, flush_l2):
     """Every step: one host -> device copy of all the step's inputs (new-token q/k/v of every
-    layer, positions, slots, block tables, lengths), packed in one pinned buffer, then the C-ABI
-    calls on views of the device copy, then one device -> host copy of every layer's output,
-    all between the CUDA events.  The KV caches stay resident, as in a serving engine."""
+    layer, block tables, lengths, and for the split step positions and slots), packed in one
+    pinned buffer, then the C-ABI calls on views of the device copy, then one device -> host
+    copy of every layer's output, all between the CUDA events.  The KV caches stay resident,
+    as in a serving engine."""
     w = st.w
     stream = torch.cuda.current_stream()
     L = w.num_layers
     items = [st.positions, st.slots, st.block_tables, st.context_lens]
     for i in range(L):
         items += [st.q_src[i], st.k[i], st.v[i]]
+    if st.fused:  # the fused step derives positions and slots from the lengths and tables
+        items[0] = items[1] = None
     offs, total = [], 0
     for t in items:
         offs.append(total)
-        total += (t.numel() * t.element_size() + 255) // 256 * 256
+        if t is not None:
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
     h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
     d_in = torch.empty(total, dtype=torch.uint8, device="cuda")
     views = []
     for t, o in zip(items, offs):
+        if t is None:
+            views.append(None)
+            continue
         n = t.numel() * t.element_size()
         h_in[o:o + n].copy_(t.detach().reshape(-1).view(torch.uint8).cpu())
         views.append(d_in[o:o + n].view(t.dtype).view(t.shape))
@@ -355,6 +380,11 @@ def run_e2e(args, st, torch, binding, flush_l2):
     def one():
         d_in.copy_(h_in, non_blocking=True)
         for i in range(L):
+            if st.fused:
+                binding.decode_step(q[i], k[i], v[i], st.cos_sin, st.k_cache[i], st.v_cache[i], bt,
+                                    ctx, w.max_context_len, w.scale, partition_tokens=st.P,
+                                    workspace=st.workspace, out=d_out[i])
+                continue
             binding.rope_kv_store(q[i], k[i], v[i], pos, st.cos_sin, slots, st.k_cache[i],
                                   st.v_cache[i])
             binding.decode(q[i], st.k_cache[i], st.v_cache[i], bt, ctx, w.max_context_len, w.scale,
@@ -391,6 +421,9 @@ def config_of(w, st, world):
         "l2": "flushed between timed steps (512 MiB write then read back, outside the events)",
         "parallelism": f"replicas x{world} (independent batches)",
     }
+    if st is not None:
+        c["step"] = ("pa_decode_step (RoPE + KV store fused into the decode launch)" if st.fused
+                     else "pa_rope_kv_store then pa_decode")
     if w.meta.get("shared_prefix_blocks"):
         c["unique_kv_bytes_per_step_per_gpu"] = w.unique_kv_bytes_per_layer() * w.num_layers
     return c
@@ -481,6 +514,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each call instead of a CUDA graph")
+    ap.add_argument("--split-step", action="store_true",
+                    help="pa_rope_kv_store then pa_decode instead of the fused pa_decode_step")
     ap.add_argument("--partition-tokens", type=int, default=None,
                     help="Flash-Decode partition size (default: the workload's, 0 = library choice)")
     ap.add_argument("--traffic", type=float, default=None,

@@ -18,6 +18,9 @@
  *            sequence has a block_table mapping logical block index -> physical block id.
  *         §3.2 Continuous Batching: append_slot gives every running sequence one new slot
  *            per decode step.
+ *         §3.4 Prefix Caching: blocks shared between sequences are reference counted and
+ *            copied before a write (copy-on-write), so the block a new token goes to is
+ *            never shared.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -176,6 +179,42 @@ int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_ca
               const int32_t* context_lens, int max_context_len, float scale,
               int partition_tokens, void* workspace, size_t workspace_bytes, void* out,
               void* stream);
+
+/*
+ * pa_decode_step -- one decode step of a layer in one launch: the RoPE + KV-cache store of
+ * each sequence's new token fused into pa_decode ([PV] §2: RoPE fused with the KV cache
+ * store, and the PagedAttention decode kernel; [ME] §3.2: the new token takes the next slot
+ * of its sequence, which is the last slot of its context).
+ *
+ * The result equals pa_rope_kv_store followed by pa_decode with, for every sequence s with
+ * n = context_lens[s] >= 1 (n counts the new token):
+ *   positions[s]    = n - 1,
+ *   slot_mapping[s] = block_tables[s][(n - 1) / 16] * 16 + (n - 1) % 16,
+ * except that q is NOT modified: the kernel rotates its own copy of q in registers.  So:
+ *   k_cache[slot][g] = rotate(k[s][g]) and v_cache[slot][g] = v[s][g], bit for bit what
+ *   pa_rope_kv_store writes; out = pa_decode over the updated caches with the rotated q.
+ * The block reached through block_tables[s][(n - 1) / 16] is read and written by this
+ * sequence only: it must not appear in another sequence's table within its context (the
+ * block of a sequence's newest token is never shared -- a shared block is copied before it
+ * is written, [ME] §3.4 copy-on-write).  Within that block, the slots before n - 1 are read
+ * and slot n - 1 is written by the same warp, in that order.
+ * Sequences with n == 0 store nothing and get a zero output row.
+ * Device-side errors: as pa_decode; and n - 1 >= max_pos -> that sequence's token is treated
+ * as pa_rope_kv_store treats it (q used unrotated, nothing stored), PA_FLAG_POSITION_OOB.
+ *
+ *   q                 [S][Hq][D] bf16, NOT yet rotated, read only
+ *   k, v              [S][Hkv][D] bf16, the new token's key and value, read only
+ *   cos_sin, max_pos  as for pa_rope_kv_store
+ *   k_cache, v_cache  [num_blocks][Hkv][16][D] bf16, read, and written at the new slots
+ *   everything else   as for pa_decode (same workspace size: pa_decode_workspace_size)
+ * Returns PA_OK or a PA_ERR_* code (nothing launched on error).  Launches one kernel, plus
+ * one merge kernel.
+ */
+int pa_decode_step(const pa_dims* dims, int num_seqs, const void* q, const void* k, const void* v,
+                   const float* cos_sin, int max_pos, void* k_cache, void* v_cache, int num_blocks,
+                   const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                   int max_context_len, float scale, int partition_tokens, void* workspace,
+                   size_t workspace_bytes, void* out, void* stream);
 
 /*
  * pa_get_device_status -- synchronise `stream`, then read and clear the calling thread's

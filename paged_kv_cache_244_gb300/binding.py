@@ -64,6 +64,9 @@ def lib():
         L.pa_decode_workspace_size.restype = ctypes.c_size_t
         L.pa_decode.argtypes = [pd, i, p, p, p, i, p, i, p, i, f, i, p, ctypes.c_size_t, p, p]
         L.pa_decode.restype = i
+        L.pa_decode_step.argtypes = [pd, i, p, p, p, p, i, p, p, i, p, i, p, i, f, i, p,
+                                     ctypes.c_size_t, p, p]
+        L.pa_decode_step.restype = i
         L.pa_get_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
         L.pa_get_device_status.restype = i
         L.pa_selftest_wait_timeout.argtypes = [ctypes.c_uint32, p]
@@ -184,6 +187,43 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len, sca
         int(max_context_len), float(scale), int(partition_tokens), _dev_ptr(workspace, "workspace"),
         ws_bytes, _dev_ptr(out, "out", bf), _stream(stream))
     _check(rc, "pa_decode")
+    return out
+
+
+def decode_step(q, k, v, cos_sin, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                scale, partition_tokens=0, workspace=None, out=None, stream=None):
+    """One fused decode step (pa_decode_step): RoPE + KV store of each sequence's new token at
+    position context_lens[s] - 1, then decode attention, in one launch.  Returns out.
+
+    q [S, Hq, D] bf16, NOT rotated (left unchanged); k, v [S, Hkv, D] bf16 (the new token);
+    cos_sin [max_pos, D] fp32; the rest as for decode().  The caches get the new K and V.
+    """
+    S, Hq, D = q.shape
+    nb, Hkv, B, D2 = k_cache.shape
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shape mismatch")
+    if tuple(k.shape) != (S, Hkv, D) or tuple(v.shape) != (S, Hkv, D):
+        raise ValueError("k / v shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables / context_lens shape mismatch")
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != D:
+        raise ValueError("cos_sin shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = decode_workspace(q, k_cache, max_context_len, partition_tokens)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    dims = make_dims(Hq, Hkv, D, B)
+    bf = torch.bfloat16
+    rc = lib().pa_decode_step(
+        ctypes.byref(dims), S, _dev_ptr(q, "q", bf), _dev_ptr(k, "k", bf), _dev_ptr(v, "v", bf),
+        _dev_ptr(cos_sin, "cos_sin", torch.float32), cos_sin.shape[0],
+        _dev_ptr(k_cache, "k_cache", bf), _dev_ptr(v_cache, "v_cache", bf), nb,
+        _dev_ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev_ptr(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
+        int(partition_tokens), _dev_ptr(workspace, "workspace"), ws_bytes, _dev_ptr(out, "out", bf),
+        _stream(stream))
+    _check(rc, "pa_decode_step")
     return out
 
 

@@ -72,6 +72,62 @@ int status_word(unsigned** out) {
   return PA_OK;
 }
 
+// Checks shared by pa_decode and pa_decode_step, and the decode arguments they launch with
+// (the fused-step fields left empty).  PA_OK with num_seqs == 0 means "nothing to do".
+int decode_args(const pa_dims* dims, int num_seqs, const void* q, const void* k_cache,
+                const void* v_cache, int num_blocks, const int32_t* block_tables, int max_blocks,
+                const int32_t* context_lens, int max_context_len, float scale, int partition_tokens,
+                void* workspace, size_t workspace_bytes, void* out, pa::DecodeArgs* a) {
+  if (const int rc = check_dims(dims)) return rc;
+  if (num_seqs < 0 || num_seqs > pa::kMaxDecodeSeqs) return PA_ERR_RANGE;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
+  if (num_blocks < 1 || max_blocks < 1 || max_context_len < 1) return PA_ERR_RANGE;
+  if (static_cast<long long>(max_context_len) > static_cast<long long>(max_blocks) * dims->block_size)
+    return PA_ERR_RANGE;
+  if (static_cast<long long>(num_blocks) * dims->num_kv_heads * dims->block_size > (1ll << 31))
+    return PA_ERR_RANGE;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return PA_ERR_RANGE;
+  const int P = check_partition(dims, num_seqs, max_context_len, partition_tokens);
+  if (P < 0) return P;
+  const size_t need = workspace_bytes_for(dims, num_seqs, max_context_len, P);
+  if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+  const void* ptrs[] = {q, k_cache, v_cache, block_tables, context_lens, out, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return PA_ERR_ALIGN;
+  unsigned* status = nullptr;
+  if (const int rc = status_word(&status)) return rc;
+
+  a->q = static_cast<const __nv_bfloat16*>(q);
+  a->k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  a->v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  a->block_tables = block_tables;
+  a->context_lens = context_lens;
+  a->out = static_cast<__nv_bfloat16*>(out);
+  // [rows][D] partial sums, then [rows] (max, sum) pairs; rows = need / ((D + 2) * 4).
+  float* ws = static_cast<float*>(workspace);
+  const size_t rows = need / ((static_cast<size_t>(dims->head_dim) + 2) * sizeof(float));
+  a->ws_o = ws;
+  a->ws_ml = reinterpret_cast<float2*>(ws + rows * dims->head_dim);
+  a->num_seqs = num_seqs;
+  a->num_q_heads = dims->num_q_heads;
+  a->num_kv_heads = dims->num_kv_heads;
+  a->num_blocks = num_blocks;
+  a->max_blocks = max_blocks;
+  a->max_context_len = max_context_len;
+  a->chunk_blocks = P / dims->block_size;
+  a->num_warps = 0;  // set by the launcher from the grid it picks
+  a->scale_log2 = scale * 1.4426950408889634f;
+  a->status = status;
+  a->k_new = nullptr;
+  a->v_new = nullptr;
+  a->cos_sin = nullptr;
+  a->max_pos = 0;
+  a->k_store = nullptr;
+  a->v_store = nullptr;
+  return PA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -128,48 +184,38 @@ int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_ca
               const int32_t* context_lens, int max_context_len, float scale,
               int partition_tokens, void* workspace, size_t workspace_bytes, void* out,
               void* stream) {
+  pa::DecodeArgs a;
+  const int rc = decode_args(dims, num_seqs, q, k_cache, v_cache, num_blocks, block_tables, max_blocks,
+                             context_lens, max_context_len, scale, partition_tokens, workspace,
+                             workspace_bytes, out, &a);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  return pa::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                 : PA_ERR_CUDA;
+}
+
+int pa_decode_step(const pa_dims* dims, int num_seqs, const void* q, const void* k, const void* v,
+                   const float* cos_sin, int max_pos, void* k_cache, void* v_cache, int num_blocks,
+                   const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                   int max_context_len, float scale, int partition_tokens, void* workspace,
+                   size_t workspace_bytes, void* out, void* stream) {
+  // The new token's arguments first (host checks only), then everything pa_decode checks.
   if (const int rc = check_dims(dims)) return rc;
   if (num_seqs < 0 || num_seqs > pa::kMaxDecodeSeqs) return PA_ERR_RANGE;
   if (num_seqs == 0) return PA_OK;
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_NULL;
-  if (num_blocks < 1 || max_blocks < 1 || max_context_len < 1) return PA_ERR_RANGE;
-  if (static_cast<long long>(max_context_len) > static_cast<long long>(max_blocks) * dims->block_size)
-    return PA_ERR_RANGE;
-  if (static_cast<long long>(num_blocks) * dims->num_kv_heads * dims->block_size > (1ll << 31))
-    return PA_ERR_RANGE;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return PA_ERR_RANGE;
-  const int P = check_partition(dims, num_seqs, max_context_len, partition_tokens);
-  if (P < 0) return P;
-  const size_t need = workspace_bytes_for(dims, num_seqs, max_context_len, P);
-  if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
-  const void* ptrs[] = {q, k_cache, v_cache, block_tables, context_lens, out, workspace};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return PA_ERR_ALIGN;
-  unsigned* status = nullptr;
-  if (const int rc = status_word(&status)) return rc;
-
+  if (!k || !v || !cos_sin) return PA_ERR_NULL;
+  if (max_pos < 1) return PA_ERR_RANGE;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(cos_sin)) return PA_ERR_ALIGN;
   pa::DecodeArgs a;
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
-  a.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
-  a.block_tables = block_tables;
-  a.context_lens = context_lens;
-  a.out = static_cast<__nv_bfloat16*>(out);
-  // [rows][D] partial sums, then [rows] (max, sum) pairs; rows = need / ((D + 2) * 4).
-  float* ws = static_cast<float*>(workspace);
-  const size_t rows = need / ((static_cast<size_t>(dims->head_dim) + 2) * sizeof(float));
-  a.ws_o = ws;
-  a.ws_ml = reinterpret_cast<float2*>(ws + rows * dims->head_dim);
-  a.num_seqs = num_seqs;
-  a.num_q_heads = dims->num_q_heads;
-  a.num_kv_heads = dims->num_kv_heads;
-  a.num_blocks = num_blocks;
-  a.max_blocks = max_blocks;
-  a.max_context_len = max_context_len;
-  a.chunk_blocks = P / dims->block_size;
-  a.num_warps = 0;  // set by the launcher from the grid it picks
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.status = status;
+  const int rc = decode_args(dims, num_seqs, q, k_cache, v_cache, num_blocks, block_tables, max_blocks,
+                             context_lens, max_context_len, scale, partition_tokens, workspace,
+                             workspace_bytes, out, &a);
+  if (rc != PA_OK) return rc;
+  a.k_new = static_cast<const __nv_bfloat16*>(k);
+  a.v_new = static_cast<const __nv_bfloat16*>(v);
+  a.cos_sin = cos_sin;
+  a.max_pos = max_pos;
+  a.k_store = static_cast<__nv_bfloat16*>(k_cache);
+  a.v_store = static_cast<__nv_bfloat16*>(v_cache);
   return pa::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
                                                                                  : PA_ERR_CUDA;
 }

@@ -160,4 +160,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// rotate_half RoPE of two adjacent rotation pairs: lo holds x[i], x[i+1], hi holds x[i+64],
+// x[i+65] (bf16), c and s the cos and sin of angles i and i+1.  In fp32, rounded to bf16 RNE:
+//   x'[i] = x[i] c - x[i+64] s,   x'[i+64] = x[i+64] c + x[i] s.
+// Every kernel that rotates goes through this one function, so they all agree bit for bit.
+__device__ __forceinline__ void rope_rotate_pairs(uint32_t& lo, uint32_t& hi, float2 c, float2 s) {
+  const float x0 = bf16lo(lo), x1 = bf16hi(lo), y0 = bf16lo(hi), y1 = bf16hi(hi);
+  const float r0 = __fmaf_rn(x0, c.x, -__fmul_rn(y0, s.x));
+  const float r1 = __fmaf_rn(x1, c.y, -__fmul_rn(y1, s.y));
+  const float r2 = __fmaf_rn(y0, c.x, __fmul_rn(x0, s.x));
+  const float r3 = __fmaf_rn(y1, c.y, __fmul_rn(x1, s.y));
+  lo = pack_bf16x2(r0, r1);
+  hi = pack_bf16x2(r2, r3);
+}
+
 }  // namespace pa

@@ -52,6 +52,15 @@ struct DecodeArgs {
   int num_warps;                    // warps of the partition kernel's grid (set at launch)
   float scale_log2;                 // softmax scale * log2(e)
   unsigned* status;
+  // Fused step only (k_new == nullptr for plain decode): q above is NOT yet rotated, and
+  // each sequence's new token -- position context_len - 1, the last slot of its context --
+  // is rotated and stored by the kernel that reads that slot's block.
+  const __nv_bfloat16* k_new;       // [S][Hkv][128]
+  const __nv_bfloat16* v_new;       // [S][Hkv][128]
+  const float* cos_sin;             // [max_pos][128]
+  int max_pos;
+  __nv_bfloat16* k_store;           // the caches again, writable: destination of the new token
+  __nv_bfloat16* v_store;
 };
 
 cudaError_t launch_rope_kv_store(const RopeArgs& a, cudaStream_t stream);

@@ -54,17 +54,29 @@ constexpr int kWarps = PA_DECODE_WARPS;
 constexpr int kStages = PA_DECODE_STAGES;
 constexpr int kHalfBytes = kBlockSize * 128;                // 16 rows x 64 bf16
 constexpr int kQBytes = 8 * kHeadDim * 2;                   // q rows of up to 8 heads
-constexpr int kStageBytes = 2 * kTileBytes + kQBytes;       // K tile + V tile + q rows
+// Fused step: behind the q rows, the new token's cos/sin row (fp32), k and v rows (bf16).
+constexpr int kCosSinOffset = 2 * kTileBytes + kQBytes;
+constexpr int kNewKOffset = kCosSinOffset + kHeadDim * 4;
+constexpr int kNewVOffset = kNewKOffset + kHeadDim * 2;
+// Stage: K tile + V tile + q rows (+ the fused step's rows), a multiple of 1024 bytes so that
+// every stage's swizzled halves stay on 1024-byte boundaries.
+template <bool kStep>
+constexpr int kStageBytes = kStep ? kNewVOffset + kHeadDim * 2 : 2 * kTileBytes + kQBytes;
+static_assert(kStageBytes<false> % 1024 == 0 && kStageBytes<true> % 1024 == 0, "stage alignment");
 constexpr int kDescOffset = kWarps * kStages * 8;           // after the mbarriers
 constexpr int kPrefixOffset = kDescOffset + kWarps * kStages * 16;
-constexpr int kTileBytesAll = kWarps * kStages * kStageBytes;
 
+// Job flags (low bits of a descriptor's flag word; valid tokens sit at bits 8-12).
 constexpr uint32_t kFirst = 1u, kLast = 2u, kWhole = 4u, kHasData = 8u;
+constexpr uint32_t kNew = 16u;   // fused step: the block holding the segment's new token
+constexpr uint32_t kRope = 32u;  // fused step: the sequence's position has a cos/sin row
 constexpr int kMinRangeBlocks = PA_DECODE_MIN_RANGE;
 
 __host__ __device__ inline int prefix_bytes(int num_seqs) { return ((num_seqs + 1) * 4 + 15) & ~15; }
+template <bool kStep>
 __host__ __device__ inline int smem_bytes(int num_seqs) {
-  return kPrefixOffset + prefix_bytes(num_seqs) + 1024 + kTileBytesAll;  // + 1024: alignment pad
+  // + 1024: alignment pad
+  return kPrefixOffset + prefix_bytes(num_seqs) + 1024 + kWarps * kStages * kStageBytes<kStep>;
 }
 
 // Flattened-axis ranges.  chunk > 0: range v = [v*chunk, (v+1)*chunk) clipped to T.  chunk == 0:
@@ -97,9 +109,11 @@ __device__ __forceinline__ int clamp_len(int len, int max_len) {
   return len < 0 ? 0 : (len > max_len ? max_len : len);
 }
 
+template <bool kStep>
 __global__ void __launch_bounds__(kWarps * 32, 1)
 decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
+  constexpr int kStageB = kStageBytes<kStep>;
   extern __shared__ unsigned char smem_raw[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -110,7 +124,7 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
   int* prefix = reinterpret_cast<int*>(smem_raw + kPrefixOffset);  // N_s, s = 0..S
   // 128-byte swizzled TMA destinations must sit on 1024-byte boundaries.
   const uint32_t tiles =
-      ((raw + kPrefixOffset + prefix_bytes(a.num_seqs) + 1023u) & ~1023u) + warp * kStages * kStageBytes;
+      ((raw + kPrefixOffset + prefix_bytes(a.num_seqs) + 1023u) & ~1023u) + warp * kStages * kStageB;
   if (lane == 0) {
     for (int st = 0; st < kStages; ++st) mbar_init(bars + 8 * st, 1);
     fence_mbar_init();
@@ -173,10 +187,11 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     long long x;          // first position
     int n;                // jobs in the window (0: none left)
     int blk, seg, fl, slot;
+    int pos;              // fused step: position of the sequence's new token
   };
   auto resolve = [&](Window& W) {
     W.blk = -1;
-    W.seg = W.fl = W.slot = 0;
+    W.seg = W.fl = W.slot = W.pos = 0;
     if (W.n == 0 || lane >= W.n) return;
     const long long x0 = R.begin(W.v), x1 = R.begin(W.v + 1);
     const long long p = W.x + lane;
@@ -197,8 +212,13 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     W.blk = a.block_tables[static_cast<size_t>(s) * a.max_blocks + j];
     W.seg = s * Hkv + g;
     const int valid = min(kBlockSize, len - j * kBlockSize);
-    const uint32_t flags = ((p == x0 || j == 0) ? kFirst : 0u) | ((p == x1 - 1 || j == ns - 1) ? kLast : 0u) |
-                           ((Xi >= x0 && Xi + ns <= x1) ? kWhole : 0u);
+    uint32_t flags = ((p == x0 || j == 0) ? kFirst : 0u) | ((p == x1 - 1 || j == ns - 1) ? kLast : 0u) |
+                     ((Xi >= x0 && Xi + ns <= x1) ? kWhole : 0u);
+    if (kStep) {
+      W.pos = len - 1;
+      if (j == ns - 1) flags |= kNew;
+      if (W.pos < a.max_pos) flags |= kRope;  // len >= 1 here, so pos >= 0
+    }
     W.fl = static_cast<int>(flags | (static_cast<uint32_t>(valid) << 8));
     W.slot = W.v + W.seg;
   };
@@ -235,15 +255,23 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int seg = __shfl_sync(kFullMask, cur.seg, pk);
     const int fl = __shfl_sync(kFullMask, cur.fl, pk);
     const int slot = __shfl_sync(kFullMask, cur.slot, pk);
+    const int pos = kStep ? __shfl_sync(kFullMask, cur.pos, pk) : 0;
     ++pk;
     const bool ok = blk >= 0 && blk < a.num_blocks;
     const bool first = (fl & kFirst) != 0;
     if (lane == 0) {
       if (!ok) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
-      descs[st] = make_int4(seg, fl | (ok ? static_cast<int>(kHasData) : 0), slot, 0);
+      // Fused step: a position without a cos/sin row leaves the token as the store kernel
+      // would -- q unrotated, nothing stored.
+      const bool rope = kStep && (fl & kRope);
+      if (kStep && (fl & kNew) && !rope) raise_flag(a.status, PA_FLAG_POSITION_OOB);
+      const bool fresh = rope && ok && (fl & kNew);  // the new token's K and V land in this tile
+      const bool trig = rope && (first || fresh);    // stage the cos/sin row
+      descs[st] = make_int4(seg, fl | (ok ? static_cast<int>(kHasData) : 0), slot, blk);
       const uint32_t bar = bars + 8 * st;
-      const uint32_t dst = tiles + st * kStageBytes;
-      const uint32_t bytes = (ok ? 2u * kTileBytes : 0u) + (first ? static_cast<uint32_t>(G) * 256u : 0u);
+      const uint32_t dst = tiles + st * kStageB;
+      const uint32_t bytes = (ok ? 2u * kTileBytes : 0u) + (first ? static_cast<uint32_t>(G) * 256u : 0u) +
+                             (trig ? kHeadDim * 4u : 0u) + (fresh ? kHeadDim * 4u : 0u);
       const int s = seg / Hkv;
       const int g = seg - s * Hkv;
       fence_proxy_async_smem();
@@ -259,6 +287,13 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (first) {
           const size_t head0 = static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(g) * G;
           bulk_copy_g2s(dst + 2 * kTileBytes, a.q + head0 * kHeadDim, static_cast<uint32_t>(G) * 256u, bar);
+        }
+        if (trig)
+          bulk_copy_g2s(dst + kCosSinOffset, a.cos_sin + static_cast<size_t>(pos) * kHeadDim, kHeadDim * 4u, bar);
+        if (fresh) {
+          const size_t row = (static_cast<size_t>(s) * Hkv + g) * kHeadDim;
+          bulk_copy_g2s(dst + kNewKOffset, a.k_new + row, kHeadDim * 2u, bar);
+          bulk_copy_g2s(dst + kNewVOffset, a.v_new + row, kHeadDim * 2u, bar);
         }
       } else {
         mbar_arrive(bar);
@@ -282,8 +317,9 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
   auto consume = [&](int st) {
     const int4 d = descs[st];
     const uint32_t fl = static_cast<uint32_t>(d.y);
-    const uint32_t kt = tiles + st * kStageBytes;
+    const uint32_t kt = tiles + st * kStageB;
     const uint32_t vt = kt + 2 * kHalfBytes;
+    unsigned char* const stage = smem_raw + (kt - raw);  // generic address of the stage
     if (fl & kFirst) {
       // q rows sit unswizzled at 256-byte stride; rows >= G are not real heads.
       const uint32_t qt = kt + 2 * kTileBytes + static_cast<uint32_t>(r * 256);
@@ -291,6 +327,19 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
       for (int k2 = 0; k2 < 4; ++k2)
         ldsm_x4(qt + (4 * k2 + mi) * 16, qb[2 * k2][0], qb[2 * k2][1], qb[2 * k2 + 1][0],
                 qb[2 * k2 + 1][1]);
+      if (kStep && (fl & kRope)) {
+        // RoPE on the B fragments: dims d, d+1 (d = 16kk + 8j + 2cq) sit in qb[kk][j] and their
+        // rotation partners d+64, d+65 in qb[kk+4][j] of the same lane.
+        const float* cs = reinterpret_cast<const float*>(stage + kCosSinOffset);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int dd = 16 * kk + 8 * j + 2 * cq;
+            rope_rotate_pairs(qb[kk][j], qb[kk + 4][j], *reinterpret_cast<const float2*>(cs + dd),
+                              *reinterpret_cast<const float2*>(cs + 64 + dd));
+          }
+      }
       if (gq >= G) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) qb[kk][0] = qb[kk][1] = 0u;
@@ -302,6 +351,36 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     if (fl & kHasData) {
       const int valid = static_cast<int>(fl >> 8);
+      if (kStep && (fl & kNew) && (fl & kRope)) {
+        // The new token (row valid - 1 of this tile): rotate its k, write k and v into the
+        // staged tiles before they are read, and store both into the cache slot.
+        const int row = valid - 1;
+        const uint32_t* kn = reinterpret_cast<const uint32_t*>(stage + kNewKOffset);
+        const uint32_t* vn = reinterpret_cast<const uint32_t*>(stage + kNewVOffset);
+        const float* cs = reinterpret_cast<const float*>(stage + kCosSinOffset);
+        uint32_t klo = kn[lane], khi = kn[32 + lane];  // dims 2l, 2l+1 and 2l+64, 2l+65
+        rope_rotate_pairs(klo, khi, reinterpret_cast<const float2*>(cs)[lane],
+                          reinterpret_cast<const float2*>(cs + 64)[lane]);
+        const uint32_t vlo = vn[lane], vhi = vn[32 + lane];
+        // byte 4l of the row in each 64-column half, through the 128-byte swizzle
+        const int off = row * 128 + ((((lane >> 2) ^ (row & 7)) << 4) | ((lane & 3) << 2));
+        *reinterpret_cast<uint32_t*>(stage + off) = klo;
+        *reinterpret_cast<uint32_t*>(stage + kHalfBytes + off) = khi;
+        *reinterpret_cast<uint32_t*>(stage + 2 * kHalfBytes + off) = vlo;
+        *reinterpret_cast<uint32_t*>(stage + 3 * kHalfBytes + off) = vhi;
+        const int s = d.x / Hkv;
+        const int g = d.x - s * Hkv;
+        const size_t crow = ((static_cast<size_t>(d.w) * Hkv + g) * kBlockSize + row) * kHeadDim;
+        uint32_t* kc = reinterpret_cast<uint32_t*>(a.k_store + crow);
+        uint32_t* vc = reinterpret_cast<uint32_t*>(a.v_store + crow);
+        kc[lane] = klo;
+        kc[32 + lane] = khi;
+        vc[lane] = vlo;
+        vc[32 + lane] = vhi;
+        // These generic writes precede a later TMA write into the same stage.
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
       // S^T = K q^T: rows = tokens, columns = heads.
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -579,8 +658,9 @@ bool cache_tensor_map(const void* cache, long long rows, CUtensorMap* out) {
 }
 
 // Persistent grid size for this device: SMs x resident CTAs per SM, capped so that the grid
-// has at most kMaxDecodeWarps warps (looked up once per device, at the largest shared-memory
-// footprint the kernel can ask for).
+// has at most kMaxDecodeWarps warps (looked up once per device and kernel variant, at the
+// largest shared-memory footprint the kernel can ask for).
+template <bool kStep>
 cudaError_t persistent_ctas(int* ctas) {
   static std::mutex mu;
   static int cached[64] = {};
@@ -590,13 +670,13 @@ cudaError_t persistent_ctas(int* ctas) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (!cached[dev]) {
-    const int smem = smem_bytes(kMaxDecodeSeqs);
-    err = cudaFuncSetAttribute(decode_partition_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = smem_bytes<kStep>(kMaxDecodeSeqs);
+    err = cudaFuncSetAttribute(decode_partition_kernel<kStep>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     int sms = 0, per_sm = 0;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_partition_kernel, kWarps * 32, smem);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_partition_kernel<kStep>, kWarps * 32, smem);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     cached[dev] = min(sms * per_sm, kMaxDecodeWarps / kWarps);
@@ -615,8 +695,9 @@ cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
   CUtensorMap tm_k, tm_v;
   if (!cache_tensor_map(a.k_cache, rows, &tm_k) || !cache_tensor_map(a.v_cache, rows, &tm_v))
     return cudaErrorInvalidValue;
+  const bool step = a.k_new != nullptr;
   int max_ctas = 0;
-  cudaError_t err = persistent_ctas(&max_ctas);
+  cudaError_t err = step ? persistent_ctas<true>(&max_ctas) : persistent_ctas<false>(&max_ctas);
   if (err != cudaSuccess) return err;
   // No more CTAs than there can be ranges.
   const long long jobs_bound = static_cast<long long>(a.num_seqs) * a.num_kv_heads *
@@ -631,11 +712,12 @@ cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas));
   cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = smem_bytes(a.num_seqs);
+  cfg.dynamicSmemBytes = step ? smem_bytes<true>(a.num_seqs) : smem_bytes<false>(a.num_seqs);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, decode_partition_kernel, tm_k, tm_v, a);
+  err = step ? cudaLaunchKernelEx(&cfg, decode_partition_kernel<true>, tm_k, tm_v, a)
+             : cudaLaunchKernelEx(&cfg, decode_partition_kernel<false>, tm_k, tm_v, a);
   if (err != cudaSuccess) return err;
 
   const long long heads = static_cast<long long>(a.num_seqs) * a.num_q_heads;

@@ -58,15 +58,11 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_store_kernel(const Ro
   const float* row = a.cos_sin + static_cast<size_t>(pos) * kHeadDim;
   const float2 c = reinterpret_cast<const float2*>(row)[lane];        // cos of pairs 2l, 2l+1
   const float2 s = reinterpret_cast<const float2*>(row + 64)[lane];   // sin of pairs 2l, 2l+1
-  const uint32_t lo = src[lane];        // x[2l], x[2l+1]
-  const uint32_t hi = src[32 + lane];   // x[2l+64], x[2l+65]
-  const float x0 = bf16lo(lo), x1 = bf16hi(lo), y0 = bf16lo(hi), y1 = bf16hi(hi);
-  const float r0 = __fmaf_rn(x0, c.x, -__fmul_rn(y0, s.x));
-  const float r1 = __fmaf_rn(x1, c.y, -__fmul_rn(y1, s.y));
-  const float r2 = __fmaf_rn(y0, c.x, __fmul_rn(x0, s.x));
-  const float r3 = __fmaf_rn(y1, c.y, __fmul_rn(x1, s.y));
-  dst[lane] = pack_bf16x2(r0, r1);
-  dst[32 + lane] = pack_bf16x2(r2, r3);
+  uint32_t lo = src[lane];        // x[2l], x[2l+1]
+  uint32_t hi = src[32 + lane];   // x[2l+64], x[2l+65]
+  rope_rotate_pairs(lo, hi, c, s);
+  dst[lane] = lo;
+  dst[32 + lane] = hi;
 }
 
 // Self-test of the bounded wait every kernel here uses on its shared-memory copies: one warp

@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for must in ("pa_rope_kv_store", "pa_decode", "pa_decode_workspace_size",
                  "pa_decode_partition_tokens", "pa_get_device_status", "pa_status_string",
-                 "pa_selftest_wait_timeout", "pa_decode_static_workspace"):
+                 "pa_selftest_wait_timeout", "pa_decode_static_workspace", "pa_decode_step"):
         assert must in names
 
 
@@ -80,6 +80,34 @@ def test_decode_rejects_bad_arguments_on_the_host(L):
     assert decode_call(L, S=8193) == b.PA_ERR_RANGE
     for kw in ("q", "kc", "vc", "bt", "ctx", "out", "ws"):
         assert decode_call(L, **{kw: MIS_PTR}) == b.PA_ERR_ALIGN, kw
+
+
+def test_decode_step_rejects_bad_arguments_on_the_host(L):
+    from paged_kv_cache_244_gb300 import binding as b
+
+    def call(d=None, S=2, maxpos=64, nb=16, maxb=4, maxctx=40, scale=0.088, part=0, wsb=1 << 30,
+             **ptrs):
+        a = dict(q=OK_PTR, k=OK_PTR, v=OK_PTR, cs=OK_PTR, kc=OK_PTR, vc=OK_PTR, bt=OK_PTR,
+                 ctx=OK_PTR, ws=OK_PTR, out=OK_PTR)
+        a.update(ptrs)
+        d = dims() if d is None else d
+        return L.pa_decode_step(ctypes.byref(d), S, a["q"], a["k"], a["v"], a["cs"], maxpos,
+                                a["kc"], a["vc"], nb, a["bt"], maxb, a["ctx"], maxctx, scale, part,
+                                a["ws"], wsb, a["out"], None)
+
+    assert call(d=dims(d=64)) == b.PA_ERR_SHAPE
+    assert call(S=-1) == b.PA_ERR_RANGE
+    assert call(S=0) == b.PA_OK
+    assert call(S=8193) == b.PA_ERR_RANGE
+    for kw in ("q", "k", "v", "cs", "kc", "vc", "bt", "ctx", "out"):
+        assert call(**{kw: None}) == b.PA_ERR_NULL, kw
+    for kw in ("q", "k", "v", "cs", "kc", "vc", "bt", "ctx", "out", "ws"):
+        assert call(**{kw: MIS_PTR}) == b.PA_ERR_ALIGN, kw
+    assert call(maxpos=0) == b.PA_ERR_RANGE
+    assert call(maxctx=65) == b.PA_ERR_RANGE
+    assert call(part=24) == b.PA_ERR_RANGE
+    assert call(scale=-1.0) == b.PA_ERR_RANGE
+    assert call(part=16, wsb=100) == b.PA_ERR_WORKSPACE
 
 
 def test_rope_kv_store_rejects_bad_arguments_on_the_host(L):

@@ -254,8 +254,8 @@ def test_bounded_wait_times_out_and_reports(pa):
 
 @pytest.mark.parametrize("P", [0, 16])
 def test_decode_replayed_from_a_cuda_graph(pa, orc, P):
-    """A graph freezes the call's arguments; every replay must still merge only its own
-    pieces (the workspace counters carry a per-call epoch that the kernel itself advances)."""
+    """A graph freezes the call's arguments: every replay reads the q its buffer holds then
+    and gives that q's result (the workspace carries nothing from one call to the next)."""
     w = W.build("graph", [40, 300, 700, 17], 200, 85)
     q, kc, vc = oracle_store(orc, w)
     d = DeviceLayer(w, q=q, k_cache=kc, v_cache=vc)
