@@ -15,7 +15,7 @@
 #endif
 // Shortest range of the even split, in blocks.
 #ifndef PA_DECODE_MIN_RANGE
-#define PA_DECODE_MIN_RANGE 4
+#define PA_DECODE_MIN_RANGE 2
 #endif
 
 namespace pa {

@@ -7,7 +7,7 @@
 // Work.  Segment i = s * Hkv + g is the block list of sequence s for KV head g: n_s =
 // ceil(len_s / 16) blocks, starting at X_i = Hkv * N_s + g * n_s on one flattened axis of
 // T = Hkv * N_S block jobs (N_s = sum of n over the sequences before s).  The axis is cut into
-// V equal contiguous ranges ("virtual warps"): V = min(#warps, ceil(T / 4)) so that every warp of
+// V equal contiguous ranges ("virtual warps"): V = min(#warps, ceil(T / 2)) so that every warp of
 // the persistent grid gets the same number of blocks +-1, or ranges of a fixed C = P / 16 blocks
 // when the caller asks for P-token partitions.  A range cut by segment boundaries gives
 // pieces; piece (v, i) covers the part of segment i inside range v and owns partial slot v + i.
@@ -63,8 +63,11 @@ constexpr int kNewVOffset = kNewKOffset + kHeadDim * 2;
 template <bool kStep>
 constexpr int kStageBytes = kStep ? kNewVOffset + kHeadDim * 2 : 2 * kTileBytes + kQBytes;
 static_assert(kStageBytes<false> % 1024 == 0 && kStageBytes<true> % 1024 == 0, "stage alignment");
-constexpr int kDescOffset = kWarps * kStages * 8;           // after the mbarriers
+// Shared-memory header: the mbarriers (8 bytes each), then the int4 job descriptors on a
+// 16-byte boundary, then the prefix of block counts.
+constexpr int kDescOffset = (kWarps * kStages * 8 + 15) & ~15;
 constexpr int kPrefixOffset = kDescOffset + kWarps * kStages * 16;
+static_assert(kDescOffset % 16 == 0 && kPrefixOffset % 16 == 0, "descriptor alignment");
 
 // Job flags (low bits of a descriptor's flag word; valid tokens sit at bits 8-12).
 constexpr uint32_t kFirst = 1u, kLast = 2u, kWhole = 4u, kHasData = 8u;
@@ -233,8 +236,10 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     N.n = N.v < R.V ? static_cast<int>(min(32ll, R.begin(N.v + 1) - N.x)) : 0;
   };
 
+  // Range v goes to warp v / gridDim.x of CTA v % gridDim.x: when there are fewer ranges than
+  // warps they spread over all SMs (one warp each) rather than filling a few SMs.
   Window cur, nxt;
-  cur.v = blockIdx.x * kWarps + warp;
+  cur.v = warp * gridDim.x + blockIdx.x;
   cur.x = cur.v < R.V ? R.begin(cur.v) : 0;
   cur.n = cur.v < R.V ? static_cast<int>(min(32ll, R.begin(cur.v + 1) - cur.x)) : 0;
   resolve(cur);
@@ -517,19 +522,24 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
   }
 }
 
-// Merge of the pieces of one (sequence, query head) per warp.  The kernel is small enough
-// (registers, no shared memory) to sit on the SMs next to the partition kernel, so it starts as
-// soon as that kernel lets dependents launch and does everything that needs no partial result
-// first: where the segment's pieces are comes from N_s and N_S, computed from the sequence
-// lengths (inputs of the partition kernel, not outputs).  After the wait, one round of loads:
-// lane p reads (m_p, l_p) of piece p while every lane reads its 4 dims of the first kMergeBatch
-// piece rows.  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.  Empty sequences get zeros.
+// Merge of the pieces of split segments.  A warp takes 32 of the 128 dims of one (sequence,
+// query head), lane = dim, so that the rows of every piece of a head are loaded at once, one
+// 4-byte word per lane and piece: the merge after the partition kernel is one round trip to
+// L2, not one per batch of pieces.  The kernel is small enough (registers, no shared memory)
+// to sit on the SMs next to the partition kernel, so it starts as soon as that kernel lets
+// dependents launch and does everything that needs no partial result first: where the
+// segment's pieces are comes from N_s and N_S, computed from the sequence lengths (inputs of
+// the partition kernel, not outputs).  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
+// Empty sequences get zeros.
 constexpr int kMergeWarps = 8;
-constexpr int kMergeBatch = 8;
+constexpr int kMergeSplit = 4;   // warps per (sequence, query head)
+constexpr int kMergeBatch = 32;  // pieces loaded per round trip
 
 __global__ void __launch_bounds__(kMergeWarps * 32, 2) decode_merge_kernel(const DecodeArgs a) {
   const int lane = threadIdx.x & 31;
-  const int w = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);  // (sequence, query head)
+  const int gw = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  const int w = gw / kMergeSplit;                  // (sequence, query head)
+  const int quarter = gw - w * kMergeSplit;        // dims 32 quarter .. 32 quarter + 31
   const int S = a.num_seqs;
   if (w >= S * a.num_q_heads) return;
   const int Hkv = a.num_kv_heads;
@@ -551,10 +561,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) decode_merge_kernel(const
     total += __shfl_xor_sync(kFullMask, total, x);
   }
   const int ns = (clamp_len(a.context_lens[s], a.max_context_len) + kBlockSize - 1) / kBlockSize;
-  uint2* orow = reinterpret_cast<uint2*>(a.out + static_cast<size_t>(w) * kHeadDim) + lane;
+  const int dim = quarter * 32 + lane;
+  __nv_bfloat16* orow = a.out + static_cast<size_t>(w) * kHeadDim + dim;
   if (ns == 0) {  // empty context: zero row (after the partition kernel, which may read `out`)
     pdl_wait_prior_grid();
-    *orow = make_uint2(0u, 0u);
+    *orow = __float2bfloat16_rn(0.f);
     return;
   }
   const Ranges R = make_ranges(static_cast<long long>(Hkv) * total, a);
@@ -564,47 +575,35 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) decode_merge_kernel(const
   if (npieces <= 1) return;  // written directly by the partition kernel
   // piece p lives in slot v_first + p + segment; its row for this head is slot * G + hl
   const size_t row_base = (static_cast<size_t>(v_first) + s * Hkv + g) * G + hl;
-  const float2* ml = a.ws_ml + row_base;                   // stride G per piece
-  const float4* rows = reinterpret_cast<const float4*>(a.ws_o + row_base * kHeadDim) + lane;
-  const size_t stride4 = static_cast<size_t>(G) * 32;      // float4s per piece
+  const float2* ml = a.ws_ml + row_base;                               // stride G per piece
+  const float* rows = a.ws_o + row_base * kHeadDim + dim;              // stride G * 128
+  const size_t stride = static_cast<size_t>(G) * kHeadDim;
   pdl_wait_prior_grid();
 
-  float2 mine = lane < npieces ? ml[lane * G] : make_float2(-INFINITY, 0.f);
-  float4 rr[kMergeBatch];
+  float M = -INFINITY, L = 0.f, acc = 0.f;
+  for (int base = 0; base < npieces; base += kMergeBatch) {
+    const int n = min(kMergeBatch, npieces - base);
+    // one round trip: this lane's (m, l) of piece base + lane, and its dim of every piece row
+    const float2 mine = lane < n ? ml[(base + lane) * G] : make_float2(-INFINITY, 0.f);
+    float r[kMergeBatch];
 #pragma unroll
-  for (int u = 0; u < kMergeBatch; ++u)
-    rr[u] = u < npieces ? rows[u * stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
-  float M = mine.x;
-  for (int p = lane + 32; p < npieces; p += 32) M = fmaxf(M, ml[p * G].x);
+    for (int u = 0; u < kMergeBatch; ++u) r[u] = u < n ? rows[(base + u) * stride] : 0.f;
+    float Mb = mine.x;
 #pragma unroll
-  for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, x));
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int base = 0; base < npieces; base += 32) {
-    const float2 v = base == 0 ? mine : (base + lane < npieces ? ml[(base + lane) * G] : make_float2(-INFINITY, 0.f));
-    const float wmine = exp2f(v.x - M);  // 0 for lanes past the last piece
-    L = fmaf(wmine, v.y, L);
-    const int n = min(32, npieces - base);
-    for (int k = 0; k < n; k += kMergeBatch) {
-      if (base + k > 0) {
+    for (int x = 16; x > 0; x >>= 1) Mb = fmaxf(Mb, __shfl_xor_sync(kFullMask, Mb, x));
+    const float Mn = fmaxf(M, Mb);
+    const float rescale = exp2f(M - Mn);  // 0 on the first batch (M = -inf)
+    M = Mn;
+    const float wmine = exp2f(mine.x - M);  // 0 for lanes past the last piece
+    float lb = wmine * mine.y;
 #pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u)
-          rr[u] = k + u < n ? rows[(base + k + u) * stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+    for (int x = 16; x > 0; x >>= 1) lb += __shfl_xor_sync(kFullMask, lb, x);
+    L = fmaf(L, rescale, lb);
+    acc *= rescale;
 #pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        const float wk = __shfl_sync(kFullMask, wmine, (k + u) & 31);
-        acc.x = fmaf(wk, rr[u].x, acc.x);
-        acc.y = fmaf(wk, rr[u].y, acc.y);
-        acc.z = fmaf(wk, rr[u].z, acc.z);
-        acc.w = fmaf(wk, rr[u].w, acc.w);
-      }
-    }
+    for (int u = 0; u < kMergeBatch; ++u) acc = fmaf(__shfl_sync(kFullMask, wmine, u), r[u], acc);
   }
-#pragma unroll
-  for (int x = 16; x > 0; x >>= 1) L += __shfl_xor_sync(kFullMask, L, x);
-  const float inv = 1.f / L;
-  *orow = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  *orow = __float2bfloat16_rn(acc / L);
 }
 
 // ---- host side ------------------------------------------------------------------------
@@ -699,11 +698,12 @@ cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
   int max_ctas = 0;
   cudaError_t err = step ? persistent_ctas<true>(&max_ctas) : persistent_ctas<false>(&max_ctas);
   if (err != cudaSuccess) return err;
-  // No more CTAs than there can be ranges.
+  // No more CTAs than there can be ranges (ranges are dealt to the CTAs one at a time).
   const long long jobs_bound = static_cast<long long>(a.num_seqs) * a.num_kv_heads *
                                ((a.max_context_len + kBlockSize - 1) / kBlockSize);
-  const long long want = a.chunk_blocks ? (jobs_bound + a.chunk_blocks - 1) / a.chunk_blocks : jobs_bound;
-  const long long ctas = min(static_cast<long long>(max_ctas), (want + kWarps - 1) / kWarps);
+  const long long want = a.chunk_blocks ? (jobs_bound + a.chunk_blocks - 1) / a.chunk_blocks
+                                        : (jobs_bound + kMinRangeBlocks - 1) / kMinRangeBlocks;
+  const long long ctas = min(static_cast<long long>(max_ctas), want);
   a.num_warps = static_cast<int>(ctas) * kWarps;
 
   cudaLaunchAttribute attr[1];
@@ -720,9 +720,9 @@ cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
              : cudaLaunchKernelEx(&cfg, decode_partition_kernel<false>, tm_k, tm_v, a);
   if (err != cudaSuccess) return err;
 
-  const long long heads = static_cast<long long>(a.num_seqs) * a.num_q_heads;
+  const long long merge_warps = static_cast<long long>(a.num_seqs) * a.num_q_heads * kMergeSplit;
   cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(static_cast<unsigned>((heads + kMergeWarps - 1) / kMergeWarps));
+  mcfg.gridDim = dim3(static_cast<unsigned>((merge_warps + kMergeWarps - 1) / kMergeWarps));
   mcfg.blockDim = dim3(kMergeWarps * 32);
   mcfg.stream = stream;
   mcfg.attrs = attr;
