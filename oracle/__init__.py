@@ -61,9 +61,35 @@ class Oracle:
         lib.orc_decode.restype = i
         lib.orc_decode_partitioned.argtypes = [i, i, i, i, i, p, p, p, i, p, i, p, d, i, i, p]
         lib.orc_decode_partitioned.restype = i
+        lib.orc_copy_blocks.argtypes = [i, ctypes.c_int64, p, ctypes.c_int64, p, ctypes.c_int64, p, i]
+        lib.orc_copy_blocks.restype = ctypes.c_int64
         lib.orc_hardware_threads.argtypes = []
         lib.orc_hardware_threads.restype = i
         self.lib = lib
+
+    def copy_blocks(self, src, dst, pairs) -> int:
+        """Block copy (copy-on-write, swap out / in): for each (from, to) row of `pairs` and
+        each pool index c, dst[c][to] = src[c][from].  src, dst: lists of equally shaped
+        [num_blocks, ...] uint16 arrays (dst written in place).  Returns the pairs skipped
+        because a block id is outside its pool."""
+        assert len(src) == len(dst)
+        for a in list(src) + list(dst):
+            assert a.dtype == np.uint16 and a.flags.c_contiguous
+        block_elems = int(np.prod(src[0].shape[1:])) if src else 1
+        for a in list(src) + list(dst):
+            assert int(np.prod(a.shape[1:])) == block_elems
+        pairs = _c(pairs, np.int64).reshape(-1, 2)
+        arr = ctypes.c_void_p * max(1, len(src))
+        sp = arr(*[a.ctypes.data for a in src])
+        dp = arr(*[a.ctypes.data for a in dst])
+        src_blocks = src[0].shape[0] if src else 0
+        dst_blocks = dst[0].shape[0] if dst else 0
+        rc = self.lib.orc_copy_blocks(len(src), block_elems, ctypes.cast(sp, ctypes.c_void_p),
+                                      src_blocks, ctypes.cast(dp, ctypes.c_void_p), dst_blocks,
+                                      _ptr(pairs), pairs.shape[0])
+        if rc < 0:
+            raise ValueError("orc_copy_blocks rejected its arguments")
+        return int(rc)
 
     def hardware_threads(self) -> int:
         return int(self.lib.orc_hardware_threads())

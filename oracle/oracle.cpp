@@ -315,6 +315,38 @@ int orc_decode_partitioned(int S, int Hq, int Hkv, int D, int B, const uint16_t*
   return 0;
 }
 
+// Block copy between two block pools: copy-on-write inside one pool, swap out / swap in
+// between the GPU pool and a CPU pool.  ("从零实现 LLM 推理引擎：深挖 vLLM 的六大核心优化",
+// §3.4 Prefix Caching / Copy-on-Write: a block shared by several sequences (ref_count > 1) is
+// replaced, before it is written, by a freshly allocated block, which must hold the same
+// contents; §3.5 CPU Swap: swap_out moves a sequence's KV blocks to CPU memory and records the
+// mapping, swap_in allocates new GPU blocks and restores them from it.)
+//   src[c], dst[c]  pools of `src_blocks` / `dst_blocks` blocks of `block_elems` bf16 each,
+//                   for every cache c < num_caches (e.g. K and V of every layer)
+//   pairs           [num_pairs][2] = (source block, destination block)
+// For each pair in order and each cache: dst[c][pair.dst] = src[c][pair.src], every element.
+// A pair naming a block outside its pool is skipped.  Returns the number of pairs skipped,
+// or -1 on a bad argument.
+int64_t orc_copy_blocks(int num_caches, int64_t block_elems, const uint16_t* const* src,
+                        int64_t src_blocks, uint16_t* const* dst, int64_t dst_blocks,
+                        const int64_t* pairs, int num_pairs) {
+  if (num_caches < 0 || block_elems <= 0 || num_pairs < 0 || src_blocks < 0 || dst_blocks < 0)
+    return -1;
+  if (num_pairs > 0 && (!pairs || !src || !dst)) return -1;
+  int64_t skipped = 0;
+  for (int i = 0; i < num_pairs; ++i) {
+    const int64_t from = pairs[2 * i], to = pairs[2 * i + 1];
+    if (from < 0 || from >= src_blocks || to < 0 || to >= dst_blocks) {
+      ++skipped;
+      continue;
+    }
+    for (int c = 0; c < num_caches; ++c)
+      for (int64_t e = 0; e < block_elems; ++e)
+        dst[c][to * block_elems + e] = src[c][from * block_elems + e];
+  }
+  return skipped;
+}
+
 int orc_hardware_threads(void) {
   const unsigned n = std::thread::hardware_concurrency();
   return n ? static_cast<int>(n) : 1;

@@ -415,6 +415,58 @@ def check_flash_decode_merge_equals_unsplit(orc):
         assert np.allclose(got, ref, rtol=1e-12, atol=1e-14), P
 
 
+def check_copy_blocks_matches_fancy_indexing(orc):
+    """Block copy between pools = numpy's own indexed assignment, bit for bit (NaN and
+    signed-zero patterns included); blocks not named as destinations are untouched."""
+    rng = np.random.default_rng(7)
+    src = [rng.integers(0, 1 << 16, (40, 2, 16, D), dtype=np.uint16) for _ in range(5)]
+    dst = [rng.integers(0, 1 << 16, (30, 2, 16, D), dtype=np.uint16) for _ in range(5)]
+    want = [d.copy() for d in dst]
+    frm = rng.permutation(40)[:17]
+    to = rng.permutation(30)[:17]
+    for c in range(5):
+        want[c][to] = src[c][frm]
+    assert orc.copy_blocks(src, dst, np.stack([frm, to], axis=1)) == 0
+    for c in range(5):
+        assert np.array_equal(dst[c], want[c])
+
+
+def check_copy_blocks_skips_out_of_range_pairs(orc):
+    rng = np.random.default_rng(8)
+    src = [rng.integers(0, 1 << 16, (8, 1, 16, D), dtype=np.uint16) for _ in range(2)]
+    dst = [np.zeros((6, 1, 16, D), np.uint16) for _ in range(2)]
+    pairs = [[0, 0], [8, 1], [-1, 2], [3, 6], [4, -5], [7, 5]]
+    assert orc.copy_blocks(src, dst, pairs) == 4
+    for c in range(2):
+        assert np.array_equal(dst[c][0], src[c][0]) and np.array_equal(dst[c][5], src[c][7])
+        assert not dst[c][1:5].any()
+
+
+def check_swap_out_in_preserves_decode(orc):
+    """Swap every block of a batch out to a CPU pool and back in to other GPU blocks, with
+    the block tables remapped: the decode output is the same to the last bit of fp64."""
+    w, q, kc, vc = _tiny_after_store(orc)
+    S = w.num_seqs
+    used = sorted({int(b) for s in range(S)
+                   for b in w.block_tables[s, :(int(w.context_lens[s]) + 15) // 16]})
+    ref, _ = orc.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    assert np.isfinite(ref).all()
+    cpu = [np.zeros((len(used),) + kc.shape[1:], np.uint16) for _ in range(2)]
+    orc.copy_blocks([kc, vc], cpu, [[b, i] for i, b in enumerate(used)])           # swap out
+    rng = np.random.default_rng(9)
+    fresh = rng.permutation(kc.shape[0])[:len(used)]                                 # new ids
+    kc2 = np.full_like(kc, W.BF16_NAN)
+    vc2 = np.full_like(vc, W.BF16_NAN)
+    orc.copy_blocks(cpu, [kc2, vc2], [[i, int(f)] for i, f in enumerate(fresh)])    # swap in
+    remap = {b: int(f) for b, f in zip(used, fresh)}
+    bt = w.block_tables.copy()
+    for s in range(S):
+        for j in range((int(w.context_lens[s]) + 15) // 16):
+            bt[s, j] = remap[int(bt[s, j])]
+    got, _ = orc.decode(q, kc2, vc2, bt, w.context_lens, w.scale)
+    assert np.array_equal(got, ref)
+
+
 ALL_CHECKS = [
     check_bf16_widen,
     check_bf16_narrow_bruteforce,
@@ -434,4 +486,7 @@ ALL_CHECKS = [
     check_decode_empty_context,
     check_store_then_decode_matches_dense,
     check_flash_decode_merge_equals_unsplit,
+    check_copy_blocks_matches_fancy_indexing,
+    check_copy_blocks_skips_out_of_range_pairs,
+    check_swap_out_in_preserves_decode,
 ]

@@ -68,6 +68,12 @@ MUTANTS = {
                     "uint32_t u = static_cast<uint32_t>(b) << 15;"),
     "merge_drops_l": ("const double w = std::exp(mp[p] - M) * lp[p] / L;",
                       "const double w = std::exp(mp[p] - M) / L;"),
+    "copy_ids_swapped": ("dst[c][to * block_elems + e] = src[c][from * block_elems + e];",
+                         "dst[c][from * block_elems + e] = src[c][to * block_elems + e];"),
+    "copy_first_cache_only": ("for (int c = 0; c < num_caches; ++c)\n      for (int64_t e = 0;",
+                              "for (int c = 0; c < 1; ++c)\n      for (int64_t e = 0;"),
+    "copy_skips_last_element": ("for (int64_t e = 0; e < block_elems; ++e)",
+                                "for (int64_t e = 0; e + 1 < block_elems; ++e)"),
 }
 
 
