@@ -20,7 +20,11 @@ The printed JSON line carries:
   roofline             the step's decode call (its partition kernel plus the merge kernel)
                        on one layer, timed alone with CUDA events, against the measured HBM
                        copy bandwidth;
-  cpu_baseline         the fp64 oracle on the host cores over a bounded sample.
+  cpu_baseline         the fp64 oracle on the host cores over a bounded sample;
+  block_ops            pa_copy_blocks over K and V of 28 layers: copy-on-write inside the
+                       device pools, swap out / in of a 2048-token sequence to page-locked
+                       host pools, beside a plain memcpy of the same bytes (--no-block-ops
+                       skips it).
 With --gpus N under torchrun each rank runs its own batch (weak scaling, no collective on
 the data path); value is all ranks' bytes over the slowest rank's time.
 `--impl reference` times the oracle instead, on the host cores (rank 0 only).
@@ -51,20 +55,21 @@ METRIC = "paged GQA decode: KV-cache HBM GB/s (% of GB300 peak) and attention to
 # the step form and a hash of the CUDA sources it was taken on: once a kernel changes, the
 # hash no longer matches and roofline.traffic is reported as null until it is captured again.
 MEASURED_TRAFFIC = {
-    ("mix64", "fused", "ff1a4db073cd8e29"): 122113024 + 3113984 + 4183296,
+    ("mix64", "fused", "6ac3fcf213c93a6a"): 122113024 + 3113984 + 4183296,
 }
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources the decode kernels compile from (their file, the device helpers,
+    the launch header)."""
     import hashlib
     csrc = ROOT / "paged_kv_cache_244_gb300" / "csrc"
     h = hashlib.sha256()
-    for f in sorted(list(csrc.glob("*.cu")) + list(csrc.glob("*.cuh")) + list(csrc.glob("*.h")) +
-                    list((ROOT / "include").glob("*.h"))):
-        h.update(f.name.encode())
-        h.update(f.read_bytes())
+    for name in ("paged_decode.cu", "pa_device.cuh", "pa_launch.h"):
+        h.update(name.encode())
+        h.update((csrc / name).read_bytes())
     return h.hexdigest()[:16]
 
 
@@ -288,6 +293,7 @@ def run_gpu(args, rank, world, dist):
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, st, torch, binding, flush_l2)
+    blocks = None if args.no_block_ops else block_ops(torch, binding, flush_l2, timed_loop, w)
 
     rc, flags = binding.get_device_status()
     if rc != 0:
@@ -348,11 +354,60 @@ def run_gpu(args, rank, world, dist):
                 "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e_ms_max / args.steps, 6)},
         "gpu_launches": st.launches_per_step * args.steps,
+        "block_ops": blocks,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     return line
+
+
+def block_ops(torch, binding, flush_l2, timed_loop, w, layers=28, pool_blocks=1024, reps=20):
+    """pa_copy_blocks on the model's whole cache: K and V of `layers` layers, pools of
+    `pool_blocks` blocks each.  copy_on_write: pool_blocks / 2 pairs inside each device pool;
+    swap_out / swap_in: one 2048-token sequence (128 blocks) to page-locked host pools and
+    back, against a plain device<->host memcpy of the same bytes.  L2 flushed before each."""
+    dev = torch.device("cuda")
+    shape = (pool_blocks, w.num_kv_heads, W.BLOCK_SIZE, W.HEAD_DIM)
+    pools = [torch.randn(shape, device=dev).to(torch.bfloat16) for _ in range(2 * layers)]
+    block_bytes = w.num_kv_heads * W.BLOCK_SIZE * W.HEAD_DIM * 2
+    rng = np.random.default_rng(0x244)
+    half = pool_blocks // 2
+    cow = np.stack([rng.permutation(half), half + rng.permutation(half)], 1).astype(np.int64)
+    cow_pairs = torch.from_numpy(cow).to(dev)
+    nseq = 128
+    host = [torch.empty((nseq,) + shape[1:], dtype=torch.bfloat16).pin_memory() for _ in pools]
+    out_pairs = torch.from_numpy(np.stack([rng.permutation(pool_blocks)[:nseq], np.arange(nseq)],
+                                          1).astype(np.int64)).to(dev)
+    in_pairs = torch.from_numpy(np.stack([np.arange(nseq), rng.permutation(pool_blocks)[:nseq]],
+                                         1).astype(np.int64)).to(dev)
+    flat_dev = torch.empty(nseq * block_bytes * len(pools), dtype=torch.uint8, device=dev)
+    flat_host = torch.empty(flat_dev.numel(), dtype=torch.uint8).pin_memory()
+
+    def rate(fn, nbytes):
+        ms = float(np.median(timed_loop(fn, reps)))
+        return round(nbytes / (ms * 1e-3) / 1e9, 1), round(ms * 1e3, 2)
+
+    cow_bytes = 2 * cow.shape[0] * len(pools) * block_bytes          # read + write
+    swap_bytes = nseq * len(pools) * block_bytes                      # each way
+    cow_gbs, cow_us = rate(lambda: binding.copy_blocks(pools, pools, cow_pairs), cow_bytes)
+    out_gbs, out_us = rate(lambda: binding.copy_blocks(pools, host, out_pairs), swap_bytes)
+    in_gbs, in_us = rate(lambda: binding.copy_blocks(host, pools, in_pairs), swap_bytes)
+    d2h, _ = rate(lambda: flat_host.copy_(flat_dev, non_blocking=True), swap_bytes)
+    h2d, _ = rate(lambda: flat_dev.copy_(flat_host, non_blocking=True), swap_bytes)
+    rc, flags = binding.get_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after block copies: {rc} flags {flags:#x}")
+    peak, kind = hbm_peak()
+    return {
+        "caches": len(pools), "pool_blocks": pool_blocks, "block_bytes_per_cache": block_bytes,
+        "copy_on_write": {"pairs": int(cow.shape[0]), "GB/s": cow_gbs, "us": cow_us,
+                          "bytes": cow_bytes, "frac_of_hbm_copy_peak": round(cow_gbs / peak, 4)},
+        "swap_out": {"blocks": nseq, "GB/s": out_gbs, "us": out_us, "bytes": swap_bytes,
+                     "memcpy_d2h_GB/s": d2h},
+        "swap_in": {"blocks": nseq, "GB/s": in_gbs, "us": in_us, "bytes": swap_bytes,
+                    "memcpy_h2d_GB/s": h2d},
+    }
 
 
 def reduce_over_ranks(maxes, sums, dist, device):
@@ -545,6 +600,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each call instead of a CUDA graph")
+    ap.add_argument("--no-block-ops", action="store_true",
+                    help="skip the pa_copy_blocks measurements (copy-on-write, swap out / in)")
     ap.add_argument("--split-step", action="store_true",
                     help="pa_rope_kv_store then pa_decode instead of the fused pa_decode_step")
     ap.add_argument("--partition-tokens", type=int, default=None,

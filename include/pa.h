@@ -21,6 +21,8 @@
  *         §3.4 Prefix Caching: blocks shared between sequences are reference counted and
  *            copied before a write (copy-on-write), so the block a new token goes to is
  *            never shared.
+ *         §3.5 CPU Swap: swap_out moves a preempted sequence's KV blocks to CPU memory and
+ *            swap_in restores them into newly allocated GPU blocks.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -78,7 +80,9 @@ enum {
   PA_ERR_CUDA = -5,        /* a CUDA runtime call failed (the launch itself, or a query) */
   PA_ERR_DEVICE_OOB = -6,  /* pa_get_device_status: a kernel met an out-of-range value */
   PA_ERR_TIMEOUT = -7,     /* pa_get_device_status: a kernel gave up a bounded wait */
-  PA_ERR_ALIGN = -8        /* a pointer is not 16-byte aligned */
+  PA_ERR_ALIGN = -8,       /* a pointer is not 16-byte aligned */
+  PA_ERR_MEMORY = -9       /* a pointer is not memory the device can address (pageable host
+                              memory, or another GPU's memory) */
 };
 
 /* Flags of the device status word (bitwise OR of everything seen since the last read). */
@@ -215,6 +219,45 @@ int pa_decode_step(const pa_dims* dims, int num_seqs, const void* q, const void*
                    const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                    int max_context_len, float scale, int partition_tokens, void* workspace,
                    size_t workspace_bytes, void* out, void* stream);
+
+/* Most caches one pa_copy_blocks call can name (K and V of up to 128 layers). */
+#define PA_MAX_BLOCK_CACHES 256
+
+/*
+ * pa_copy_blocks -- copy whole KV-cache blocks between two block pools, for every cache of a
+ * model in one launch: copy-on-write inside one pool ([ME] §3.4: a block shared by several
+ * sequences is replaced, before it is written, by a freshly allocated block that must hold
+ * the same contents) and swap out / swap in between the GPU pool and a pool in CPU memory
+ * ([ME] §3.5).
+ *
+ * For each pair i, (from, to) = (block_pairs[2i], block_pairs[2i + 1]), and each cache c:
+ *   dst_caches[c][to] = src_caches[c][from]   (the whole block: every KV head, slot and dim,
+ *                                              bit for bit)
+ * Pairs are copied concurrently: the destination blocks must be distinct and none may be the
+ * source of another pair (true of copy-on-write and of swaps); otherwise the result is
+ * unspecified.
+ * Device-side errors: a pair naming a block outside its pool is skipped (nothing of it is
+ * read or written), PA_FLAG_BLOCK_ID_OOB.
+ *
+ *   dims            shape; one block of one cache is num_kv_heads * block_size * head_dim
+ *                   bf16 (block_size 16, head_dim 128: num_kv_heads tiles of 4 KiB)
+ *   num_caches      1 .. PA_MAX_BLOCK_CACHES (e.g. 2 * layers: K and V of every layer)
+ *   src_caches      HOST array of num_caches pool pointers, each [src_num_blocks][Hkv][16][D]
+ *   src_num_blocks  >= 1
+ *   dst_caches      HOST array of num_caches pool pointers, each [dst_num_blocks][Hkv][16][D]
+ *                   (the same pointers as src_caches for copy-on-write inside one pool)
+ *   dst_num_blocks  >= 1
+ *   block_pairs     [num_pairs][2] int64, in memory the device can read
+ *   num_pairs       >= 0 (0 is a no-op)
+ * Every pool pointer, and block_pairs, may be this GPU's memory or page-locked host memory
+ * (cudaHostAlloc, cudaHostRegister, PyTorch pin_memory), which the kernel reads and writes
+ * in place over the CPU-GPU link.  Anything else (pageable host memory, another GPU's
+ * memory) returns PA_ERR_MEMORY.  Pool pointers must be 16-byte aligned.
+ * Returns PA_OK or a PA_ERR_* code (nothing launched on error).  Launches one kernel.
+ */
+int pa_copy_blocks(const pa_dims* dims, int num_caches, const void* const* src_caches,
+                   int64_t src_num_blocks, void* const* dst_caches, int64_t dst_num_blocks,
+                   const int64_t* block_pairs, int num_pairs, void* stream);
 
 /*
  * pa_get_device_status -- synchronise `stream`, then read and clear the calling thread's

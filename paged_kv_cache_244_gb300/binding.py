@@ -24,6 +24,8 @@ PA_ERR_CUDA = -5
 PA_ERR_DEVICE_OOB = -6
 PA_ERR_TIMEOUT = -7
 PA_ERR_ALIGN = -8
+PA_ERR_MEMORY = -9
+PA_MAX_BLOCK_CACHES = 256
 
 PA_FLAG_BLOCK_ID_OOB = 0x1
 PA_FLAG_CONTEXT_LEN_OOB = 0x2
@@ -67,6 +69,8 @@ def lib():
         L.pa_decode_step.argtypes = [pd, i, p, p, p, p, i, p, p, i, p, i, p, i, f, i, p,
                                      ctypes.c_size_t, p, p]
         L.pa_decode_step.restype = i
+        L.pa_copy_blocks.argtypes = [pd, i, p, ctypes.c_int64, p, ctypes.c_int64, p, i, p]
+        L.pa_copy_blocks.restype = i
         L.pa_get_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
         L.pa_get_device_status.restype = i
         L.pa_selftest_wait_timeout.argtypes = [ctypes.c_uint32, p]
@@ -225,6 +229,52 @@ def decode_step(q, k, v, cos_sin, k_cache, v_cache, block_tables, context_lens, 
         _stream(stream))
     _check(rc, "pa_decode_step")
     return out
+
+
+def _pool_ptr(t: torch.Tensor, name: str):
+    """A block pool: a contiguous bf16 tensor on the GPU or in page-locked host memory."""
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or page-locked (pin_memory) host tensor")
+    return t.data_ptr()
+
+
+def copy_blocks(src_caches, dst_caches, block_pairs, stream=None):
+    """Whole-block copies (pa_copy_blocks): for each row (from, to) of block_pairs and each
+    cache c, dst_caches[c][to] = src_caches[c][from].  Copy-on-write inside one pool (pass the
+    same list twice) or swap out / in between GPU pools and page-locked host pools.
+
+    src_caches, dst_caches: equally long lists of [num_blocks, Hkv, B, D] bf16 tensors (CUDA
+    or pinned host; all sources one pool size, all destinations one pool size); block_pairs:
+    [n, 2] int64 (CUDA or pinned host).
+    """
+    if len(src_caches) != len(dst_caches) or not src_caches:
+        raise ValueError("src_caches and dst_caches must be non-empty lists of equal length")
+    n_src, Hkv, B, D = src_caches[0].shape
+    n_dst = dst_caches[0].shape[0]
+    for t in src_caches:
+        if tuple(t.shape) != (n_src, Hkv, B, D):
+            raise ValueError("source pools differ in shape")
+    for t in dst_caches:
+        if tuple(t.shape) != (n_dst, Hkv, B, D):
+            raise ValueError("destination pools differ in shape")
+    if block_pairs.dtype != torch.int64 or block_pairs.dim() != 2 or block_pairs.shape[1] != 2:
+        raise ValueError("block_pairs must be an [n, 2] int64 tensor")
+    if not block_pairs.is_contiguous() or not (block_pairs.is_cuda or block_pairs.is_pinned()):
+        raise ValueError("block_pairs must be contiguous, on the GPU or in pinned host memory")
+    n = len(src_caches)
+    arr = ctypes.c_void_p * n
+    src = arr(*[_pool_ptr(t, "src_caches") for t in src_caches])
+    dst = arr(*[_pool_ptr(t, "dst_caches") for t in dst_caches])
+    dims = make_dims(Hkv, Hkv, D, B)
+    rc = lib().pa_copy_blocks(ctypes.byref(dims), n, ctypes.cast(src, ctypes.c_void_p), n_src,
+                              ctypes.cast(dst, ctypes.c_void_p), n_dst,
+                              ctypes.c_void_p(block_pairs.data_ptr()), block_pairs.shape[0],
+                              _stream(stream))
+    _check(rc, "pa_copy_blocks")
 
 
 def selftest_wait_timeout(limit_us: int = 1000, stream=None):

@@ -128,6 +128,30 @@ int decode_args(const pa_dims* dims, int num_seqs, const void* q, const void* k_
   return PA_OK;
 }
 
+// Device address of a pointer the current GPU can dereference: its own memory, managed
+// memory or page-locked host memory.  PA_ERR_MEMORY for anything else.
+int device_address(const void* p, const void** out) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the (non-sticky) error the failed query recorded
+    return PA_ERR_MEMORY;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  switch (attr.type) {
+    case cudaMemoryTypeDevice:
+      if (attr.device != dev) return PA_ERR_MEMORY;
+      *out = attr.devicePointer;
+      return *out ? PA_OK : PA_ERR_MEMORY;
+    case cudaMemoryTypeManaged:
+    case cudaMemoryTypeHost:
+      *out = attr.devicePointer;
+      return *out ? PA_OK : PA_ERR_MEMORY;
+    default:
+      return PA_ERR_MEMORY;
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -220,6 +244,44 @@ int pa_decode_step(const pa_dims* dims, int num_seqs, const void* q, const void*
                                                                                  : PA_ERR_CUDA;
 }
 
+int pa_copy_blocks(const pa_dims* dims, int num_caches, const void* const* src_caches,
+                   int64_t src_num_blocks, void* const* dst_caches, int64_t dst_num_blocks,
+                   const int64_t* block_pairs, int num_pairs, void* stream) {
+  if (const int rc = check_dims(dims)) return rc;
+  if (num_pairs < 0) return PA_ERR_RANGE;
+  if (num_pairs == 0) return PA_OK;
+  if (num_caches < 1 || num_caches > PA_MAX_BLOCK_CACHES) return PA_ERR_RANGE;
+  if (src_num_blocks < 1 || dst_num_blocks < 1) return PA_ERR_RANGE;
+  if (!src_caches || !dst_caches || !block_pairs) return PA_ERR_NULL;
+  for (int c = 0; c < num_caches; ++c) {
+    if (!src_caches[c] || !dst_caches[c]) return PA_ERR_NULL;
+    if (!aligned16(src_caches[c]) || !aligned16(dst_caches[c])) return PA_ERR_ALIGN;
+  }
+  if (reinterpret_cast<uintptr_t>(block_pairs) % alignof(int64_t) != 0) return PA_ERR_ALIGN;
+  unsigned* status = nullptr;
+  if (const int rc = status_word(&status)) return rc;
+  pa::BlockCopyArgs a;
+  for (int c = 0; c < num_caches; ++c) {
+    const void* s = nullptr;
+    const void* d = nullptr;
+    if (const int rc = device_address(src_caches[c], &s)) return rc;
+    if (const int rc = device_address(dst_caches[c], &d)) return rc;
+    a.src[c] = static_cast<const uint4*>(s);
+    a.dst[c] = static_cast<uint4*>(const_cast<void*>(d));
+  }
+  const void* pairs = nullptr;
+  if (const int rc = device_address(block_pairs, &pairs)) return rc;
+  a.pairs = static_cast<const int64_t*>(pairs);
+  a.src_blocks = src_num_blocks;
+  a.dst_blocks = dst_num_blocks;
+  a.num_pairs = num_pairs;
+  a.num_caches = num_caches;
+  a.tiles_per_block = dims->num_kv_heads;
+  a.status = status;
+  return pa::launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                     : PA_ERR_CUDA;
+}
+
 int pa_get_device_status(void* stream, uint32_t* flags) {
   unsigned* status = nullptr;
   if (const int rc = status_word(&status)) return rc;
@@ -256,6 +318,7 @@ const char* pa_status_string(int status) {
     case PA_ERR_DEVICE_OOB: return "PA_ERR_DEVICE_OOB: a kernel met an out-of-range value";
     case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a kernel gave up a bounded wait";
     case PA_ERR_ALIGN: return "PA_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case PA_ERR_MEMORY: return "PA_ERR_MEMORY: a pointer is not memory this GPU can address";
     default: return "unknown pa status";
   }
 }

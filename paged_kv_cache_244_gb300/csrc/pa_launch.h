@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "pa.h"
+
 // Decode kernel shape: warps per CTA and shared-memory stages per warp.
 #ifndef PA_DECODE_WARPS
 #define PA_DECODE_WARPS 8
@@ -63,7 +65,20 @@ struct DecodeArgs {
   __nv_bfloat16* v_store;
 };
 
+// Whole-block copies between pools (copy-on-write, swap out / in).  Pool pointers are device
+// addresses (of device memory or of page-locked host memory).
+struct BlockCopyArgs {
+  const uint4* src[PA_MAX_BLOCK_CACHES];
+  uint4* dst[PA_MAX_BLOCK_CACHES];
+  const int64_t* pairs;             // [num_pairs][2] (from, to)
+  long long src_blocks, dst_blocks;
+  int num_pairs, num_caches;
+  int tiles_per_block;              // Hkv: 4 KiB (block, KV head) tiles per block of one cache
+  unsigned* status;
+};
+
 cudaError_t launch_rope_kv_store(const RopeArgs& a, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const BlockCopyArgs& a, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 

@@ -31,7 +31,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for must in ("pa_rope_kv_store", "pa_decode", "pa_decode_workspace_size",
                  "pa_decode_partition_tokens", "pa_get_device_status", "pa_status_string",
-                 "pa_selftest_wait_timeout", "pa_decode_static_workspace", "pa_decode_step"):
+                 "pa_selftest_wait_timeout", "pa_decode_static_workspace", "pa_decode_step",
+                 "pa_copy_blocks"):
         assert must in names
 
 
@@ -108,6 +109,31 @@ def test_decode_step_rejects_bad_arguments_on_the_host(L):
     assert call(part=24) == b.PA_ERR_RANGE
     assert call(scale=-1.0) == b.PA_ERR_RANGE
     assert call(part=16, wsb=100) == b.PA_ERR_WORKSPACE
+
+
+def test_copy_blocks_rejects_bad_arguments_on_the_host(L):
+    from paged_kv_cache_244_gb300 import binding as b
+    arr = ctypes.c_void_p * 4
+
+    def call(d=None, n=2, nsrc=8, ndst=8, npairs=3, src=None, dst=None, pairs=OK_PTR):
+        src = arr(OK_PTR, OK_PTR, OK_PTR, OK_PTR) if src is None else src
+        dst = arr(OK_PTR, OK_PTR, OK_PTR, OK_PTR) if dst is None else dst
+        d = dims(2, 2) if d is None else d
+        return L.pa_copy_blocks(ctypes.byref(d), n, ctypes.cast(src, ctypes.c_void_p), nsrc,
+                                ctypes.cast(dst, ctypes.c_void_p), ndst, pairs, npairs, None)
+
+    assert call(d=dims(2, 2, d=64)) == b.PA_ERR_SHAPE
+    assert call(npairs=-1) == b.PA_ERR_RANGE
+    assert call(npairs=0) == b.PA_OK
+    assert call(n=0) == b.PA_ERR_RANGE
+    assert call(n=b.PA_MAX_BLOCK_CACHES + 1) == b.PA_ERR_RANGE
+    assert call(nsrc=0) == b.PA_ERR_RANGE
+    assert call(ndst=0) == b.PA_ERR_RANGE
+    assert call(pairs=None) == b.PA_ERR_NULL
+    assert call(src=arr(OK_PTR, None, OK_PTR, OK_PTR)) == b.PA_ERR_NULL
+    assert call(dst=arr(OK_PTR, MIS_PTR, OK_PTR, OK_PTR)) == b.PA_ERR_ALIGN
+    assert call(pairs=P(0x10004)) == b.PA_ERR_ALIGN
+    assert L.pa_copy_blocks(ctypes.byref(dims(2, 2)), 2, None, 8, None, 8, OK_PTR, 1, None) == b.PA_ERR_NULL
 
 
 def test_rope_kv_store_rejects_bad_arguments_on_the_host(L):
