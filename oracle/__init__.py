@@ -61,11 +61,83 @@ class Oracle:
         lib.orc_decode.restype = i
         lib.orc_decode_partitioned.argtypes = [i, i, i, i, i, p, p, p, i, p, i, p, d, i, i, p]
         lib.orc_decode_partitioned.restype = i
+        lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_to_f64.restype = d
+        lib.orc_f64_to_e4m3.argtypes = [d]
+        lib.orc_f64_to_e4m3.restype = ctypes.c_uint8
+        lib.orc_quantize_cache.argtypes = [ctypes.c_int64, i, i, i, p, p, p]
+        lib.orc_quantize_cache.restype = i
+        lib.orc_rope_kv_store_fp8.argtypes = [i, i, i, i, i, p, p, p, p, p, i, p, p, p, i, p, p]
+        lib.orc_rope_kv_store_fp8.restype = i
+        lib.orc_decode_fp8.argtypes = [i, i, i, i, i, p, p, p, p, p, i, p, i, p, d, i, p, p]
+        lib.orc_decode_fp8.restype = i
         lib.orc_copy_blocks.argtypes = [i, ctypes.c_int64, p, ctypes.c_int64, p, ctypes.c_int64, p, i]
         lib.orc_copy_blocks.restype = ctypes.c_int64
         lib.orc_hardware_threads.argtypes = []
         lib.orc_hardware_threads.restype = i
         self.lib = lib
+
+    # ---- FP8 (E4M3) KV cache -----------------------------------------------------------
+    def e4m3_to_f64(self, code: int) -> float:
+        return float(self.lib.orc_e4m3_to_f64(int(code) & 0xFF))
+
+    def f64_to_e4m3(self, x: float) -> int:
+        """E4M3 code nearest to x, ties to even, saturating to +-448 (NaN stays NaN)."""
+        return int(self.lib.orc_f64_to_e4m3(float(x)))
+
+    def quantize_cache(self, cache_bits, scale) -> np.ndarray:
+        """E4M3 codes of a bf16 cache [num_blocks, Hkv, B, D] (bits) with one fp32 scale per
+        KV head: code of fp32(x) * fp32(1 / scale)."""
+        src = _c(cache_bits, np.uint16)
+        nb, Hkv, B, D = src.shape
+        scale = _c(scale, np.float32)
+        assert scale.shape == (Hkv,)
+        dst = np.empty(src.shape, np.uint8)
+        if self.lib.orc_quantize_cache(src.size, Hkv, B, D, _ptr(src), _ptr(scale), _ptr(dst)) != 0:
+            raise ValueError("orc_quantize_cache rejected its arguments")
+        return dst
+
+    def rope_kv_store_fp8(self, q, k, v, positions, cos_sin, slot_mapping, k_cache, v_cache,
+                          k_scale, v_scale):
+        """As rope_kv_store, into uint8 E4M3 caches with per-KV-head scales (in place)."""
+        q = np.array(q, dtype=np.uint16, copy=True, order="C")
+        k, v = _c(k, np.uint16), _c(v, np.uint16)
+        positions = _c(positions, np.int32)
+        cos_sin = _c(cos_sin, np.float32)
+        slot_mapping = _c(slot_mapping, np.int64)
+        k_scale, v_scale = _c(k_scale, np.float32), _c(v_scale, np.float32)
+        for c in (k_cache, v_cache):
+            assert c.dtype == np.uint8 and c.flags.c_contiguous
+        T, Hq, D = q.shape
+        nb, Hkv, B, D2 = k_cache.shape
+        assert D2 == D and k.shape == (T, Hkv, D) and v.shape == (T, Hkv, D)
+        assert k_scale.shape == (Hkv,) and v_scale.shape == (Hkv,)
+        rc = self.lib.orc_rope_kv_store_fp8(T, Hq, Hkv, D, B, _ptr(q), _ptr(k), _ptr(v),
+                                            _ptr(positions), _ptr(cos_sin), cos_sin.shape[0],
+                                            _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), nb,
+                                            _ptr(k_scale), _ptr(v_scale))
+        if rc != 0:
+            raise ValueError("orc_rope_kv_store_fp8 rejected its arguments")
+        return q
+
+    def decode_fp8(self, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                   scale, nthreads=0):
+        """Decode over uint8 E4M3 caches; returns (out fp64 [S, Hq, D], out bf16 bits)."""
+        q = _c(q, np.uint16)
+        kc, vc = _c(k_cache, np.uint8), _c(v_cache, np.uint8)
+        ks, vs = _c(k_scale, np.float32), _c(v_scale, np.float32)
+        bt = _c(block_tables, np.int32)
+        ctx = _c(context_lens, np.int32)
+        S, Hq, D = q.shape
+        nb, Hkv, B, _ = kc.shape
+        out = np.empty((S, Hq, D), np.float64)
+        outb = np.empty((S, Hq, D), np.uint16)
+        rc = self.lib.orc_decode_fp8(S, Hq, Hkv, D, B, _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks),
+                                     _ptr(vs), nb, _ptr(bt), bt.shape[1] if bt.ndim == 2 else 0,
+                                     _ptr(ctx), float(scale), int(nthreads), _ptr(out), _ptr(outb))
+        if rc != 0:
+            raise ValueError("orc_decode_fp8 rejected its arguments")
+        return out, outb
 
     def copy_blocks(self, src, dst, pairs) -> int:
         """Block copy (copy-on-write, swap out / in): for each (from, to) row of `pairs` and

@@ -79,6 +79,51 @@ uint16_t narrow_bf16(double x) {
   return static_cast<uint16_t>(u >> 16);
 }
 
+// FP8 E4M3 (the OCP "E4M3FN" format): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+// bits; exponent 0 holds the subnormals m/8 * 2^-6; S.1111.111 is NaN; no infinities, so the
+// largest finite magnitude is 1.75 * 2^8 = 448.
+double e4m3_value(uint8_t b) {
+  const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  double v;
+  if (e == 15 && m == 7) v = std::numeric_limits<double>::quiet_NaN();
+  else if (e == 0) v = std::ldexp(m / 8.0, -6);
+  else v = std::ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+// Nearest E4M3 code to x, ties to even, magnitudes beyond 448 (infinities included) clamped to
+// 448 ("saturate to finite"); NaN gives the NaN code.  The quantum is 2^-9 below 2^-6 and
+// 2^(e-3) in the binade [2^e, 2^(e+1)).
+uint8_t e4m3_encode(double x) {
+  if (std::isnan(x)) return std::signbit(x) ? 0xFF : 0x7F;
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+  const double a = std::fabs(x);
+  if (a >= 448.0) return sign | 0x7E;
+  int qexp = -9;                              // subnormal quantum
+  if (a >= std::ldexp(1.0, -6)) {
+    int e = 0;
+    std::frexp(a, &e);                        // a in [2^(e-1), 2^e)
+    qexp = (e - 1) - 3;
+  }
+  const double q = std::nearbyint(std::ldexp(a, -qexp));  // ties to even
+  const double y = std::ldexp(q, qexp);       // the rounded magnitude, exact
+  if (y >= 448.0) return sign | 0x7E;         // cannot happen below 448, kept for clarity
+  if (y < std::ldexp(1.0, -6)) return sign | static_cast<uint8_t>(q);       // subnormal or 2^-6
+  int e = 0;
+  std::frexp(y, &e);
+  const int ef = (e - 1) + 7;                  // biased exponent of y
+  const int m = static_cast<int>(std::ldexp(y, -(e - 1)) * 8.0) - 8;
+  return sign | static_cast<uint8_t>((ef << 3) | m);
+}
+
+// The value a stored code is taken from: the bf16 input times the reciprocal of the scale,
+// both in fp32 with round-to-nearest (the precision the kernels quantise in).
+double quant_input(uint16_t x_bf16, float scale) {
+  const float inv = 1.0f / scale;
+  const float y = static_cast<float>(widen_bf16(x_bf16)) * inv;
+  return static_cast<double>(y);
+}
+
 size_t cache_index(int blk, int h, int off, int d, int Hkv, int B, int D) {
   return ((static_cast<size_t>(blk) * Hkv + h) * B + off) * static_cast<size_t>(D) + d;
 }
@@ -345,6 +390,131 @@ int64_t orc_copy_blocks(int num_caches, int64_t block_elems, const uint16_t* con
         dst[c][to * block_elems + e] = src[c][from * block_elems + e];
   }
   return skipped;
+}
+
+// ---- FP8 (E4M3) KV cache with one scale per KV head --------------------------------------
+// The pages name low-precision quantisation as a way to cut memory and raise inference speed
+// ("nano-vllm：vLLM 极简实现与大模型推理流程解析", §学习要点: FP8 or INT4 quantisation with
+// almost no loss of accuracy; "从零实现15倍加速：一个纯PyTorch LLM推理引擎的技术剖析", §未来展望:
+// INT8 / FP16 quantisation to save memory and bandwidth) but give no format.  The plain
+// reading for the KV cache: each cached K (V) element is stored as the E4M3 code of
+// x / scale_g, where scale_g is the K (V) scale of its KV head, and read back as
+// code * scale_g.
+
+double orc_e4m3_to_f64(uint8_t b) { return e4m3_value(b); }
+
+uint8_t orc_f64_to_e4m3(double x) { return e4m3_encode(x); }
+
+// Quantise n bf16 values of head-major cache rows: element i belongs to KV head
+// (i / (B * D)) % Hkv, the layout [num_blocks][Hkv][B][D].
+int orc_quantize_cache(int64_t n, int Hkv, int B, int D, const uint16_t* src, const float* scale,
+                       uint8_t* dst) {
+  if (n < 0 || Hkv <= 0 || B <= 0 || D <= 0 || (n > 0 && (!src || !scale || !dst))) return -1;
+  const int64_t per_head = static_cast<int64_t>(B) * D;
+  for (int64_t i = 0; i < n; ++i) {
+    const int g = static_cast<int>((i / per_head) % Hkv);
+    dst[i] = e4m3_encode(quant_input(src[i], scale[g]));
+  }
+  return 0;
+}
+
+// RoPE + KV-cache store into FP8 caches: q is rotated in place exactly as orc_rope_kv_store
+// does (bf16); k is rotated and rounded to bf16 as there, then stored as the E4M3 code of
+// k_rot / k_scale[h]; v is stored as the code of v / v_scale[h].
+int orc_rope_kv_store_fp8(int T, int Hq, int Hkv, int D, int B, uint16_t* q, const uint16_t* k,
+                          const uint16_t* v, const int32_t* positions, const float* cos_sin,
+                          int max_pos, const int64_t* slot_mapping, uint8_t* k_cache,
+                          uint8_t* v_cache, int num_blocks, const float* k_scale,
+                          const float* v_scale) {
+  if (T < 0 || !shape_ok(Hq, Hkv, D, B)) return -1;
+  if (T == 0) return 0;
+  if (!q || !k || !v || !positions || !cos_sin || !slot_mapping || !k_cache || !v_cache ||
+      !k_scale || !v_scale)
+    return -1;
+  for (int t = 0; t < T; ++t) {
+    if (positions[t] < 0 || positions[t] >= max_pos) return -1;
+    if (slot_mapping[t] >= static_cast<int64_t>(num_blocks) * B) return -1;
+  }
+  std::vector<double> y(D);
+  for (int t = 0; t < T; ++t) {
+    const float* row = cos_sin + static_cast<size_t>(positions[t]) * D;
+    for (int h = 0; h < Hq; ++h) {
+      uint16_t* qh = q + (static_cast<size_t>(t) * Hq + h) * D;
+      rotate_half(qh, D, row, y.data());
+      for (int d = 0; d < D; ++d) qh[d] = narrow_bf16(y[d]);
+    }
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    const int blk = static_cast<int>(slot / B);
+    const int off = static_cast<int>(slot % B);
+    for (int h = 0; h < Hkv; ++h) {
+      const uint16_t* kh = k + (static_cast<size_t>(t) * Hkv + h) * D;
+      const uint16_t* vh = v + (static_cast<size_t>(t) * Hkv + h) * D;
+      rotate_half(kh, D, row, y.data());
+      for (int d = 0; d < D; ++d) {
+        k_cache[cache_index(blk, h, off, d, Hkv, B, D)] =
+            e4m3_encode(quant_input(narrow_bf16(y[d]), k_scale[h]));
+        v_cache[cache_index(blk, h, off, d, Hkv, B, D)] = e4m3_encode(quant_input(vh[d], v_scale[h]));
+      }
+    }
+  }
+  return 0;
+}
+
+// Decode over FP8 caches: the same single-token attention as orc_decode, each cached element
+// read as code * scale of its KV head (exact in double).
+int orc_decode_fp8(int S, int Hq, int Hkv, int D, int B, const uint16_t* q, const uint8_t* k_cache,
+                   const uint8_t* v_cache, const float* k_scale, const float* v_scale,
+                   int num_blocks, const int32_t* block_tables, int max_blocks,
+                   const int32_t* context_lens, double scale, int nthreads, double* out_f64,
+                   uint16_t* out_bf16) {
+  if (S < 0 || !shape_ok(Hq, Hkv, D, B) || max_blocks < 0) return -1;
+  if (S == 0) return 0;
+  if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables || !context_lens)
+    return -1;
+  if (!table_ok(block_tables, max_blocks, context_lens, S, num_blocks, B)) return -1;
+  const int G = Hq / Hkv;
+  parallel_units(S * Hkv, nthreads, [&](int unit) {
+    const int s = unit / Hkv;
+    const int g = unit % Hkv;
+    const int ctx = context_lens[s];
+    const int32_t* bt_row = block_tables + static_cast<size_t>(s) * max_blocks;
+    const double ks = static_cast<double>(k_scale[g]);
+    const double vs = static_cast<double>(v_scale[g]);
+    std::vector<double> scores(std::max(ctx, 1));
+    std::vector<double> o(D);
+    for (int h = g * G; h < (g + 1) * G; ++h) {
+      const size_t obase = (static_cast<size_t>(s) * Hq + h) * D;
+      std::fill(o.begin(), o.end(), 0.0);
+      if (ctx > 0) {
+        for (int t = 0; t < ctx; ++t) {
+          const int blk = bt_row[t / B];
+          const int off = t % B;
+          double dot = 0.0;
+          for (int d = 0; d < D; ++d)
+            dot += widen_bf16(q[obase + d]) *
+                   (e4m3_value(k_cache[cache_index(blk, g, off, d, Hkv, B, D)]) * ks);
+          scores[t] = scale * dot;
+        }
+        const double m = *std::max_element(scores.begin(), scores.begin() + ctx);
+        double l = 0.0;
+        for (int t = 0; t < ctx; ++t) {
+          const double p = std::exp(scores[t] - m);
+          l += p;
+          const int blk = bt_row[t / B];
+          const int off = t % B;
+          for (int d = 0; d < D; ++d)
+            o[d] += p * (e4m3_value(v_cache[cache_index(blk, g, off, d, Hkv, B, D)]) * vs);
+        }
+        for (int d = 0; d < D; ++d) o[d] /= l;
+      }
+      for (int d = 0; d < D; ++d) {
+        if (out_f64) out_f64[obase + d] = o[d];
+        if (out_bf16) out_bf16[obase + d] = narrow_bf16(o[d]);
+      }
+    }
+  });
+  return 0;
 }
 
 int orc_hardware_threads(void) {

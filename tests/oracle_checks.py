@@ -467,6 +467,140 @@ def check_swap_out_in_preserves_decode(orc):
     assert np.array_equal(got, ref)
 
 
+# ---- FP8 (E4M3) KV cache ------------------------------------------------------------------
+# The independent reference for the E4M3 format is PyTorch's own float8_e4m3fn conversion.
+
+def _torch_e4m3_decode(codes):
+    import torch
+    return torch.from_numpy(np.asarray(codes, np.uint8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _torch_e4m3_encode(x_f32):
+    import torch
+    t = torch.from_numpy(np.asarray(x_f32, np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def check_e4m3_decode_all_codes(orc):
+    want = _torch_e4m3_decode(np.arange(256))
+    for c in range(256):
+        got = orc.e4m3_to_f64(c)
+        if np.isnan(want[c]):
+            assert np.isnan(got), c
+        else:
+            assert got == want[c] and np.signbit(got) == np.signbit(want[c]), (c, got, want[c])
+    # the format's landmarks: max 448, smallest normal 2^-6, smallest subnormal 2^-9
+    assert orc.e4m3_to_f64(0x7E) == 448.0 and orc.e4m3_to_f64(0x08) == 2.0 ** -6
+    assert orc.e4m3_to_f64(0x01) == 2.0 ** -9
+
+
+def check_e4m3_encode_rne_and_saturation(orc):
+    codes = np.arange(0x7E + 1)
+    vals = _torch_e4m3_decode(codes)
+    mids = (vals[:-1] + vals[1:]) / 2               # exact ties (fp32-representable)
+    rng = np.random.default_rng(21)
+    rand = np.ldexp(rng.uniform(1, 2, 4000), rng.integers(-12, 9, 4000))
+    xs = np.concatenate([vals, mids, np.nextafter(mids, 0), np.nextafter(mids, 1e9), rand])
+    xs = np.concatenate([xs, -xs]).astype(np.float32)
+    xs = xs[np.abs(xs) <= 448]
+    want = _torch_e4m3_encode(xs)
+    got = np.array([orc.f64_to_e4m3(float(x)) for x in xs], np.uint8)
+    assert np.array_equal(got, want)
+    for big in (448.5, 464.0, 480.0, 1e6, float("inf")):
+        assert orc.f64_to_e4m3(big) == 0x7E and orc.f64_to_e4m3(-big) == 0xFE
+    assert orc.f64_to_e4m3(float("nan")) & 0x7F == 0x7F
+
+
+def check_quantize_cache_definition(orc):
+    """code = E4M3(fp32(x) * fp32(1 / scale_g)) with g the element's KV head."""
+    rng = W.SplitMix64(22)
+    cache = rng.normal_bf16(6 * 2 * 16 * D, 2.0).reshape(6, 2, 16, D)
+    scale = np.array([4.5 / 448, 7.0 / 448], np.float32)
+    got = orc.quantize_cache(cache, scale)
+    x = W.bf16_bits_to_f32(cache)
+    inv = (np.float32(1.0) / scale).astype(np.float32)
+    y = (x * inv[None, :, None, None]).astype(np.float32)
+    inside = np.abs(y) <= 448
+    assert inside.mean() > 0.9 and (~inside).any()       # both regimes are exercised
+    assert np.array_equal(got[inside], _torch_e4m3_encode(y[inside]))
+    assert np.array_equal(got[~inside], np.where(y[~inside] > 0, 0x7E, 0xFE).astype(np.uint8))
+
+
+def check_quantize_decides_in_fp32(orc):
+    """The code is taken from fp32(x) * fp32(1 / scale), the kernels' precision, not from the
+    exact quotient: over every bf16 value in range, with scale 7 (where the two differ for 25
+    values), the oracle agrees with the fp32 product everywhere."""
+    bits = np.arange(0x3C00, 0x43E0, dtype=np.uint16)          # ~0.0078 .. ~450
+    pad = -bits.size % (16 * D)
+    bits = np.concatenate([bits, np.zeros(pad, np.uint16)])     # whole 16 x D rows
+    x = W.bf16_bits_to_f32(bits).astype(np.float32)
+    for sc in (7.0, 3.0, 0.7):
+        s32 = np.float32(sc)
+        y32 = (x * (np.float32(1.0) / s32)).astype(np.float32)
+        got = orc.quantize_cache(bits.reshape(-1, 1, 16, D), np.array([s32], np.float32)).reshape(-1)
+        m = np.abs(y32) <= 448
+        assert np.array_equal(got[m], _torch_e4m3_encode(y32[m])), sc
+
+
+def _fp8_case(orc, seed=23):
+    rng = W.SplitMix64(seed)
+    ctxs = [1, 16, 17, 100, 333]
+    Hq, Hkv = 12, 2
+    Kd = [rng.normal_bf16(Hkv * c * D, 1.0).reshape(Hkv, c, D) for c in ctxs]
+    Vd = [rng.normal_bf16(Hkv * c * D, 1.0).reshape(Hkv, c, D) for c in ctxs]
+    q = rng.normal_bf16(len(ctxs) * Hq * D, 1.0).reshape(len(ctxs), Hq, D)
+    kc, vc, bt = _paged_from_dense(Kd, Vd, 48, rng, fill=0)
+    ks = np.array([5.0 / 448, 4.0 / 448], np.float32)
+    vs = np.array([4.5 / 448, 6.0 / 448], np.float32)
+    return q, orc.quantize_cache(kc, ks), orc.quantize_cache(vc, vs), ks, vs, bt, np.array(ctxs, np.int32)
+
+
+def check_decode_fp8_dense_equivalence(orc):
+    """FP8 decode = dense fp64 attention over the exactly dequantised K, V (torch decode)."""
+    q, k8, v8, ks, vs, bt, ctx = _fp8_case(orc)
+    scale = 1.0 / math.sqrt(D)
+    got, _ = orc.decode_fp8(q, k8, v8, ks, vs, bt, ctx, scale)
+    kd = _torch_e4m3_decode(k8) * ks.astype(np.float64)[None, :, None, None]
+    vd = _torch_e4m3_decode(v8) * vs.astype(np.float64)[None, :, None, None]
+    for s, c in enumerate(ctx):
+        blocks = bt[s, :(int(c) + 15) // 16]
+        Kd = kd[blocks].transpose(1, 0, 2, 3).reshape(2, -1, D)[:, :c]
+        Vd = vd[blocks].transpose(1, 0, 2, 3).reshape(2, -1, D)[:, :c]
+        qs = W.bf16_bits_to_f32(q[s]).astype(np.float64)
+        for h in range(12):
+            g = h // 6
+            ref = softmax(scale * (Kd[g] @ qs[h])) @ Vd[g]
+            assert np.allclose(got[s, h], ref, rtol=1e-12, atol=1e-14), (s, h)
+
+
+def check_rope_kv_store_fp8_is_bf16_store_then_quantise(orc):
+    """The FP8 store equals the bf16 store followed by quantisation of the stored rows."""
+    w = W.make("tiny")
+    ks = np.array([3.0 / 448, 5.0 / 448], np.float32)
+    vs = np.array([2.0 / 448, 4.0 / 448], np.float32)
+    kc16, vc16 = w.k_cache[0].copy(), w.v_cache[0].copy()
+    q16 = orc.rope_kv_store(w.q[0], w.k[0], w.v[0], w.positions, w.cos_sin, w.slot_mapping, kc16, vc16)
+    kc8 = np.zeros(kc16.shape, np.uint8)
+    vc8 = np.zeros(vc16.shape, np.uint8)
+    q8 = orc.rope_kv_store_fp8(w.q[0], w.k[0], w.v[0], w.positions, w.cos_sin, w.slot_mapping,
+                               kc8, vc8, ks, vs)
+    assert np.array_equal(q8, q16)
+    blk, off = np.divmod(w.slot_mapping, W.BLOCK_SIZE)
+    for i in range(len(blk)):
+        krow = kc16[blk[i], :, off[i]]
+        vrow = vc16[blk[i], :, off[i]]
+        for g in range(2):
+            inv_k = np.float32(1.0) / ks[g]
+            inv_v = np.float32(1.0) / vs[g]
+            want_k = _torch_e4m3_encode((W.bf16_bits_to_f32(krow[g]) * inv_k).astype(np.float32))
+            want_v = _torch_e4m3_encode((W.bf16_bits_to_f32(vrow[g]) * inv_v).astype(np.float32))
+            assert np.array_equal(kc8[blk[i], g, off[i]], want_k)
+            assert np.array_equal(vc8[blk[i], g, off[i]], want_v)
+    mask = np.ones(kc8.shape, bool)
+    mask[blk, :, off] = False
+    assert not kc8[mask].any() and not vc8[mask].any()
+
+
 ALL_CHECKS = [
     check_bf16_widen,
     check_bf16_narrow_bruteforce,
@@ -489,4 +623,10 @@ ALL_CHECKS = [
     check_copy_blocks_matches_fancy_indexing,
     check_copy_blocks_skips_out_of_range_pairs,
     check_swap_out_in_preserves_decode,
+    check_e4m3_decode_all_codes,
+    check_e4m3_encode_rne_and_saturation,
+    check_quantize_cache_definition,
+    check_quantize_decides_in_fp32,
+    check_decode_fp8_dense_equivalence,
+    check_rope_kv_store_fp8_is_bf16_store_then_quantise,
 ]

@@ -74,6 +74,19 @@ MUTANTS = {
                               "for (int c = 0; c < 1; ++c)\n      for (int64_t e = 0;"),
     "copy_skips_last_element": ("for (int64_t e = 0; e < block_elems; ++e)",
                                 "for (int64_t e = 0; e + 1 < block_elems; ++e)"),
+    "e4m3_bias_8": ("else v = std::ldexp(1.0 + m / 8.0, e - 7);",
+                    "else v = std::ldexp(1.0 + m / 8.0, e - 8);"),
+    "e4m3_ties_away": ("const double q = std::nearbyint(std::ldexp(a, -qexp));  // ties to even",
+                       "const double q = std::round(std::ldexp(a, -qexp));"),
+    "e4m3_no_saturation": ("if (a >= 448.0) return sign | 0x7E;", "if (a >= 448.0) return sign | 0x7F;"),
+    "quantise_divides_in_double": ("const float y = static_cast<float>(widen_bf16(x_bf16)) * inv;",
+                                   "const float y = static_cast<float>(widen_bf16(x_bf16) / scale);"),
+    "fp8_store_k_with_v_scale": ("e4m3_encode(quant_input(narrow_bf16(y[d]), k_scale[h]));",
+                                 "e4m3_encode(quant_input(narrow_bf16(y[d]), v_scale[h]));"),
+    "fp8_decode_drops_k_scale": ("(e4m3_value(k_cache[cache_index(blk, g, off, d, Hkv, B, D)]) * ks);",
+                                 "(e4m3_value(k_cache[cache_index(blk, g, off, d, Hkv, B, D)]) * 1.0);"),
+    "fp8_decode_wrong_v_head": ("o[d] += p * (e4m3_value(v_cache[cache_index(blk, g, off, d, Hkv, B, D)]) * vs);",
+                                "o[d] += p * (e4m3_value(v_cache[cache_index(blk, (g + 1) % Hkv, off, d, Hkv, B, D)]) * vs);"),
 }
 
 
