@@ -69,6 +69,14 @@ def lib():
         L.pa_decode_step.argtypes = [pd, i, p, p, p, p, i, p, p, i, p, i, p, i, f, i, p,
                                      ctypes.c_size_t, p, p]
         L.pa_decode_step.restype = i
+        L.pa_rope_kv_store_fp8.argtypes = [pd, i, p, p, p, p, p, i, p, p, p, i, p, p, p]
+        L.pa_rope_kv_store_fp8.restype = i
+        L.pa_decode_fp8.argtypes = [pd, i, p, p, p, p, p, i, p, i, p, i, f, i, p, ctypes.c_size_t,
+                                    p, p]
+        L.pa_decode_fp8.restype = i
+        L.pa_decode_step_fp8.argtypes = [pd, i, p, p, p, p, i, p, p, p, p, i, p, i, p, i, f, i, p,
+                                         ctypes.c_size_t, p, p]
+        L.pa_decode_step_fp8.restype = i
         L.pa_copy_blocks.argtypes = [pd, i, p, ctypes.c_int64, p, ctypes.c_int64, p, i, p]
         L.pa_copy_blocks.restype = i
         L.pa_get_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
@@ -228,6 +236,89 @@ def decode_step(q, k, v, cos_sin, k_cache, v_cache, block_tables, context_lens, 
         int(partition_tokens), _dev_ptr(workspace, "workspace"), ws_bytes, _dev_ptr(out, "out", bf),
         _stream(stream))
     _check(rc, "pa_decode_step")
+    return out
+
+
+# ---- FP8 (E4M3) caches: uint8 tensors of codes, fp32 scales [Hkv] per KV head ----------
+
+def _fp8_args(k_cache, v_cache, k_scale, v_scale):
+    nb, Hkv, B, D = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache differ in shape")
+    if tuple(k_scale.shape) != (Hkv,) or tuple(v_scale.shape) != (Hkv,):
+        raise ValueError("k_scale and v_scale must be [num_kv_heads] float32")
+    u8, f32 = torch.uint8, torch.float32
+    return (nb, Hkv, B, D, _dev_ptr(k_cache, "k_cache", u8), _dev_ptr(v_cache, "v_cache", u8),
+            _dev_ptr(k_scale, "k_scale", f32), _dev_ptr(v_scale, "v_scale", f32))
+
+
+def rope_kv_store_fp8(q, k, v, positions, cos_sin, slot_mapping, k_cache, v_cache, k_scale,
+                      v_scale, stream=None):
+    """pa_rope_kv_store_fp8: q rotated in place (bf16); rotated k and v stored as E4M3 codes
+    (k_cache, v_cache uint8 [num_blocks, Hkv, B, D]) with per-KV-head scales."""
+    T, Hq, D = q.shape
+    nb, Hkv, B, D2, kc, vc, ks, vs = _fp8_args(k_cache, v_cache, k_scale, v_scale)
+    if D2 != D or tuple(k.shape) != (T, Hkv, D) or tuple(v.shape) != (T, Hkv, D):
+        raise ValueError("shape mismatch between q, k, v and the caches")
+    if positions.shape != (T,) or slot_mapping.shape != (T,) or cos_sin.shape[1] != D:
+        raise ValueError("positions / slot_mapping / cos_sin shape mismatch")
+    dims = make_dims(Hq, Hkv, D, B)
+    bf = torch.bfloat16
+    rc = lib().pa_rope_kv_store_fp8(
+        ctypes.byref(dims), T, _dev_ptr(q, "q", bf), _dev_ptr(k, "k", bf), _dev_ptr(v, "v", bf),
+        _dev_ptr(positions, "positions", torch.int32), _dev_ptr(cos_sin, "cos_sin", torch.float32),
+        cos_sin.shape[0], _dev_ptr(slot_mapping, "slot_mapping", torch.int64), kc, vc, nb, ks, vs,
+        _stream(stream))
+    _check(rc, "pa_rope_kv_store_fp8")
+
+
+def decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+               max_context_len, scale, partition_tokens=0, workspace=None, out=None, stream=None):
+    """pa_decode_fp8: decode attention over E4M3 caches.  Returns out [S, Hq, D] bf16."""
+    S, Hq, D = q.shape
+    nb, Hkv, B, D2, kc, vc, ks, vs = _fp8_args(k_cache, v_cache, k_scale, v_scale)
+    if D2 != D or block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = decode_workspace(q, k_cache, max_context_len, partition_tokens)
+    dims = make_dims(Hq, Hkv, D, B)
+    rc = lib().pa_decode_fp8(
+        ctypes.byref(dims), S, _dev_ptr(q, "q", torch.bfloat16), kc, vc, ks, vs, nb,
+        _dev_ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev_ptr(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
+        int(partition_tokens), _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dev_ptr(out, "out", torch.bfloat16),
+        _stream(stream))
+    _check(rc, "pa_decode_fp8")
+    return out
+
+
+def decode_step_fp8(q, k, v, cos_sin, k_cache, v_cache, k_scale, v_scale, block_tables,
+                    context_lens, max_context_len, scale, partition_tokens=0, workspace=None,
+                    out=None, stream=None):
+    """pa_decode_step_fp8: the fused step over E4M3 caches (q left unchanged)."""
+    S, Hq, D = q.shape
+    nb, Hkv, B, D2, kc, vc, ks, vs = _fp8_args(k_cache, v_cache, k_scale, v_scale)
+    if D2 != D or tuple(k.shape) != (S, Hkv, D) or tuple(v.shape) != (S, Hkv, D):
+        raise ValueError("k / v shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables / context_lens shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = decode_workspace(q, k_cache, max_context_len, partition_tokens)
+    dims = make_dims(Hq, Hkv, D, B)
+    bf = torch.bfloat16
+    rc = lib().pa_decode_step_fp8(
+        ctypes.byref(dims), S, _dev_ptr(q, "q", bf), _dev_ptr(k, "k", bf), _dev_ptr(v, "v", bf),
+        _dev_ptr(cos_sin, "cos_sin", torch.float32), cos_sin.shape[0], kc, vc, ks, vs, nb,
+        _dev_ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev_ptr(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
+        int(partition_tokens), _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dev_ptr(out, "out", bf), _stream(stream))
+    _check(rc, "pa_decode_step_fp8")
     return out
 
 

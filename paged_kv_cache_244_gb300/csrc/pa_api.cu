@@ -125,6 +125,8 @@ int decode_args(const pa_dims* dims, int num_seqs, const void* q, const void* k_
   a->max_pos = 0;
   a->k_store = nullptr;
   a->v_store = nullptr;
+  a->k_scale = nullptr;
+  a->v_scale = nullptr;
   return PA_OK;
 }
 
@@ -152,14 +154,11 @@ int device_address(const void* p, const void** out) {
   }
 }
 
-}  // namespace
-
-extern "C" {
-
-int pa_rope_kv_store(const pa_dims* dims, int num_tokens, void* q, const void* k, const void* v,
-                     const int32_t* positions, const float* cos_sin, int max_pos,
-                     const int64_t* slot_mapping, void* k_cache, void* v_cache, int num_blocks,
-                     void* stream) {
+// pa_rope_kv_store and its E4M3 form (scales non-null).
+int rope_store(const pa_dims* dims, int num_tokens, void* q, const void* k, const void* v,
+               const int32_t* positions, const float* cos_sin, int max_pos,
+               const int64_t* slot_mapping, void* k_cache, void* v_cache, int num_blocks,
+               const float* k_scale, const float* v_scale, void* stream) {
   if (const int rc = check_dims(dims)) return rc;
   if (num_tokens < 0) return PA_ERR_RANGE;
   if (num_tokens == 0) return PA_OK;
@@ -171,7 +170,7 @@ int pa_rope_kv_store(const pa_dims* dims, int num_tokens, void* q, const void* k
     if (!aligned16(p)) return PA_ERR_ALIGN;
   unsigned* status = nullptr;
   if (const int rc = status_word(&status)) return rc;
-  pa::RopeArgs a;
+  pa::RopeArgs a{};
   a.q = static_cast<__nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
@@ -186,9 +185,77 @@ int pa_rope_kv_store(const pa_dims* dims, int num_tokens, void* q, const void* k
   a.max_pos = max_pos;
   a.num_blocks = num_blocks;
   a.status = status;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   return pa::launch_rope_kv_store(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
+}
+
+// pa_decode_step and its E4M3 form (scales non-null).
+int decode_step(const pa_dims* dims, int num_seqs, const void* q, const void* k, const void* v,
+                const float* cos_sin, int max_pos, void* k_cache, void* v_cache,
+                const float* k_scale, const float* v_scale, int num_blocks,
+                const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                int max_context_len, float scale, int partition_tokens, void* workspace,
+                size_t workspace_bytes, void* out, void* stream) {
+  // The new token's arguments first (host checks only), then everything pa_decode checks.
+  if (const int rc = check_dims(dims)) return rc;
+  if (num_seqs < 0 || num_seqs > pa::kMaxDecodeSeqs) return PA_ERR_RANGE;
+  if (num_seqs == 0) return PA_OK;
+  if (!k || !v || !cos_sin) return PA_ERR_NULL;
+  if (max_pos < 1) return PA_ERR_RANGE;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(cos_sin)) return PA_ERR_ALIGN;
+  pa::DecodeArgs a{};
+  const int rc = decode_args(dims, num_seqs, q, k_cache, v_cache, num_blocks, block_tables, max_blocks,
+                             context_lens, max_context_len, scale, partition_tokens, workspace,
+                             workspace_bytes, out, &a);
+  if (rc != PA_OK) return rc;
+  a.k_new = static_cast<const __nv_bfloat16*>(k);
+  a.v_new = static_cast<const __nv_bfloat16*>(v);
+  a.cos_sin = cos_sin;
+  a.max_pos = max_pos;
+  a.k_store = static_cast<__nv_bfloat16*>(k_cache);
+  a.v_store = static_cast<__nv_bfloat16*>(v_cache);
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  return pa::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                 : PA_ERR_CUDA;
+}
+
+// Host checks of the E4M3 scale arrays (after the shape and count checks their callers share).
+int scales_ok(const pa_dims* dims, int num_seqs, const float* k_scale, const float* v_scale) {
+  if (const int rc = check_dims(dims)) return rc;
+  if (num_seqs < 0 || num_seqs > pa::kMaxDecodeSeqs) return PA_ERR_RANGE;
+  if (num_seqs == 0) return PA_OK;
+  if (!k_scale || !v_scale) return PA_ERR_NULL;
+  if (!aligned16(k_scale) || !aligned16(v_scale)) return PA_ERR_ALIGN;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_rope_kv_store(const pa_dims* dims, int num_tokens, void* q, const void* k, const void* v,
+                     const int32_t* positions, const float* cos_sin, int max_pos,
+                     const int64_t* slot_mapping, void* k_cache, void* v_cache, int num_blocks,
+                     void* stream) {
+  return rope_store(dims, num_tokens, q, k, v, positions, cos_sin, max_pos, slot_mapping, k_cache,
+                    v_cache, num_blocks, nullptr, nullptr, stream);
+}
+
+int pa_rope_kv_store_fp8(const pa_dims* dims, int num_tokens, void* q, const void* k,
+                         const void* v, const int32_t* positions, const float* cos_sin,
+                         int max_pos, const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                         int num_blocks, const float* k_scale, const float* v_scale, void* stream) {
+  if (num_tokens > 0) {
+    if (const int rc = check_dims(dims)) return rc;
+    if (!k_scale || !v_scale) return PA_ERR_NULL;
+    if (!aligned16(k_scale) || !aligned16(v_scale)) return PA_ERR_ALIGN;
+  }
+  return rope_store(dims, num_tokens, q, k, v, positions, cos_sin, max_pos, slot_mapping, k_cache,
+                    v_cache, num_blocks, k_scale, v_scale, stream);
 }
 
 int pa_decode_partition_tokens(const pa_dims* dims, int num_seqs, int max_context_len,
@@ -208,7 +275,7 @@ int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_ca
               const int32_t* context_lens, int max_context_len, float scale,
               int partition_tokens, void* workspace, size_t workspace_bytes, void* out,
               void* stream) {
-  pa::DecodeArgs a;
+  pa::DecodeArgs a{};
   const int rc = decode_args(dims, num_seqs, q, k_cache, v_cache, num_blocks, block_tables, max_blocks,
                              context_lens, max_context_len, scale, partition_tokens, workspace,
                              workspace_bytes, out, &a);
@@ -222,24 +289,36 @@ int pa_decode_step(const pa_dims* dims, int num_seqs, const void* q, const void*
                    const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                    int max_context_len, float scale, int partition_tokens, void* workspace,
                    size_t workspace_bytes, void* out, void* stream) {
-  // The new token's arguments first (host checks only), then everything pa_decode checks.
-  if (const int rc = check_dims(dims)) return rc;
-  if (num_seqs < 0 || num_seqs > pa::kMaxDecodeSeqs) return PA_ERR_RANGE;
-  if (num_seqs == 0) return PA_OK;
-  if (!k || !v || !cos_sin) return PA_ERR_NULL;
-  if (max_pos < 1) return PA_ERR_RANGE;
-  if (!aligned16(k) || !aligned16(v) || !aligned16(cos_sin)) return PA_ERR_ALIGN;
-  pa::DecodeArgs a;
+  return decode_step(dims, num_seqs, q, k, v, cos_sin, max_pos, k_cache, v_cache, nullptr, nullptr,
+                     num_blocks, block_tables, max_blocks, context_lens, max_context_len, scale,
+                     partition_tokens, workspace, workspace_bytes, out, stream);
+}
+
+int pa_decode_step_fp8(const pa_dims* dims, int num_seqs, const void* q, const void* k,
+                       const void* v, const float* cos_sin, int max_pos, void* k_cache,
+                       void* v_cache, const float* k_scale, const float* v_scale, int num_blocks,
+                       const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                       int max_context_len, float scale, int partition_tokens, void* workspace,
+                       size_t workspace_bytes, void* out, void* stream) {
+  if (const int rc = scales_ok(dims, num_seqs, k_scale, v_scale)) return rc;
+  return decode_step(dims, num_seqs, q, k, v, cos_sin, max_pos, k_cache, v_cache, k_scale, v_scale,
+                     num_blocks, block_tables, max_blocks, context_lens, max_context_len, scale,
+                     partition_tokens, workspace, workspace_bytes, out, stream);
+}
+
+int pa_decode_fp8(const pa_dims* dims, int num_seqs, const void* q, const void* k_cache,
+                  const void* v_cache, const float* k_scale, const float* v_scale, int num_blocks,
+                  const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
+                  int max_context_len, float scale, int partition_tokens, void* workspace,
+                  size_t workspace_bytes, void* out, void* stream) {
+  if (const int rc = scales_ok(dims, num_seqs, k_scale, v_scale)) return rc;
+  pa::DecodeArgs a{};
   const int rc = decode_args(dims, num_seqs, q, k_cache, v_cache, num_blocks, block_tables, max_blocks,
                              context_lens, max_context_len, scale, partition_tokens, workspace,
                              workspace_bytes, out, &a);
-  if (rc != PA_OK) return rc;
-  a.k_new = static_cast<const __nv_bfloat16*>(k);
-  a.v_new = static_cast<const __nv_bfloat16*>(v);
-  a.cos_sin = cos_sin;
-  a.max_pos = max_pos;
-  a.k_store = static_cast<__nv_bfloat16*>(k_cache);
-  a.v_store = static_cast<__nv_bfloat16*>(v_cache);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   return pa::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
                                                                                  : PA_ERR_CUDA;
 }
@@ -260,7 +339,7 @@ int pa_copy_blocks(const pa_dims* dims, int num_caches, const void* const* src_c
   if (reinterpret_cast<uintptr_t>(block_pairs) % alignof(int64_t) != 0) return PA_ERR_ALIGN;
   unsigned* status = nullptr;
   if (const int rc = status_word(&status)) return rc;
-  pa::BlockCopyArgs a;
+  pa::BlockCopyArgs a{};
   for (int c = 0; c < num_caches; ++c) {
     const void* s = nullptr;
     const void* d = nullptr;

@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "pa.h"
 
@@ -148,6 +149,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Same shape with f16 operands (the E4M3 cache path: E4M3 widens exactly to f16).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // ---- bf16 ------------------------------------------------------------------------------
 // Widen a packed pair of bf16 (low half = element 0) to two floats: bf16 is the top half
 // of an fp32 bit pattern.
@@ -158,6 +169,47 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---- f16 and E4M3 (FP8) -----------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float f16lo(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+__device__ __forceinline__ float f16hi(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+// bf16 pair -> f16 pair, round to nearest (exact for bf16 values inside the f16 range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) { return pack_f16x2(bf16lo(w), bf16hi(w)); }
+
+// Two E4M3 codes (low byte = element 0) -> f16 pair, exact (NaN stays NaN).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(x));
+  return r;
+}
+// Four codes b0..b3 -> f16 pairs (b0, b1) and (b2, b3).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xffffu));
+  hi = e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16));
+}
+// Four codes b0..b3 -> f16 pairs (b0, b2) and (b1, b3).
+__device__ __forceinline__ void e4m3x4_pairs_to_f16(uint32_t w, uint32_t& even, uint32_t& odd) {
+  uint32_t p;
+  asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(p) : "r"(w));  // bytes b0 b2 b1 b3
+  e4m3x4_to_f16x2x2(p, even, odd);
+}
+// E4M3 codes of a bf16 pair times `inv` (fp32, round to nearest), round to nearest even,
+// saturating to +-448; low byte = element 0.
+__device__ __forceinline__ uint16_t e4m3x2_of(uint32_t bf16_pair, float inv) {
+  const float lo = __fmul_rn(bf16lo(bf16_pair), inv);
+  const float hi = __fmul_rn(bf16hi(bf16_pair), inv);
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // rotate_half RoPE of two adjacent rotation pairs: lo holds x[i], x[i+1], hi holds x[i+64],

@@ -38,6 +38,9 @@ struct RopeArgs {
   __nv_bfloat16* v_cache;
   int num_tokens, num_q_heads, num_kv_heads, max_pos, num_blocks;
   unsigned* status;                 // device status word
+  // E4M3 caches (k_scale == nullptr for bf16): the caches hold one-byte codes.
+  const float* k_scale;             // [Hkv]
+  const float* v_scale;             // [Hkv]
 };
 
 struct DecodeArgs {
@@ -63,6 +66,10 @@ struct DecodeArgs {
   int max_pos;
   __nv_bfloat16* k_store;           // the caches again, writable: destination of the new token
   __nv_bfloat16* v_store;
+  // E4M3 caches (k_scale == nullptr for bf16): the caches hold one-byte codes, element =
+  // code * scale of its KV head.
+  const float* k_scale;             // [Hkv]
+  const float* v_scale;             // [Hkv]
 };
 
 // Whole-block copies between pools (copy-on-write, swap out / in).  Pool pointers are device

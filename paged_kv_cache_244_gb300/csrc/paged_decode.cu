@@ -54,20 +54,32 @@ constexpr int kWarps = PA_DECODE_WARPS;
 constexpr int kStages = PA_DECODE_STAGES;
 constexpr int kHalfBytes = kBlockSize * 128;                // 16 rows x 64 bf16
 constexpr int kQBytes = 8 * kHeadDim * 2;                   // q rows of up to 8 heads
-// Fused step: behind the q rows, the new token's cos/sin row (fp32), k and v rows (bf16).
-constexpr int kCosSinOffset = 2 * kTileBytes + kQBytes;
-constexpr int kNewKOffset = kCosSinOffset + kHeadDim * 4;
-constexpr int kNewVOffset = kNewKOffset + kHeadDim * 2;
-// Stage: K tile + V tile + q rows (+ the fused step's rows), a multiple of 1024 bytes so that
-// every stage's swizzled halves stay on 1024-byte boundaries.
-template <bool kStep>
-constexpr int kStageBytes = kStep ? kNewVOffset + kHeadDim * 2 : 2 * kTileBytes + kQBytes;
-static_assert(kStageBytes<false> % 1024 == 0 && kStageBytes<true> % 1024 == 0, "stage alignment");
-// Shared-memory header: the mbarriers (8 bytes each), then the int4 job descriptors on a
-// 16-byte boundary, then the prefix of block counts.
-constexpr int kDescOffset = (kWarps * kStages * 8 + 15) & ~15;
-constexpr int kPrefixOffset = kDescOffset + kWarps * kStages * 16;
-static_assert(kDescOffset % 16 == 0 && kPrefixOffset % 16 == 0, "descriptor alignment");
+
+__host__ __device__ inline int prefix_bytes(int num_seqs) { return ((num_seqs + 1) * 4 + 15) & ~15; }
+
+// Shared-memory layout of one kernel variant.  kStep fuses the new token's RoPE + store; kFp8
+// reads E4M3 caches, whose (block, KV head) tiles are 2 KiB instead of 4 KiB, so more stages
+// fit.  Header: the mbarriers (8 bytes each), the int4 job descriptors on a 16-byte boundary,
+// the prefix of block counts.  Stage: [K tile | V tile | q rows | (kStep) the new token's
+// cos/sin row (fp32), k row and v row (bf16)], a multiple of 1024 bytes so that every tile
+// stays on the 1024-byte boundary its 128-byte swizzle needs.
+template <bool kStep, bool kFp8>
+struct Layout {
+  static constexpr int kTile = kFp8 ? kTileBytes / 2 : kTileBytes;
+  static constexpr int kStagesN = kFp8 ? (kStep ? 3 : 4) : kStages;
+  static constexpr int kQOff = 2 * kTile;
+  static constexpr int kCosSinOff = kQOff + kQBytes;
+  static constexpr int kNewKOff = kCosSinOff + kHeadDim * 4;
+  static constexpr int kNewVOff = kNewKOff + kHeadDim * 2;
+  static constexpr int kStage = kStep ? kNewVOff + kHeadDim * 2 : kQOff + kQBytes;
+  static constexpr int kDescOff = (kWarps * kStagesN * 8 + 15) & ~15;
+  static constexpr int kPrefixOff = kDescOff + kWarps * kStagesN * 16;
+  static_assert(kStage % 1024 == 0 && kTile % 1024 == 0, "tiles on 1024-byte boundaries");
+  static_assert(kDescOff % 16 == 0 && kPrefixOff % 16 == 0, "descriptor alignment");
+  __host__ __device__ static int smem(int num_seqs) {
+    return kPrefixOff + prefix_bytes(num_seqs) + 1024 + kWarps * kStagesN * kStage;  // + pad
+  }
+};
 
 // Job flags (low bits of a descriptor's flag word; valid tokens sit at bits 8-12).
 constexpr uint32_t kFirst = 1u, kLast = 2u, kWhole = 4u, kHasData = 8u;
@@ -75,12 +87,6 @@ constexpr uint32_t kNew = 16u;   // fused step: the block holding the segment's 
 constexpr uint32_t kRope = 32u;  // fused step: the sequence's position has a cos/sin row
 constexpr int kMinRangeBlocks = PA_DECODE_MIN_RANGE;
 
-__host__ __device__ inline int prefix_bytes(int num_seqs) { return ((num_seqs + 1) * 4 + 15) & ~15; }
-template <bool kStep>
-__host__ __device__ inline int smem_bytes(int num_seqs) {
-  // + 1024: alignment pad
-  return kPrefixOffset + prefix_bytes(num_seqs) + 1024 + kWarps * kStages * kStageBytes<kStep>;
-}
 
 // Flattened-axis ranges.  chunk > 0: range v = [v*chunk, (v+1)*chunk) clipped to T.  chunk == 0:
 // V = min(num_warps, ceil(T / kMinRangeBlocks)) ranges, range v = [floor(v T / V),
@@ -112,24 +118,26 @@ __device__ __forceinline__ int clamp_len(int len, int max_len) {
   return len < 0 ? 0 : (len > max_len ? max_len : len);
 }
 
-template <bool kStep>
+template <bool kStep, bool kFp8>
 __global__ void __launch_bounds__(kWarps * 32, 1)
 decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
-  constexpr int kStageB = kStageBytes<kStep>;
+  using L = Layout<kStep, kFp8>;
+  constexpr int kStagesN = L::kStagesN;
+  constexpr int kStageB = L::kStage;
   extern __shared__ unsigned char smem_raw[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t bars = raw + warp * kStages * 8;
-  int4* descs = reinterpret_cast<int4*>(smem_raw + kDescOffset) + warp * kStages;
-  int* prefix = reinterpret_cast<int*>(smem_raw + kPrefixOffset);  // N_s, s = 0..S
+  const uint32_t bars = raw + warp * kStagesN * 8;
+  int4* descs = reinterpret_cast<int4*>(smem_raw + L::kDescOff) + warp * kStagesN;
+  int* prefix = reinterpret_cast<int*>(smem_raw + L::kPrefixOff);  // N_s, s = 0..S
   // 128-byte swizzled TMA destinations must sit on 1024-byte boundaries.
   const uint32_t tiles =
-      ((raw + kPrefixOffset + prefix_bytes(a.num_seqs) + 1023u) & ~1023u) + warp * kStages * kStageB;
+      ((raw + L::kPrefixOff + prefix_bytes(a.num_seqs) + 1023u) & ~1023u) + warp * kStagesN * kStageB;
   if (lane == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(bars + 8 * st, 1);
+    for (int st = 0; st < kStagesN; ++st) mbar_init(bars + 8 * st, 1);
     fence_mbar_init();
     prefetch_tensor_map(&tm_k);
     prefetch_tensor_map(&tm_v);
@@ -275,7 +283,7 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
       descs[st] = make_int4(seg, fl | (ok ? static_cast<int>(kHasData) : 0), slot, blk);
       const uint32_t bar = bars + 8 * st;
       const uint32_t dst = tiles + st * kStageB;
-      const uint32_t bytes = (ok ? 2u * kTileBytes : 0u) + (first ? static_cast<uint32_t>(G) * 256u : 0u) +
+      const uint32_t bytes = (ok ? 2u * L::kTile : 0u) + (first ? static_cast<uint32_t>(G) * 256u : 0u) +
                              (trig ? kHeadDim * 4u : 0u) + (fresh ? kHeadDim * 4u : 0u);
       const int s = seg / Hkv;
       const int g = seg - s * Hkv;
@@ -284,21 +292,26 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
         mbar_arrive_expect_tx(bar, bytes);
         if (ok) {
           const int y = (blk * Hkv + g) * kBlockSize;
-          tma_load_2d(dst, &tm_k, 0, y, bar);
-          tma_load_2d(dst + kHalfBytes, &tm_k, 64, y, bar);
-          tma_load_2d(dst + 2 * kHalfBytes, &tm_v, 0, y, bar);
-          tma_load_2d(dst + 3 * kHalfBytes, &tm_v, 64, y, bar);
+          if constexpr (kFp8) {  // one 128-byte x 16-row box per tile
+            tma_load_2d(dst, &tm_k, 0, y, bar);
+            tma_load_2d(dst + L::kTile, &tm_v, 0, y, bar);
+          } else {               // two 64-column halves per tile
+            tma_load_2d(dst, &tm_k, 0, y, bar);
+            tma_load_2d(dst + kHalfBytes, &tm_k, 64, y, bar);
+            tma_load_2d(dst + 2 * kHalfBytes, &tm_v, 0, y, bar);
+            tma_load_2d(dst + 3 * kHalfBytes, &tm_v, 64, y, bar);
+          }
         }
         if (first) {
           const size_t head0 = static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(g) * G;
-          bulk_copy_g2s(dst + 2 * kTileBytes, a.q + head0 * kHeadDim, static_cast<uint32_t>(G) * 256u, bar);
+          bulk_copy_g2s(dst + L::kQOff, a.q + head0 * kHeadDim, static_cast<uint32_t>(G) * 256u, bar);
         }
         if (trig)
-          bulk_copy_g2s(dst + kCosSinOffset, a.cos_sin + static_cast<size_t>(pos) * kHeadDim, kHeadDim * 4u, bar);
+          bulk_copy_g2s(dst + L::kCosSinOff, a.cos_sin + static_cast<size_t>(pos) * kHeadDim, kHeadDim * 4u, bar);
         if (fresh) {
           const size_t row = (static_cast<size_t>(s) * Hkv + g) * kHeadDim;
-          bulk_copy_g2s(dst + kNewKOffset, a.k_new + row, kHeadDim * 2u, bar);
-          bulk_copy_g2s(dst + kNewVOffset, a.v_new + row, kHeadDim * 2u, bar);
+          bulk_copy_g2s(dst + L::kNewKOff, a.k_new + row, kHeadDim * 2u, bar);
+          bulk_copy_g2s(dst + L::kNewVOff, a.v_new + row, kHeadDim * 2u, bar);
         }
       } else {
         mbar_arrive(bar);
@@ -313,6 +326,8 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
   const uint32_t v_row = static_cast<uint32_t>((r + 8 * (mi >> 1)) * 128);  // V: tokens 0-7 / 8-15
   const int v_col = mi & 1;                                                  // V: chunk 2mt / 2mt+1
   uint32_t qb[8][2];                     // B operand q^T: head gq, dims 16kk + 2cq (+1), +8
+                                         // (E4M3 caches: dims 16kk + 4cq .. +3, f16)
+  float k_fold = 0.f, v_fold = 0.f;      // E4M3 caches: softmax scale * K scale, V scale
   float m0 = -INFINITY, m1 = -INFINITY;  // running max of head columns 2cq, 2cq+1
   float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
   float o[8][4];                         // O^T: dims 16mt + gq (+8), heads 2cq, 2cq+1
@@ -323,31 +338,60 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int4 d = descs[st];
     const uint32_t fl = static_cast<uint32_t>(d.y);
     const uint32_t kt = tiles + st * kStageB;
-    const uint32_t vt = kt + 2 * kHalfBytes;
+    const uint32_t vt = kt + (kFp8 ? L::kTile : 2 * kHalfBytes);
     unsigned char* const stage = smem_raw + (kt - raw);  // generic address of the stage
     if (fl & kFirst) {
-      // q rows sit unswizzled at 256-byte stride; rows >= G are not real heads.
-      const uint32_t qt = kt + 2 * kTileBytes + static_cast<uint32_t>(r * 256);
+      if constexpr (kFp8) {
+        // B fragments in the order the E4M3 K fragments come in (k index permuted, see
+        // fp8_scores): lane (gq, cq) takes dims 16c + 4cq .. 16c + 4cq + 3 of head gq as two
+        // bf16 pairs, rotates them (fused step) and widens them to f16 pairs.
+        const uint2* qrow = reinterpret_cast<const uint2*>(stage + L::kQOff + gq * 256);
+        uint2 w[8];
 #pragma unroll
-      for (int k2 = 0; k2 < 4; ++k2)
-        ldsm_x4(qt + (4 * k2 + mi) * 16, qb[2 * k2][0], qb[2 * k2][1], qb[2 * k2 + 1][0],
-                qb[2 * k2 + 1][1]);
-      if (kStep && (fl & kRope)) {
-        // RoPE on the B fragments: dims d, d+1 (d = 16kk + 8j + 2cq) sit in qb[kk][j] and their
-        // rotation partners d+64, d+65 in qb[kk+4][j] of the same lane.
-        const float* cs = reinterpret_cast<const float*>(stage + kCosSinOffset);
+        for (int c = 0; c < 8; ++c) w[c] = qrow[4 * c + cq];
+        if (kStep && (fl & kRope)) {
+          const float* cs = reinterpret_cast<const float*>(stage + L::kCosSinOff);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int dd = 16 * kk + 8 * j + 2 * cq;
-            rope_rotate_pairs(qb[kk][j], qb[kk + 4][j], *reinterpret_cast<const float2*>(cs + dd),
+          for (int c = 0; c < 4; ++c) {
+            const int dd = 16 * c + 4 * cq;
+            rope_rotate_pairs(w[c].x, w[c + 4].x, *reinterpret_cast<const float2*>(cs + dd),
                               *reinterpret_cast<const float2*>(cs + 64 + dd));
+            rope_rotate_pairs(w[c].y, w[c + 4].y, *reinterpret_cast<const float2*>(cs + dd + 2),
+                              *reinterpret_cast<const float2*>(cs + 66 + dd));
           }
-      }
-      if (gq >= G) {
+        }
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) qb[kk][0] = qb[kk][1] = 0u;
+        for (int c = 0; c < 8; ++c) {
+          qb[c][0] = gq < G ? bf16x2_to_f16x2(w[c].x) : 0u;
+          qb[c][1] = gq < G ? bf16x2_to_f16x2(w[c].y) : 0u;
+        }
+        const int g = d.x % Hkv;
+        k_fold = a.scale_log2 * a.k_scale[g];
+        v_fold = a.v_scale[g];
+      } else {
+        // q rows sit unswizzled at 256-byte stride; rows >= G are not real heads.
+        const uint32_t qt = kt + L::kQOff + static_cast<uint32_t>(r * 256);
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2)
+          ldsm_x4(qt + (4 * k2 + mi) * 16, qb[2 * k2][0], qb[2 * k2][1], qb[2 * k2 + 1][0],
+                  qb[2 * k2 + 1][1]);
+        if (kStep && (fl & kRope)) {
+          // RoPE on the B fragments: dims d, d+1 (d = 16kk + 8j + 2cq) sit in qb[kk][j] and their
+          // rotation partners d+64, d+65 in qb[kk+4][j] of the same lane.
+          const float* cs = reinterpret_cast<const float*>(stage + L::kCosSinOff);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int dd = 16 * kk + 8 * j + 2 * cq;
+              rope_rotate_pairs(qb[kk][j], qb[kk + 4][j], *reinterpret_cast<const float2*>(cs + dd),
+                                *reinterpret_cast<const float2*>(cs + 64 + dd));
+            }
+        }
+        if (gq >= G) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) qb[kk][0] = qb[kk][1] = 0u;
+        }
       }
       m0 = m1 = -INFINITY;
       l0 = l1 = 0.f;
@@ -360,44 +404,87 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
         // The new token (row valid - 1 of this tile): rotate its k, write k and v into the
         // staged tiles before they are read, and store both into the cache slot.
         const int row = valid - 1;
-        const uint32_t* kn = reinterpret_cast<const uint32_t*>(stage + kNewKOffset);
-        const uint32_t* vn = reinterpret_cast<const uint32_t*>(stage + kNewVOffset);
-        const float* cs = reinterpret_cast<const float*>(stage + kCosSinOffset);
+        const uint32_t* kn = reinterpret_cast<const uint32_t*>(stage + L::kNewKOff);
+        const uint32_t* vn = reinterpret_cast<const uint32_t*>(stage + L::kNewVOff);
+        const float* cs = reinterpret_cast<const float*>(stage + L::kCosSinOff);
         uint32_t klo = kn[lane], khi = kn[32 + lane];  // dims 2l, 2l+1 and 2l+64, 2l+65
         rope_rotate_pairs(klo, khi, reinterpret_cast<const float2*>(cs)[lane],
                           reinterpret_cast<const float2*>(cs + 64)[lane]);
         const uint32_t vlo = vn[lane], vhi = vn[32 + lane];
-        // byte 4l of the row in each 64-column half, through the 128-byte swizzle
-        const int off = row * 128 + ((((lane >> 2) ^ (row & 7)) << 4) | ((lane & 3) << 2));
-        *reinterpret_cast<uint32_t*>(stage + off) = klo;
-        *reinterpret_cast<uint32_t*>(stage + kHalfBytes + off) = khi;
-        *reinterpret_cast<uint32_t*>(stage + 2 * kHalfBytes + off) = vlo;
-        *reinterpret_cast<uint32_t*>(stage + 3 * kHalfBytes + off) = vhi;
         const int s = d.x / Hkv;
         const int g = d.x - s * Hkv;
         const size_t crow = ((static_cast<size_t>(d.w) * Hkv + g) * kBlockSize + row) * kHeadDim;
-        uint32_t* kc = reinterpret_cast<uint32_t*>(a.k_store + crow);
-        uint32_t* vc = reinterpret_cast<uint32_t*>(a.v_store + crow);
-        kc[lane] = klo;
-        kc[32 + lane] = khi;
-        vc[lane] = vlo;
-        vc[32 + lane] = vhi;
+        if constexpr (kFp8) {
+          // E4M3 codes of k_rot / k_scale and v / v_scale, as the FP8 store kernel makes them.
+          const float ik = __frcp_rn(a.k_scale[g]), iv = __frcp_rn(a.v_scale[g]);
+          const uint16_t ck0 = e4m3x2_of(klo, ik), ck1 = e4m3x2_of(khi, ik);
+          const uint16_t cv0 = e4m3x2_of(vlo, iv), cv1 = e4m3x2_of(vhi, iv);
+          // bytes 2l and 2l + 64 of the row, through the 128-byte swizzle
+          const int base = row * 128 + 2 * (lane & 7);
+          const int off0 = base + (((lane >> 3) ^ (row & 7)) << 4);
+          const int off1 = base + ((((lane >> 3) + 4) ^ (row & 7)) << 4);
+          *reinterpret_cast<uint16_t*>(stage + off0) = ck0;
+          *reinterpret_cast<uint16_t*>(stage + off1) = ck1;
+          *reinterpret_cast<uint16_t*>(stage + L::kTile + off0) = cv0;
+          *reinterpret_cast<uint16_t*>(stage + L::kTile + off1) = cv1;
+          uint16_t* kc = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.k_store) + crow);
+          uint16_t* vc = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.v_store) + crow);
+          kc[lane] = ck0;
+          kc[32 + lane] = ck1;
+          vc[lane] = cv0;
+          vc[32 + lane] = cv1;
+        } else {
+          // byte 4l of the row in each 64-column half, through the 128-byte swizzle
+          const int off = row * 128 + ((((lane >> 2) ^ (row & 7)) << 4) | ((lane & 3) << 2));
+          *reinterpret_cast<uint32_t*>(stage + off) = klo;
+          *reinterpret_cast<uint32_t*>(stage + kHalfBytes + off) = khi;
+          *reinterpret_cast<uint32_t*>(stage + 2 * kHalfBytes + off) = vlo;
+          *reinterpret_cast<uint32_t*>(stage + 3 * kHalfBytes + off) = vhi;
+          uint32_t* kc = reinterpret_cast<uint32_t*>(a.k_store + crow);
+          uint32_t* vc = reinterpret_cast<uint32_t*>(a.v_store + crow);
+          kc[lane] = klo;
+          kc[32 + lane] = khi;
+          vc[lane] = vlo;
+          vc[32 + lane] = vhi;
+        }
         // These generic writes precede a later TMA write into the same stage.
         fence_proxy_async_smem();
         __syncwarp();
       }
       // S^T = K q^T: rows = tokens, columns = heads.
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (kFp8) {
+        // E4M3 K tile: ldmatrix reads it as 16-bit pairs, so lane (gq, cq) of matrix (rows
+        // 8h..8h+7, 16-byte chunk c) gets dims 16c + 4cq .. +3 of token 8h + gq.  Widened to two
+        // f16 pairs they are the A fragments of k indices (2cq, 2cq+1) and (2cq+8, 2cq+9), the
+        // same permutation of the 16 dims as the B fragments above: the sum over k is unchanged.
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        uint32_t a0, a1, a2, a3;
-        const int chunk = (2 * kk + k_col) & 7;
-        ldsm_x4(kt + (kk >> 2) * kHalfBytes + k_row + ((chunk ^ r) << 4), a0, a1, a2, a3);
-        mma_bf16_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        for (int c2 = 0; c2 < 4; ++c2) {
+          uint32_t w0, w1, w2, w3;
+          const int chunk = 2 * c2 + k_col;
+          ldsm_x4(kt + k_row + ((chunk ^ r) << 4), w0, w1, w2, w3);
+          uint32_t lo0, hi0, lo1, hi1;
+          e4m3x4_to_f16x2x2(w0, lo0, hi0);
+          e4m3x4_to_f16x2x2(w1, lo1, hi1);
+          mma_f16_16816(sc, lo0, lo1, hi0, hi1, qb[2 * c2][0], qb[2 * c2][1]);
+          e4m3x4_to_f16x2x2(w2, lo0, hi0);
+          e4m3x4_to_f16x2x2(w3, lo1, hi1);
+          mma_f16_16816(sc, lo0, lo1, hi0, hi1, qb[2 * c2 + 1][0], qb[2 * c2 + 1][1]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sc[i] *= k_fold;
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          const int chunk = (2 * kk + k_col) & 7;
+          ldsm_x4(kt + (kk >> 2) * kHalfBytes + k_row + ((chunk ^ r) << 4), a0, a1, a2, a3);
+          mma_bf16_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sc[i] *= a.scale_log2;
       }
       // sc: [0] = (token gq, head 2cq), [1] = (gq, 2cq+1), [2] = (gq+8, 2cq), [3] = (gq+8, 2cq+1)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sc[i] *= a.scale_log2;
       uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
       if (valid < kBlockSize) {
         if (gq >= valid) sc[0] = sc[1] = -INFINITY;
@@ -419,11 +506,20 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
       const float al1 = exp2f(m1 - mn1);
       m0 = mn0;
       m1 = mn1;
-      // P rounded to bf16 (the MMA operand); the running sums add the same rounded values.
-      const uint32_t p_lo = pack_bf16x2(exp2f(sc[0] - mn0), exp2f(sc[1] - mn1));  // token gq
-      const uint32_t p_hi = pack_bf16x2(exp2f(sc[2] - mn0), exp2f(sc[3] - mn1));  // token gq+8
-      l0 = fmaf(l0, al0, bf16lo(p_lo) + bf16lo(p_hi));
-      l1 = fmaf(l1, al1, bf16hi(p_lo) + bf16hi(p_hi));
+      // P rounded to the MMA operand type (bf16, or f16 with E4M3 caches); the running sums
+      // add the same rounded values.
+      uint32_t p_lo, p_hi;
+      if constexpr (kFp8) {
+        p_lo = pack_f16x2(exp2f(sc[0] - mn0), exp2f(sc[1] - mn1));  // token gq
+        p_hi = pack_f16x2(exp2f(sc[2] - mn0), exp2f(sc[3] - mn1));  // token gq+8
+        l0 = fmaf(l0, al0, f16lo(p_lo) + f16lo(p_hi));
+        l1 = fmaf(l1, al1, f16hi(p_lo) + f16hi(p_hi));
+      } else {
+        p_lo = pack_bf16x2(exp2f(sc[0] - mn0), exp2f(sc[1] - mn1));  // token gq
+        p_hi = pack_bf16x2(exp2f(sc[2] - mn0), exp2f(sc[3] - mn1));  // token gq+8
+        l0 = fmaf(l0, al0, bf16lo(p_lo) + bf16lo(p_hi));
+        l1 = fmaf(l1, al1, bf16hi(p_lo) + bf16hi(p_hi));
+      }
       // B operand P^T: tokens 2cq, 2cq+1 (and +8) of head gq.
       const uint32_t pb0 = movmatrix_trans(p_lo);
       const uint32_t pb1 = movmatrix_trans(p_hi);
@@ -436,13 +532,34 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
           o[mt][3] *= al1;
         }
       }
-      // O^T += V^T P^T, one 16-dim slab at a time.
+      if constexpr (kFp8) {
+        // O^T += V^T P^T.  The transposing ldmatrix of the E4M3 V tile gives lane (gq, cq) the
+        // bytes V[2cq][2gq], V[2cq][2gq+1], V[2cq+1][2gq], V[2cq+1][2gq+1] of one 16-dim chunk:
+        // regrouped by dim and widened they are the A fragments of rows gq (dim 2gq) and gq+8
+        // (dim 2gq+1), k = tokens 2cq, 2cq+1.  So accumulator row gq holds dim 16mt + 2gq and
+        // row gq+8 dim 16mt + 2gq + 1.
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        uint32_t v0, v1, v2, v3;
-        const int chunk = (2 * mt + v_col) & 7;
-        ldsm_x4_trans(vt + (mt >> 2) * kHalfBytes + v_row + ((chunk ^ r) << 4), v0, v1, v2, v3);
-        mma_bf16_16816(o[mt], v0 & vmask_lo, v1 & vmask_lo, v2 & vmask_hi, v3 & vmask_hi, pb0, pb1);
+        for (int c2 = 0; c2 < 4; ++c2) {
+          uint32_t w0, w1, w2, w3;
+          const int chunk = 2 * c2 + k_col;
+          ldsm_x4_trans(vt + k_row + ((chunk ^ r) << 4), w0, w1, w2, w3);
+          uint32_t e0, d0, e1, d1;
+          e4m3x4_pairs_to_f16(w0, e0, d0);  // tokens 2cq, 2cq+1: dims 2gq (e), 2gq+1 (d)
+          e4m3x4_pairs_to_f16(w1, e1, d1);  // tokens 2cq+8, 2cq+9
+          mma_f16_16816(o[2 * c2], e0 & vmask_lo, d0 & vmask_lo, e1 & vmask_hi, d1 & vmask_hi, pb0, pb1);
+          e4m3x4_pairs_to_f16(w2, e0, d0);
+          e4m3x4_pairs_to_f16(w3, e1, d1);
+          mma_f16_16816(o[2 * c2 + 1], e0 & vmask_lo, d0 & vmask_lo, e1 & vmask_hi, d1 & vmask_hi, pb0, pb1);
+        }
+      } else {
+        // O^T += V^T P^T, one 16-dim slab at a time.
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t v0, v1, v2, v3;
+          const int chunk = (2 * mt + v_col) & 7;
+          ldsm_x4_trans(vt + (mt >> 2) * kHalfBytes + v_row + ((chunk ^ r) << 4), v0, v1, v2, v3);
+          mma_bf16_16816(o[mt], v0 & vmask_lo, v1 & vmask_lo, v2 & vmask_hi, v3 & vmask_hi, pb0, pb1);
+        }
       }
     }
     if (fl & kLast) {
@@ -457,7 +574,36 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
         L0 += __shfl_xor_sync(kFullMask, L0, x);
         L1 += __shfl_xor_sync(kFullMask, L1, x);
       }
-      if (fl & kWhole) {
+      if constexpr (kFp8) {
+        // Accumulator rows gq / gq+8 are dims 16mt + 2gq / +1 of heads 2cq, 2cq+1: each lane
+        // holds a dim pair of two heads, scaled by the V scale of the KV head.
+        const bool h0 = 2 * cq < G;
+        const bool h1 = 2 * cq + 1 < G;
+        if (fl & kWhole) {
+          const float i0 = v_fold / L0;
+          const float i1 = v_fold / L1;
+          uint32_t* orow0 = reinterpret_cast<uint32_t*>(a.out + (head0 + 2 * cq) * kHeadDim);
+          uint32_t* orow1 = orow0 + kHeadDim / 2;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            if (h0) orow0[8 * mt + gq] = pack_bf16x2(o[mt][0] * i0, o[mt][2] * i0);
+            if (h1) orow1[8 * mt + gq] = pack_bf16x2(o[mt][1] * i1, o[mt][3] * i1);
+          }
+        } else {
+          const size_t row0 = static_cast<size_t>(d.z) * G + 2 * cq;  // head 2cq of the group
+          float2* w0 = reinterpret_cast<float2*>(a.ws_o + row0 * kHeadDim) + gq;
+          float2* w1 = w0 + kHeadDim / 2;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            if (h0) w0[8 * mt] = make_float2(o[mt][0] * v_fold, o[mt][2] * v_fold);
+            if (h1) w1[8 * mt] = make_float2(o[mt][1] * v_fold, o[mt][3] * v_fold);
+          }
+          if (gq == 0) {
+            if (h0) a.ws_ml[row0] = make_float2(m0, L0);
+            if (h1) a.ws_ml[row0 + 1] = make_float2(m1, L1);
+          }
+        }
+      } else if (fl & kWhole) {
         const float i0 = 1.f / L0;
         const float i1 = 1.f / L1;
         uint32_t* orow = reinterpret_cast<uint32_t*>(a.out + (head0 + gq) * kHeadDim);
@@ -499,24 +645,24 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
   // ---------------------------------------------------------------- pipeline --------
   int produced = 0, consumed = 0;
   bool more = true;
-  while (more && produced < kStages) {
-    if (produce(produced % kStages)) ++produced;
+  while (more && produced < kStagesN) {
+    if (produce(produced % kStagesN)) ++produced;
     else more = false;
   }
   while (consumed < produced) {
-    const int st = consumed % kStages;
-    if (!mbar_wait_bounded(bars + 8 * st, (consumed / kStages) & 1)) {
+    const int st = consumed % kStagesN;
+    if (!mbar_wait_bounded(bars + 8 * st, (consumed / kStagesN) & 1)) {
       if (lane == 0) raise_flag(a.status, PA_FLAG_TIMEOUT);
       // Let the other copies in flight land (bounded) before the CTA can exit.
       for (int j = consumed + 1; j < produced; ++j)
-        mbar_wait_bounded(bars + 8 * (j % kStages), (j / kStages) & 1);
+        mbar_wait_bounded(bars + 8 * (j % kStagesN), (j / kStagesN) & 1);
       break;
     }
     consume(st);
     ++consumed;
     __syncwarp();
     if (more) {
-      if (produce(produced % kStages)) ++produced;
+      if (produce(produced % kStagesN)) ++produced;
       else more = false;
     }
   }
@@ -622,12 +768,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Tensor map of one cache viewed as a 2-D bf16 array [num_blocks * Hkv * 16 rows][128 cols],
-// box 64 cols x 16 rows, 128-byte swizzle.  Encoded maps are cached by (address, rows).
-bool cache_tensor_map(const void* cache, long long rows, CUtensorMap* out) {
+// Tensor map of one cache viewed as a 2-D array [num_blocks * Hkv * 16 rows][128 cols] with
+// 128-byte swizzle: bf16 in boxes of 64 cols x 16 rows (two per tile), E4M3 bytes in boxes of
+// 128 cols x 16 rows (one per tile).  Encoded maps are cached by (address, rows, type).
+bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* out) {
   struct Entry {
     const void* ptr;
     long long rows;
+    bool fp8;
     CUtensorMap map;
   };
   static std::mutex mu;
@@ -635,23 +783,25 @@ bool cache_tensor_map(const void* cache, long long rows, CUtensorMap* out) {
   static int used = 0, next = 0;
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < used; ++i)
-    if (table[i].ptr == cache && table[i].rows == rows) {
+    if (table[i].ptr == cache && table[i].rows == rows && table[i].fp8 == fp8) {
       *out = table[i].map;
       return true;
     }
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return false;
   CUtensorMap m;
+  const cuuint64_t elem = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * elem};
+  cuuint32_t box[2] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(kBlockSize)};
   cuuint32_t estr[2] = {1, 1};
-  if (encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  if (encode(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
   const int slot = used < 16 ? used++ : (next++ & 15);
-  table[slot] = Entry{cache, rows, m};
+  table[slot] = Entry{cache, rows, fp8, m};
   *out = m;
   return true;
 }
@@ -659,7 +809,7 @@ bool cache_tensor_map(const void* cache, long long rows, CUtensorMap* out) {
 // Persistent grid size for this device: SMs x resident CTAs per SM, capped so that the grid
 // has at most kMaxDecodeWarps warps (looked up once per device and kernel variant, at the
 // largest shared-memory footprint the kernel can ask for).
-template <bool kStep>
+template <bool kStep, bool kFp8>
 cudaError_t persistent_ctas(int* ctas) {
   static std::mutex mu;
   static int cached[64] = {};
@@ -669,13 +819,14 @@ cudaError_t persistent_ctas(int* ctas) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (!cached[dev]) {
-    const int smem = smem_bytes<kStep>(kMaxDecodeSeqs);
-    err = cudaFuncSetAttribute(decode_partition_kernel<kStep>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = Layout<kStep, kFp8>::smem(kMaxDecodeSeqs);
+    auto kernel = decode_partition_kernel<kStep, kFp8>;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     int sms = 0, per_sm = 0;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_partition_kernel<kStep>, kWarps * 32, smem);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kWarps * 32, smem);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     cached[dev] = min(sms * per_sm, kMaxDecodeWarps / kWarps);
@@ -684,19 +835,11 @@ cudaError_t persistent_ctas(int* ctas) {
   return cudaSuccess;
 }
 
-}  // namespace
-
-cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
-  DecodeArgs a = args;
-  const int G = a.num_q_heads / a.num_kv_heads;
-  if (G < 1 || G > 8 || a.num_seqs > kMaxDecodeSeqs) return cudaErrorInvalidValue;
-  const long long rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * kBlockSize;
-  CUtensorMap tm_k, tm_v;
-  if (!cache_tensor_map(a.k_cache, rows, &tm_k) || !cache_tensor_map(a.v_cache, rows, &tm_v))
-    return cudaErrorInvalidValue;
-  const bool step = a.k_new != nullptr;
+template <bool kStep, bool kFp8>
+cudaError_t launch_partition(DecodeArgs& a, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                             const cudaLaunchAttribute* attr, cudaStream_t stream) {
   int max_ctas = 0;
-  cudaError_t err = step ? persistent_ctas<true>(&max_ctas) : persistent_ctas<false>(&max_ctas);
+  cudaError_t err = persistent_ctas<kStep, kFp8>(&max_ctas);
   if (err != cudaSuccess) return err;
   // No more CTAs than there can be ranges (ranges are dealt to the CTAs one at a time).
   const long long jobs_bound = static_cast<long long>(a.num_seqs) * a.num_kv_heads *
@@ -705,19 +848,36 @@ cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
                                         : (jobs_bound + kMinRangeBlocks - 1) / kMinRangeBlocks;
   const long long ctas = min(static_cast<long long>(max_ctas), want);
   a.num_warps = static_cast<int>(ctas) * kWarps;
-
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas));
   cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = step ? smem_bytes<true>(a.num_seqs) : smem_bytes<false>(a.num_seqs);
+  cfg.dynamicSmemBytes = Layout<kStep, kFp8>::smem(a.num_seqs);
   cfg.stream = stream;
-  cfg.attrs = attr;
+  cfg.attrs = const_cast<cudaLaunchAttribute*>(attr);
   cfg.numAttrs = 1;
-  err = step ? cudaLaunchKernelEx(&cfg, decode_partition_kernel<true>, tm_k, tm_v, a)
-             : cudaLaunchKernelEx(&cfg, decode_partition_kernel<false>, tm_k, tm_v, a);
+  return cudaLaunchKernelEx(&cfg, decode_partition_kernel<kStep, kFp8>, tm_k, tm_v, a);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
+  DecodeArgs a = args;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  if (G < 1 || G > 8 || a.num_seqs > kMaxDecodeSeqs) return cudaErrorInvalidValue;
+  const bool step = a.k_new != nullptr;
+  const bool fp8 = a.k_scale != nullptr;
+  const long long rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * kBlockSize;
+  CUtensorMap tm_k, tm_v;
+  if (!cache_tensor_map(a.k_cache, rows, fp8, &tm_k) || !cache_tensor_map(a.v_cache, rows, fp8, &tm_v))
+    return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaError_t err;
+  if (fp8) err = step ? launch_partition<true, true>(a, tm_k, tm_v, attr, stream)
+                      : launch_partition<false, true>(a, tm_k, tm_v, attr, stream);
+  else err = step ? launch_partition<true, false>(a, tm_k, tm_v, attr, stream)
+                  : launch_partition<false, false>(a, tm_k, tm_v, attr, stream);
   if (err != cudaSuccess) return err;
 
   const long long merge_warps = static_cast<long long>(a.num_seqs) * a.num_q_heads * kMergeSplit;

@@ -8,6 +8,9 @@
 // rotate k into its cache slot and copy v next to it.  Lane l owns the rotation pairs
 // (2l, 2l+64) and (2l+1, 2l+65): two 32-bit loads of bf16 pairs, two float2 loads of the
 // cos/sin row, two 32-bit stores, so each head vector moves as one 256-byte line.
+// With E4M3 caches (kFp8) the rotated k and the raw v are stored as the E4M3 codes of
+// x * (1 / scale of the KV head), both in fp32 with round to nearest, coded round to nearest
+// even with saturation; two one-byte codes per lane and pair.
 // Launch-bound (a few KiB per token): no shared memory, no staging.
 
 #include "pa_device.cuh"
@@ -18,6 +21,7 @@ namespace {
 
 constexpr int kRopeWarps = 8;
 
+template <bool kFp8>
 __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_store_kernel(const RopeArgs a) {
   pdl_wait_prior_grid();
   pdl_allow_next_grid();
@@ -35,6 +39,8 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_store_kernel(const Ro
   }
   const uint32_t* src;
   uint32_t* dst;
+  uint16_t* dst8 = nullptr;  // E4M3 K cache row
+  float inv_k = 0.f;
   if (h < a.num_q_heads) {
     dst = reinterpret_cast<uint32_t*>(a.q + (static_cast<size_t>(t) * a.num_q_heads + h) * kHeadDim);
     src = dst;
@@ -52,8 +58,19 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_store_kernel(const Ro
     const size_t cache_off = ((static_cast<size_t>(blk) * a.num_kv_heads + g) * kBlockSize + off) * kHeadDim;
     src = reinterpret_cast<const uint32_t*>(a.k + in_off);
     dst = reinterpret_cast<uint32_t*>(a.k_cache + cache_off);
-    reinterpret_cast<uint2*>(a.v_cache + cache_off)[lane] =
-        reinterpret_cast<const uint2*>(a.v + in_off)[lane];
+    if constexpr (kFp8) {
+      uint8_t* kc8 = reinterpret_cast<uint8_t*>(a.k_cache) + cache_off;
+      uint16_t* vc8 = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.v_cache) + cache_off);
+      const uint32_t* vin = reinterpret_cast<const uint32_t*>(a.v + in_off);
+      const float inv_v = __frcp_rn(a.v_scale[g]);
+      vc8[lane] = e4m3x2_of(vin[lane], inv_v);             // dims 2l, 2l+1
+      vc8[32 + lane] = e4m3x2_of(vin[32 + lane], inv_v);   // dims 2l+64, 2l+65
+      dst8 = reinterpret_cast<uint16_t*>(kc8);
+      inv_k = __frcp_rn(a.k_scale[g]);
+    } else {
+      reinterpret_cast<uint2*>(a.v_cache + cache_off)[lane] =
+          reinterpret_cast<const uint2*>(a.v + in_off)[lane];
+    }
   }
   const float* row = a.cos_sin + static_cast<size_t>(pos) * kHeadDim;
   const float2 c = reinterpret_cast<const float2*>(row)[lane];        // cos of pairs 2l, 2l+1
@@ -61,8 +78,13 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rope_kv_store_kernel(const Ro
   uint32_t lo = src[lane];        // x[2l], x[2l+1]
   uint32_t hi = src[32 + lane];   // x[2l+64], x[2l+65]
   rope_rotate_pairs(lo, hi, c, s);
-  dst[lane] = lo;
-  dst[32 + lane] = hi;
+  if (kFp8 && dst8) {
+    dst8[lane] = e4m3x2_of(lo, inv_k);
+    dst8[32 + lane] = e4m3x2_of(hi, inv_k);
+  } else {
+    dst[lane] = lo;
+    dst[32 + lane] = hi;
+  }
 }
 
 // Self-test of the bounded wait every kernel here uses on its shared-memory copies: one warp
@@ -98,7 +120,8 @@ cudaError_t launch_rope_kv_store(const RopeArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, rope_kv_store_kernel, a);
+  if (a.k_scale) return cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<true>, a);
+  return cudaLaunchKernelEx(&cfg, rope_kv_store_kernel<false>, a);
 }
 
 }  // namespace pa

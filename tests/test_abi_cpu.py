@@ -32,7 +32,7 @@ def test_header_declares_the_entry_points():
     for must in ("pa_rope_kv_store", "pa_decode", "pa_decode_workspace_size",
                  "pa_decode_partition_tokens", "pa_get_device_status", "pa_status_string",
                  "pa_selftest_wait_timeout", "pa_decode_static_workspace", "pa_decode_step",
-                 "pa_copy_blocks"):
+                 "pa_copy_blocks", "pa_rope_kv_store_fp8", "pa_decode_fp8", "pa_decode_step_fp8"):
         assert must in names
 
 
@@ -134,6 +134,39 @@ def test_copy_blocks_rejects_bad_arguments_on_the_host(L):
     assert call(dst=arr(OK_PTR, MIS_PTR, OK_PTR, OK_PTR)) == b.PA_ERR_ALIGN
     assert call(pairs=P(0x10004)) == b.PA_ERR_ALIGN
     assert L.pa_copy_blocks(ctypes.byref(dims(2, 2)), 2, None, 8, None, 8, OK_PTR, 1, None) == b.PA_ERR_NULL
+
+
+def test_fp8_entry_points_reject_bad_arguments_on_the_host(L):
+    from paged_kv_cache_244_gb300 import binding as b
+    d = dims()
+
+    def dec(ks=OK_PTR, vs=OK_PTR, S=2, **kw):
+        a = dict(q=OK_PTR, kc=OK_PTR, vc=OK_PTR, bt=OK_PTR, ctx=OK_PTR, ws=OK_PTR, out=OK_PTR)
+        a.update(kw)
+        return L.pa_decode_fp8(ctypes.byref(d), S, a["q"], a["kc"], a["vc"], ks, vs, 16, a["bt"], 4,
+                               a["ctx"], 40, 0.088, 0, a["ws"], 1 << 30, a["out"], None)
+
+    assert dec(S=0) == b.PA_OK
+    assert dec(ks=None) == b.PA_ERR_NULL and dec(vs=None) == b.PA_ERR_NULL
+    assert dec(ks=MIS_PTR) == b.PA_ERR_ALIGN
+    assert dec(q=None) == b.PA_ERR_NULL and dec(kc=MIS_PTR) == b.PA_ERR_ALIGN
+    assert dec(S=-1) == b.PA_ERR_RANGE
+
+    def store(ks=OK_PTR, vs=OK_PTR, T=3):
+        return L.pa_rope_kv_store_fp8(ctypes.byref(d), T, OK_PTR, OK_PTR, OK_PTR, OK_PTR, OK_PTR, 64,
+                                      OK_PTR, OK_PTR, OK_PTR, 16, ks, vs, None)
+
+    assert store(T=0) == b.PA_OK
+    assert store(ks=None) == b.PA_ERR_NULL and store(vs=MIS_PTR) == b.PA_ERR_ALIGN
+
+    def step(ks=OK_PTR, vs=OK_PTR, S=2, k=OK_PTR):
+        return L.pa_decode_step_fp8(ctypes.byref(d), S, OK_PTR, k, OK_PTR, OK_PTR, 64, OK_PTR, OK_PTR,
+                                    ks, vs, 16, OK_PTR, 4, OK_PTR, 40, 0.088, 0, OK_PTR, 1 << 30,
+                                    OK_PTR, None)
+
+    assert step(S=0) == b.PA_OK
+    assert step(ks=None) == b.PA_ERR_NULL and step(vs=MIS_PTR) == b.PA_ERR_ALIGN
+    assert step(k=None) == b.PA_ERR_NULL
 
 
 def test_rope_kv_store_rejects_bad_arguments_on_the_host(L):
