@@ -21,6 +21,8 @@ The printed JSON line carries:
                        on one layer, timed alone with CUDA events, against the measured HBM
                        copy bandwidth;
   cpu_baseline         the fp64 oracle on the host cores over a bounded sample;
+  fp8_kv               the step's decode on E4M3 caches (pa_decode_fp8, pa_decode_step_fp8),
+                       bandwidth counted on the E4M3 bytes (--no-fp8 skips it);
   block_ops            pa_copy_blocks over K and V of 28 layers: copy-on-write inside the
                        device pools, swap out / in of a 2048-token sequence to page-locked
                        host pools, beside a plain memcpy of the same bytes (--no-block-ops
@@ -294,6 +296,7 @@ def run_gpu(args, rank, world, dist):
     # end to end through the public API with host buffers
     e2e = run_e2e(args, st, torch, binding, flush_l2)
     blocks = None if args.no_block_ops else block_ops(torch, binding, flush_l2, timed_loop, w)
+    fp8 = None if args.no_fp8 else fp8_kv(torch, binding, timed_loop, st, args.steps)
 
     rc, flags = binding.get_device_status()
     if rc != 0:
@@ -355,6 +358,7 @@ def run_gpu(args, rank, world, dist):
                 "ms_per_step": round(e2e_ms_max / args.steps, 6)},
         "gpu_launches": st.launches_per_step * args.steps,
         "block_ops": blocks,
+        "fp8_kv": fp8,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -408,6 +412,46 @@ def block_ops(torch, binding, flush_l2, timed_loop, w, layers=28, pool_blocks=10
         "swap_in": {"blocks": nseq, "GB/s": in_gbs, "us": in_us, "bytes": swap_bytes,
                     "memcpy_h2d_GB/s": h2d},
     }
+
+
+def fp8_kv(torch, binding, timed_loop, st, steps):
+    """The step's decode on E4M3 caches (one byte per element, one scale per KV head), layer 0
+    of the workload: pa_decode_fp8 and pa_decode_step_fp8, L2 flushed before each call.  The
+    codes are made once on the GPU with torch's float8 cast from the bf16 caches (set-up, not
+    timed); achieved bandwidth counts the E4M3 bytes, half the bf16 bytes."""
+    w = st.w
+
+    def codes(cache):
+        amax = cache.float().abs().nan_to_num(0.0).amax(dim=(0, 2, 3)).clamp_min(1e-3)
+        scale = (amax / 448.0).float().contiguous()
+        c = (cache.float() / scale[None, :, None, None]).clamp(-448, 448).to(torch.float8_e4m3fn)
+        return c.view(torch.uint8).contiguous(), scale
+
+    k8, ks = codes(st.k_cache[0])
+    v8, vs = codes(st.v_cache[0])
+    out = torch.empty_like(st.q[0])
+    dec = lambda: binding.decode_fp8(st.q[0], k8, v8, ks, vs, st.block_tables, st.context_lens,
+                                     w.max_context_len, w.scale, partition_tokens=st.P,
+                                     workspace=st.workspace, out=out)
+    stp = lambda: binding.decode_step_fp8(st.q[0], st.k[0], st.v[0], st.cos_sin, k8, v8, ks, vs,
+                                          st.block_tables, st.context_lens, w.max_context_len,
+                                          w.scale, partition_tokens=st.P, workspace=st.workspace,
+                                          out=out)
+    dec()
+    stp()
+    dec_ms = float(np.mean(timed_loop(dec, steps)))
+    stp_ms = float(np.mean(timed_loop(stp, steps)))
+    rc, flags = binding.get_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after the E4M3 decode: {rc} flags {flags:#x}")
+    nbytes = w.kv_bytes_per_layer() // 2
+    peak, _ = hbm_peak()
+    gbs = nbytes / (dec_ms * 1e-3) / 1e9
+    return {"algorithmic_bytes_per_launch": nbytes,
+            "pa_decode_fp8_us": round(dec_ms * 1e3, 3), "GB/s": round(gbs, 1),
+            "frac_of_hbm_copy_peak": round(gbs / peak, 4),
+            "pa_decode_step_fp8_us": round(stp_ms * 1e3, 3),
+            "context_tokens_per_s": round(int(w.context_lens.astype(np.int64).sum()) / (dec_ms * 1e-3), 1)}
 
 
 def reduce_over_ranks(maxes, sums, dist, device):
@@ -600,6 +644,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each call instead of a CUDA graph")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the E4M3-cache decode measurement")
     ap.add_argument("--no-block-ops", action="store_true",
                     help="skip the pa_copy_blocks measurements (copy-on-write, swap out / in)")
     ap.add_argument("--split-step", action="store_true",
