@@ -61,6 +61,8 @@ class Oracle:
         lib.orc_decode.restype = i
         lib.orc_decode_partitioned.argtypes = [i, i, i, i, i, p, p, p, i, p, i, p, d, i, i, p]
         lib.orc_decode_partitioned.restype = i
+        lib.orc_prefill.argtypes = [i, i, i, i, i, p, p, p, p, p, i, p, i, d, i, p, p]
+        lib.orc_prefill.restype = i
         lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         lib.orc_e4m3_to_f64.restype = d
         lib.orc_f64_to_e4m3.argtypes = [d]
@@ -76,6 +78,28 @@ class Oracle:
         lib.orc_hardware_threads.argtypes = []
         lib.orc_hardware_threads.restype = i
         self.lib = lib
+
+    def prefill(self, q, q_start, k_cache, v_cache, block_tables, context_lens, scale, nthreads=0):
+        """Paged (chunked) prefill: query i of sequence s, at position
+        context_lens[s] - n_s + i, attends causally to its cached tokens 0..position.
+        q [T, Hq, D] bf16 bits, q_start [S + 1]; returns (out fp64 [T, Hq, D], out bf16 bits)."""
+        q = _c(q, np.uint16)
+        qs = _c(q_start, np.int32)
+        kc, vc = _c(k_cache, np.uint16), _c(v_cache, np.uint16)
+        bt = _c(block_tables, np.int32)
+        ctx = _c(context_lens, np.int32)
+        T, Hq, D = q.shape
+        nb, Hkv, B, _ = kc.shape
+        S = ctx.shape[0]
+        assert qs.shape == (S + 1,) and qs[-1] == T
+        out = np.empty((T, Hq, D), np.float64)
+        outb = np.empty((T, Hq, D), np.uint16)
+        rc = self.lib.orc_prefill(S, Hq, Hkv, D, B, _ptr(q), _ptr(qs), _ptr(ctx), _ptr(kc), _ptr(vc),
+                                  nb, _ptr(bt), bt.shape[1] if bt.ndim == 2 else 0, float(scale),
+                                  int(nthreads), _ptr(out), _ptr(outb))
+        if rc != 0:
+            raise ValueError("orc_prefill rejected its arguments")
+        return out, outb
 
     # ---- FP8 (E4M3) KV cache -----------------------------------------------------------
     def e4m3_to_f64(self, code: int) -> float:

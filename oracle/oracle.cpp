@@ -392,6 +392,64 @@ int64_t orc_copy_blocks(int num_caches, int64_t block_elems, const uint16_t* con
   return skipped;
 }
 
+// Paged prefill / chunked prefill: sequence s brings n_s = q_start[s+1] - q_start[s] new
+// query tokens whose K and V are already in the cache, and context_lens[s] counts every cached
+// token including them, so query i of s sits at position p = context_lens[s] - n_s + i and
+// attends, causally, to the cached tokens 0..p of its sequence ("Pico-vLLM：从零手写的工业级LLM
+// 推理引擎实现", §2 Kernel层: PagedAttention Prefill Kernel, after the FlashAttention work;
+// "从零实现 LLM 推理引擎：深挖 vLLM 的六大核心优化", §3.3 Chunked Prefill: a prompt is prefilled
+// in chunks, each continuing from the tokens already prefilled).  A full prefill is the case
+// context_lens[s] = n_s; one new token (n_s = 1) is the decode.
+//   q [T][Hq][D] bf16 (T = q_start[S]), out [T][Hq][D].
+int orc_prefill(int S, int Hq, int Hkv, int D, int B, const uint16_t* q, const int32_t* q_start,
+                const int32_t* context_lens, const uint16_t* k_cache, const uint16_t* v_cache,
+                int num_blocks, const int32_t* block_tables, int max_blocks, double scale,
+                int nthreads, double* out_f64, uint16_t* out_bf16) {
+  if (S < 0 || !shape_ok(Hq, Hkv, D, B) || max_blocks < 0) return -1;
+  if (S == 0) return 0;
+  if (!q || !q_start || !context_lens || !k_cache || !v_cache || !block_tables) return -1;
+  if (q_start[0] != 0) return -1;
+  for (int s = 0; s < S; ++s) {
+    const int n = q_start[s + 1] - q_start[s];
+    if (n < 0 || context_lens[s] < n) return -1;
+  }
+  if (!table_ok(block_tables, max_blocks, context_lens, S, num_blocks, B)) return -1;
+  const int G = Hq / Hkv;
+  parallel_units(S * Hkv, nthreads, [&](int unit) {
+    const int s = unit / Hkv;
+    const int g = unit % Hkv;
+    const int ctx = context_lens[s];
+    const int n = q_start[s + 1] - q_start[s];
+    const int32_t* bt_row = block_tables + static_cast<size_t>(s) * max_blocks;
+    std::vector<double> scores(std::max(ctx, 1));
+    std::vector<double> o(D);
+    for (int i = 0; i < n; ++i) {
+      const int pos = ctx - n + i;          // attends to tokens 0..pos
+      for (int h = g * G; h < (g + 1) * G; ++h) {
+        const size_t obase = (static_cast<size_t>(q_start[s] + i) * Hq + h) * D;
+        head_scores(q + obase, k_cache, bt_row, g, 0, pos + 1, Hkv, B, D, scale, scores.data());
+        const double m = *std::max_element(scores.begin(), scores.begin() + pos + 1);
+        double l = 0.0;
+        std::fill(o.begin(), o.end(), 0.0);
+        for (int t = 0; t <= pos; ++t) {
+          const double p = std::exp(scores[t] - m);
+          l += p;
+          const int blk = bt_row[t / B];
+          const int off = t % B;
+          for (int d = 0; d < D; ++d)
+            o[d] += p * widen_bf16(v_cache[cache_index(blk, g, off, d, Hkv, B, D)]);
+        }
+        for (int d = 0; d < D; ++d) {
+          o[d] /= l;
+          if (out_f64) out_f64[obase + d] = o[d];
+          if (out_bf16) out_bf16[obase + d] = narrow_bf16(o[d]);
+        }
+      }
+    }
+  });
+  return 0;
+}
+
 // ---- FP8 (E4M3) KV cache with one scale per KV head --------------------------------------
 // The pages name low-precision quantisation as a way to cut memory and raise inference speed
 // ("nano-vllm：vLLM 极简实现与大模型推理流程解析", §学习要点: FP8 or INT4 quantisation with

@@ -467,6 +467,87 @@ def check_swap_out_in_preserves_decode(orc):
     assert np.array_equal(got, ref)
 
 
+# ---- paged (chunked) prefill -------------------------------------------------------------
+
+def _prefill_case(seed, ctxs, Hq=12, Hkv=2, nb=64):
+    rng = W.SplitMix64(seed)
+    Kd = [rng.normal_bf16(Hkv * c * D, 1.5).reshape(Hkv, c, D) for c in ctxs]
+    Vd = [rng.normal_bf16(Hkv * c * D, 1.0).reshape(Hkv, c, D) for c in ctxs]
+    kc, vc, bt = _paged_from_dense(Kd, Vd, nb, rng)
+    return rng, Kd, Vd, kc, vc, bt
+
+
+def check_prefill_full_equals_dense_causal(orc):
+    """Full prefill (the whole context is new) = causal dense attention (scipy softmax over
+    tokens 0..i for query i) on contiguous K/V."""
+    ctxs = [1, 17, 70]
+    Hq, Hkv = 12, 2
+    rng, Kd, Vd, kc, vc, bt = _prefill_case(51, ctxs)
+    T = sum(ctxs)
+    q = rng.normal_bf16(T * Hq * D, 1.0).reshape(T, Hq, D)
+    qs = np.concatenate([[0], np.cumsum(ctxs)]).astype(np.int32)
+    scale = 1.0 / math.sqrt(D)
+    got, _ = orc.prefill(q, qs, kc, vc, bt, np.array(ctxs, np.int32), scale)
+    for s, c in enumerate(ctxs):
+        for i in range(c):
+            for h in range(Hq):
+                K = W.bf16_bits_to_f32(Kd[s][h // 6][:i + 1]).astype(np.float64)
+                V = W.bf16_bits_to_f32(Vd[s][h // 6][:i + 1]).astype(np.float64)
+                qh = W.bf16_bits_to_f32(q[qs[s] + i, h]).astype(np.float64)
+                ref = softmax(scale * (K @ qh)) @ V
+                assert np.allclose(got[qs[s] + i, h], ref, rtol=1e-12, atol=1e-14), (s, i, h)
+
+
+def check_prefill_one_token_is_decode(orc):
+    w, q, kc, vc = _tiny_after_store(orc)
+    S = w.num_seqs
+    got, _ = orc.prefill(q, np.arange(S + 1, dtype=np.int32), kc, vc, w.block_tables,
+                         w.context_lens, w.scale)
+    ref, _ = orc.decode(q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    assert np.array_equal(got, ref)
+
+
+def check_prefill_chunks_compose(orc):
+    """A prompt prefilled in two chunks gives, token for token, the one-chunk result."""
+    ctxs = [40, 93]
+    Hq = 12
+    rng, Kd, Vd, kc, vc, bt = _prefill_case(52, ctxs)
+    T = sum(ctxs)
+    q = rng.normal_bf16(T * Hq * D, 1.0).reshape(T, Hq, D)
+    qs = np.concatenate([[0], np.cumsum(ctxs)]).astype(np.int32)
+    ctx = np.array(ctxs, np.int32)
+    whole, _ = orc.prefill(q, qs, kc, vc, bt, ctx, 0.09)
+    cut = [13, 64]                                       # first chunks
+    q1 = np.concatenate([q[qs[s]:qs[s] + cut[s]] for s in range(2)])
+    a, _ = orc.prefill(q1, np.array([0, cut[0], sum(cut)], np.int32), kc, vc, bt,
+                       np.array(cut, np.int32), 0.09)
+    q2 = np.concatenate([q[qs[s] + cut[s]:qs[s + 1]] for s in range(2)])
+    n2 = [ctxs[s] - cut[s] for s in range(2)]
+    b, _ = orc.prefill(q2, np.array([0, n2[0], sum(n2)], np.int32), kc, vc, bt, ctx, 0.09)
+    for s in range(2):
+        assert np.array_equal(whole[qs[s]:qs[s] + cut[s]], a[sum(cut[:s]):sum(cut[:s + 1])])
+        assert np.array_equal(whole[qs[s] + cut[s]:qs[s + 1]], b[sum(n2[:s]):sum(n2[:s + 1])])
+
+
+def check_prefill_is_causal(orc):
+    """Changing the K/V of token j changes exactly the outputs of queries at positions >= j."""
+    ctxs = [50]
+    Hq = 12
+    rng, Kd, Vd, kc, vc, bt = _prefill_case(53, ctxs)
+    q = rng.normal_bf16(50 * Hq * D, 1.0).reshape(50, Hq, D)
+    qs = np.array([0, 50], np.int32)
+    ctx = np.array([50], np.int32)
+    before, _ = orc.prefill(q, qs, kc, vc, bt, ctx, 0.09)
+    j = 29
+    blk, off = int(bt[0, j // 16]), j % 16
+    kc2, vc2 = kc.copy(), vc.copy()
+    kc2[blk, :, off] = rng.normal_bf16(2 * D, 3.0).reshape(2, D)
+    vc2[blk, :, off] = rng.normal_bf16(2 * D, 3.0).reshape(2, D)
+    after, _ = orc.prefill(q, qs, kc2, vc2, bt, ctx, 0.09)
+    assert np.array_equal(after[:j], before[:j])
+    assert (np.abs(after[j:] - before[j:]).max(axis=(1, 2)) > 0).all()
+
+
 # ---- FP8 (E4M3) KV cache ------------------------------------------------------------------
 # The independent reference for the E4M3 format is PyTorch's own float8_e4m3fn conversion.
 
@@ -629,4 +710,8 @@ ALL_CHECKS = [
     check_quantize_decides_in_fp32,
     check_decode_fp8_dense_equivalence,
     check_rope_kv_store_fp8_is_bf16_store_then_quantise,
+    check_prefill_full_equals_dense_causal,
+    check_prefill_one_token_is_decode,
+    check_prefill_chunks_compose,
+    check_prefill_is_causal,
 ]

@@ -85,6 +85,11 @@ MUTANTS = {
                                  "e4m3_encode(quant_input(narrow_bf16(y[d]), v_scale[h]));"),
     "fp8_decode_drops_k_scale": ("(e4m3_value(k_cache[cache_index(blk, g, off, d, Hkv, B, D)]) * ks);",
                                  "(e4m3_value(k_cache[cache_index(blk, g, off, d, Hkv, B, D)]) * 1.0);"),
+    "prefill_position_from_start": ("const int pos = ctx - n + i;          // attends to tokens 0..pos",
+                                    "const int pos = i;"),
+    "prefill_sum_drops_last": ("for (int t = 0; t <= pos; ++t) {", "for (int t = 0; t < pos; ++t) {"),
+    "prefill_q_row_stride": ("const size_t obase = (static_cast<size_t>(q_start[s] + i) * Hq + h) * D;",
+                             "const size_t obase = (static_cast<size_t>(q_start[s] + i) * Hkv + h) * D;"),
     "fp8_decode_wrong_v_head": ("o[d] += p * (e4m3_value(v_cache[cache_index(blk, g, off, d, Hkv, B, D)]) * vs);",
                                 "o[d] += p * (e4m3_value(v_cache[cache_index(blk, (g + 1) % Hkv, off, d, Hkv, B, D)]) * vs);"),
 }
