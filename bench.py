@@ -23,6 +23,8 @@ The printed JSON line carries:
   cpu_baseline         the fp64 oracle on the host cores over a bounded sample;
   fp8_kv               the step's decode on E4M3 caches (pa_decode_fp8, pa_decode_step_fp8),
                        bandwidth counted on the E4M3 bytes (--no-fp8 skips it);
+  prefill              pa_prefill on two prefill workloads, TFLOP/s against the measured bf16
+                       dense peak (--no-prefill skips it);
   block_ops            pa_copy_blocks over K and V of 28 layers: copy-on-write inside the
                        device pools, swap out / in of a 2048-token sequence to page-locked
                        host pools, beside a plain memcpy of the same bytes (--no-block-ops
@@ -73,6 +75,14 @@ def kernel_source_hash() -> str:
         h.update(name.encode())
         h.update((csrc / name).read_bytes())
     return h.hexdigest()[:16]
+
+
+def bf16_peak():
+    try:
+        d = json.loads((ROOT / "MEASURED_PEAKS.json").read_text())
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def hbm_peak():
@@ -297,6 +307,7 @@ def run_gpu(args, rank, world, dist):
     e2e = run_e2e(args, st, torch, binding, flush_l2)
     blocks = None if args.no_block_ops else block_ops(torch, binding, flush_l2, timed_loop, w)
     fp8 = None if args.no_fp8 else fp8_kv(torch, binding, timed_loop, st, args.steps)
+    pre = None if args.no_prefill else prefill_runs(torch, binding, timed_loop, max(5, args.steps // 4))
 
     rc, flags = binding.get_device_status()
     if rc != 0:
@@ -359,6 +370,7 @@ def run_gpu(args, rank, world, dist):
         "gpu_launches": st.launches_per_step * args.steps,
         "block_ops": blocks,
         "fp8_kv": fp8,
+        "prefill": pre,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -452,6 +464,42 @@ def fp8_kv(torch, binding, timed_loop, st, steps):
             "frac_of_hbm_copy_peak": round(gbs / peak, 4),
             "pa_decode_step_fp8_us": round(stp_ms * 1e3, 3),
             "context_tokens_per_s": round(int(w.context_lens.astype(np.int64).sum()) / (dec_ms * 1e-3), 1)}
+
+
+def prefill_runs(torch, binding, timed_loop, steps):
+    """pa_prefill on the named prefill workloads (4 whole 2048-token prompts; 16 chunks of 256
+    tokens continuing 1792 cached ones), Qwen2.5-1.5B attention shape, one layer, L2 flushed
+    before each call.  Tensor roofline: attention flops (4 Hq D per causal (query, key) pair)
+    over the measured bf16 dense peak."""
+    dev = torch.device("cuda")
+    peak, kind = bf16_peak()
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    res = {}
+    for name in W.PREFILL_WORKLOADS:
+        w = W.make_prefill(name)
+        q, kc, vc = bf(w.q), bf(w.k_cache), bf(w.v_cache)
+        qs = torch.from_numpy(w.q_start).to(dev)
+        bt = torch.from_numpy(w.block_tables).to(dev)
+        ctx = torch.from_numpy(w.context_lens).to(dev)
+        out = torch.empty_like(q)
+        call = lambda: binding.prefill(q, qs, kc, vc, bt, ctx, w.max_query_len, w.max_context_len,
+                                       w.scale, out=out)
+        call()
+        ms = float(np.mean(timed_loop(call, steps)))
+        rc, flags = binding.get_device_status()
+        if rc != 0:
+            raise RuntimeError(f"device status after pa_prefill: {rc} flags {flags:#x}")
+        tf = w.attention_flops() / (ms * 1e-3) / 1e12
+        res[name] = {"num_seqs": w.num_seqs, "new_tokens": w.num_tokens,
+                     "max_context_len": w.max_context_len, "us": round(ms * 1e3, 2),
+                     "attention_flops": w.attention_flops(), "TFLOP/s": round(tf, 1),
+                     "roofline": {"bound": "tensor", "peak": peak, "peak_kind": f"{kind} bf16_tflops",
+                                  "unit": "TFLOP/s", "frac": round(tf / peak, 4)},
+                     "new_tokens_per_s": round(w.num_tokens / (ms * 1e-3), 1)}
+    return res
 
 
 def reduce_over_ranks(maxes, sums, dist, device):
@@ -645,6 +693,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each call instead of a CUDA graph")
     ap.add_argument("--no-fp8", action="store_true", help="skip the E4M3-cache decode measurement")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the pa_prefill measurement")
     ap.add_argument("--no-block-ops", action="store_true",
                     help="skip the pa_copy_blocks measurements (copy-on-write, swap out / in)")
     ap.add_argument("--split-step", action="store_true",

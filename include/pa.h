@@ -9,8 +9,8 @@
  *   [PV]  "Pico-vLLM：从零手写的工业级LLM推理引擎实现"
  *         §1 模型实现层: RoPE computed with rotate_half in place; GQA, where groups of query
  *            heads share one KV head.
- *         §2 Kernel层: the PagedAttention decode kernel (one new token per sequence attends
- *            over its cached context) and the fused RoPE + KV cache store.
+ *         §2 Kernel层: the PagedAttention prefill and decode kernels (new tokens attend over
+ *            their cached context) and the fused RoPE + KV cache store.
  *         §H200上的详细对比: Flash Decode, i.e. the context split into partitions whose
  *            partial softmax results are merged.
  *   [NV]  "nano-vllm：vLLM 极简实现与大模型推理流程解析"
@@ -22,6 +22,8 @@
  *            sequence has a block_table mapping logical block index -> physical block id.
  *         §3.2 Continuous Batching: append_slot gives every running sequence one new slot
  *            per decode step.
+ *         §3.3 Chunked Prefill: a long prompt is prefilled a chunk at a time, each chunk
+ *            continuing from the tokens already prefilled.
  *         §3.4 Prefix Caching: blocks shared between sequences are reference counted and
  *            copied before a write (copy-on-write), so the block a new token goes to is
  *            never shared.
@@ -223,6 +225,43 @@ int pa_decode_step(const pa_dims* dims, int num_seqs, const void* q, const void*
                    const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                    int max_context_len, float scale, int partition_tokens, void* workspace,
                    size_t workspace_bytes, void* out, void* stream);
+
+/*
+ * pa_prefill -- paged (chunked) prefill attention ([PV] §2: the PagedAttention prefill kernel;
+ * [ME] §3.3 Chunked Prefill: a prompt is prefilled in chunks, each continuing from the tokens
+ * already in the cache; [ME] §3.4: a prefix found in the cache is not recomputed).
+ *
+ * Sequence s brings n_s = q_start[s+1] - q_start[s] new query tokens, rows q_start[s] ..
+ * q_start[s+1] - 1 of q and out, whose K and V are already stored in the paged cache (e.g. by
+ * pa_rope_kv_store with positions context_lens[s] - n_s + i).  context_lens[s] counts every
+ * cached token of s including the new ones.  Query i of s sits at position
+ * p = context_lens[s] - n_s + i and, for each query head h (KV head g = h / (Hq / Hkv)):
+ *   out[q_start[s] + i][h] = sum_{t <= p} softmax_t(scale * q . K_t) V_t   (bf16 RNE)
+ * with K_t, V_t reached through block_tables[s][t / 16] as in pa_decode.  A full prefill is
+ * context_lens[s] = n_s; one new token per sequence is pa_decode's result.
+ * Device-side errors: a sequence with q_start[s] < 0, n_s < 0, q_start[s+1] > num_tokens,
+ * n_s > max_query_len, context_lens[s] < n_s or > max_context_len is skipped (its rows are not
+ * written), PA_FLAG_CONTEXT_LEN_OOB; a block id outside [0, num_blocks) -> that block is
+ * skipped, PA_FLAG_BLOCK_ID_OOB.
+ *
+ *   num_seqs          S >= 0, S * Hkv <= 65535 (0 is a no-op)
+ *   num_tokens        T = rows of q and out (0 is a no-op)
+ *   q                 [T][Hq][D] bf16 (rotated), read only
+ *   q_start           [S + 1] int32, device, non-decreasing, q_start[0] = 0
+ *   max_query_len     host bound of every n_s, 1 <= it <= max_context_len
+ *   k_cache, v_cache  [num_blocks][Hkv][16][D] bf16, read only
+ *   block_tables      [S][max_blocks] int32
+ *   context_lens      [S] int32
+ *   max_context_len   host bound of context_lens, 1 <= it <= max_blocks * 16
+ *   scale             softmax scale, finite and > 0
+ *   out               [T][Hq][D] bf16, written at the rows of valid sequences
+ * Returns PA_OK or a PA_ERR_* code (nothing launched on error).  Launches one kernel.
+ */
+int pa_prefill(const pa_dims* dims, int num_seqs, int num_tokens, const void* q,
+               const int32_t* q_start, int max_query_len, const void* k_cache,
+               const void* v_cache, int num_blocks, const int32_t* block_tables, int max_blocks,
+               const int32_t* context_lens, int max_context_len, float scale, void* out,
+               void* stream);
 
 /*
  * FP8 (E4M3) KV cache -- the same three operations over caches of one-byte codes

@@ -77,6 +77,8 @@ def lib():
         L.pa_decode_step_fp8.argtypes = [pd, i, p, p, p, p, i, p, p, p, p, i, p, i, p, i, f, i, p,
                                          ctypes.c_size_t, p, p]
         L.pa_decode_step_fp8.restype = i
+        L.pa_prefill.argtypes = [pd, i, i, p, p, i, p, p, i, p, i, p, i, f, p, p]
+        L.pa_prefill.restype = i
         L.pa_copy_blocks.argtypes = [pd, i, p, ctypes.c_int64, p, ctypes.c_int64, p, i, p]
         L.pa_copy_blocks.restype = i
         L.pa_get_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
@@ -236,6 +238,35 @@ def decode_step(q, k, v, cos_sin, k_cache, v_cache, block_tables, context_lens, 
         int(partition_tokens), _dev_ptr(workspace, "workspace"), ws_bytes, _dev_ptr(out, "out", bf),
         _stream(stream))
     _check(rc, "pa_decode_step")
+    return out
+
+
+def prefill(q, q_start, k_cache, v_cache, block_tables, context_lens, max_query_len,
+            max_context_len, scale, out=None, stream=None):
+    """Paged (chunked) prefill attention (pa_prefill).  Returns out [T, Hq, D] bf16.
+
+    q [T, Hq, D] bf16 (rotated); q_start [S + 1] int32 (rows of each sequence); context_lens
+    [S] int32 (cached tokens including the new ones); max_query_len / max_context_len host
+    bounds; caches and block_tables as for decode().
+    """
+    T, Hq, D = q.shape
+    nb, Hkv, B, D2 = k_cache.shape
+    S = context_lens.shape[0]
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shape mismatch")
+    if q_start.shape != (S + 1,) or block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("q_start / block_tables shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    dims = make_dims(Hq, Hkv, D, B)
+    bf = torch.bfloat16
+    rc = lib().pa_prefill(
+        ctypes.byref(dims), S, T, _dev_ptr(q, "q", bf), _dev_ptr(q_start, "q_start", torch.int32),
+        int(max_query_len), _dev_ptr(k_cache, "k_cache", bf), _dev_ptr(v_cache, "v_cache", bf), nb,
+        _dev_ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev_ptr(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
+        _dev_ptr(out, "out", bf), _stream(stream))
+    _check(rc, "pa_prefill")
     return out
 
 

@@ -323,6 +323,51 @@ int pa_decode_fp8(const pa_dims* dims, int num_seqs, const void* q, const void* 
                                                                                  : PA_ERR_CUDA;
 }
 
+int pa_prefill(const pa_dims* dims, int num_seqs, int num_tokens, const void* q,
+               const int32_t* q_start, int max_query_len, const void* k_cache,
+               const void* v_cache, int num_blocks, const int32_t* block_tables, int max_blocks,
+               const int32_t* context_lens, int max_context_len, float scale, void* out,
+               void* stream) {
+  if (const int rc = check_dims(dims)) return rc;
+  if (num_seqs < 0 || num_tokens < 0) return PA_ERR_RANGE;
+  if (num_seqs == 0 || num_tokens == 0) return PA_OK;
+  if (!q || !q_start || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PA_ERR_NULL;
+  if (num_blocks < 1 || max_blocks < 1 || max_context_len < 1 || max_query_len < 1) return PA_ERR_RANGE;
+  if (max_query_len > max_context_len) return PA_ERR_RANGE;
+  if (static_cast<long long>(max_context_len) > static_cast<long long>(max_blocks) * dims->block_size)
+    return PA_ERR_RANGE;
+  if (static_cast<long long>(num_blocks) * dims->num_kv_heads * dims->block_size > (1ll << 31))
+    return PA_ERR_RANGE;
+  if (static_cast<long long>(num_seqs) * dims->num_kv_heads > 65535) return PA_ERR_RANGE;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return PA_ERR_RANGE;
+  const void* ptrs[] = {q, q_start, k_cache, v_cache, block_tables, context_lens, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return PA_ERR_ALIGN;
+  unsigned* status = nullptr;
+  if (const int rc = status_word(&status)) return rc;
+  pa::PrefillArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  a.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  a.q_start = q_start;
+  a.context_lens = context_lens;
+  a.block_tables = block_tables;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.num_seqs = num_seqs;
+  a.num_tokens = num_tokens;
+  a.num_q_heads = dims->num_q_heads;
+  a.num_kv_heads = dims->num_kv_heads;
+  a.num_blocks = num_blocks;
+  a.max_blocks = max_blocks;
+  a.max_query_len = max_query_len;
+  a.max_context_len = max_context_len;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status;
+  return pa::launch_prefill(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                                   : PA_ERR_CUDA;
+}
+
 int pa_copy_blocks(const pa_dims* dims, int num_caches, const void* const* src_caches,
                    int64_t src_num_blocks, void* const* dst_caches, int64_t dst_num_blocks,
                    const int64_t* block_pairs, int num_pairs, void* stream) {

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -84,7 +85,28 @@ struct BlockCopyArgs {
   unsigned* status;
 };
 
+// Paged (chunked) prefill: q [num_tokens][Hq][128], sequence s owns rows
+// q_start[s] .. q_start[s+1] - 1, query i of s at position context_lens[s] - n_s + i.
+struct PrefillArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_cache;     // [num_blocks][Hkv][16][128]
+  const __nv_bfloat16* v_cache;
+  const int32_t* q_start;           // [S + 1]
+  const int32_t* context_lens;      // [S]
+  const int32_t* block_tables;      // [S][max_blocks]
+  __nv_bfloat16* out;               // [num_tokens][Hq][128]
+  int num_seqs, num_tokens, num_q_heads, num_kv_heads, num_blocks, max_blocks;
+  int max_query_len, max_context_len;
+  float scale_log2;
+  unsigned* status;
+};
+
+// TMA tensor map of a paged cache viewed as [num_blocks * Hkv * 16][128] (bf16 boxes of 64 x 16,
+// or E4M3 boxes of 128 x 16), 128-byte swizzle; encoded once per (address, rows, type).
+bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* out);
+
 cudaError_t launch_rope_kv_store(const RopeArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const BlockCopyArgs& a, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);

@@ -768,44 +768,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Tensor map of one cache viewed as a 2-D array [num_blocks * Hkv * 16 rows][128 cols] with
-// 128-byte swizzle: bf16 in boxes of 64 cols x 16 rows (two per tile), E4M3 bytes in boxes of
-// 128 cols x 16 rows (one per tile).  Encoded maps are cached by (address, rows, type).
-bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* out) {
-  struct Entry {
-    const void* ptr;
-    long long rows;
-    bool fp8;
-    CUtensorMap map;
-  };
-  static std::mutex mu;
-  static Entry table[16];
-  static int used = 0, next = 0;
-  std::lock_guard<std::mutex> lock(mu);
-  for (int i = 0; i < used; ++i)
-    if (table[i].ptr == cache && table[i].rows == rows && table[i].fp8 == fp8) {
-      *out = table[i].map;
-      return true;
-    }
-  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-  if (!encode) return false;
-  CUtensorMap m;
-  const cuuint64_t elem = fp8 ? 1 : 2;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * elem};
-  cuuint32_t box[2] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(kBlockSize)};
-  cuuint32_t estr[2] = {1, 1};
-  if (encode(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-             const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return false;
-  const int slot = used < 16 ? used++ : (next++ & 15);
-  table[slot] = Entry{cache, rows, fp8, m};
-  *out = m;
-  return true;
-}
-
 // Persistent grid size for this device: SMs x resident CTAs per SM, capped so that the grid
 // has at most kMaxDecodeWarps warps (looked up once per device and kernel variant, at the
 // largest shared-memory footprint the kernel can ask for).
@@ -859,6 +821,44 @@ cudaError_t launch_partition(DecodeArgs& a, const CUtensorMap& tm_k, const CUten
 }
 
 }  // namespace
+
+// Tensor map of one cache viewed as a 2-D array [num_blocks * Hkv * 16 rows][128 cols] with
+// 128-byte swizzle: bf16 in boxes of 64 cols x 16 rows (two per tile), E4M3 bytes in boxes of
+// 128 cols x 16 rows (one per tile).  Encoded maps are cached by (address, rows, type).
+bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* out) {
+  struct Entry {
+    const void* ptr;
+    long long rows;
+    bool fp8;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry table[16];
+  static int used = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (table[i].ptr == cache && table[i].rows == rows && table[i].fp8 == fp8) {
+      *out = table[i].map;
+      return true;
+    }
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return false;
+  CUtensorMap m;
+  const cuuint64_t elem = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * elem};
+  cuuint32_t box[2] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(kBlockSize)};
+  cuuint32_t estr[2] = {1, 1};
+  if (encode(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const int slot = used < 16 ? used++ : (next++ & 15);
+  table[slot] = Entry{cache, rows, fp8, m};
+  *out = m;
+  return true;
+}
 
 cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
   DecodeArgs a = args;

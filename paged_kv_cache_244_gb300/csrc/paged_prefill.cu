@@ -1,0 +1,305 @@
+// Paged (chunked) prefill attention for sm_103a.
+//
+// "Pico-vLLM：从零手写的工业级LLM推理引擎实现", §2 Kernel层 (PagedAttention prefill kernel, after
+// the FlashAttention work); "从零实现 LLM 推理引擎：深挖 vLLM 的六大核心优化", §3.1 (16-token blocks,
+// block tables) and §3.3 Chunked Prefill (a prompt prefilled in chunks, each continuing from
+// the tokens already in the cache).
+//
+// Sequence s brings n_s = q_start[s+1] - q_start[s] new query tokens whose K and V are already
+// in the paged cache; context_lens[s] counts every cached token including them.  Query i sits
+// at position p_i = context_lens[s] - n_s + i and attends causally to cached tokens 0..p_i.
+//
+// CTA = (sequence, KV head g, tile of 16 query tokens), one warp per query head of the group
+// (G <= 8 warps), so every K/V tile brought in is used by all G heads.  Each warp holds its
+// 16 x 128 Q tile as MMA A fragments and walks the key blocks 0 .. p_last / 16:
+//   S (16 x 16) = Q K^T      16 mma.sync m16n8k16 (bf16 -> fp32), B = K via ldmatrix
+//   online softmax           per row, in the log2 domain; causal mask t > p_i; V rows past
+//                            the context zeroed in the operand (they may hold anything)
+//   O (16 x 128) += P V      16 MMAs; P is the S accumulators rounded to bf16 (the C layout of
+//                            two n8 tiles is the A layout of one k16 step), B = V via
+//                            transposing ldmatrix
+// Key blocks come through a 3-stage ring: thread 0 issues the TMA tensor loads of block b + 3
+// (two 64-column halves each of the K and V tile, 128-byte swizzle) once every warp has
+// released block b (an mbarrier with one arrival per warp).  All waits are bounded.
+// Tiles are scheduled latest first: the last tiles of a sequence see the most keys.
+
+#include <mutex>
+
+#include <cuda.h>
+
+#include "pa_device.cuh"
+#include "pa_launch.h"
+
+namespace pa {
+namespace {
+
+constexpr int kQTile = 16;                          // query tokens per CTA
+constexpr int kPfStages = 3;
+constexpr int kPfMaxWarps = 8;                      // G <= 8
+constexpr int kPfHalf = kBlockSize * 128;           // 16 rows x 64 bf16
+constexpr int kPfStageBytes = 2 * kTileBytes;       // K tile + V tile
+constexpr int kPfQBytes = kQTile * kHeadDim * 2;    // one warp's Q tile: 4 KiB
+// header: full[3], empty[3] mbarriers, block-present flags; then 1024-aligned stages, Q tiles
+constexpr int kPfHeader = 1024;
+constexpr int kPfSmem = kPfHeader + kPfStages * kPfStageBytes + kPfMaxWarps * kPfQBytes + 1024;
+
+__global__ void __launch_bounds__(kPfMaxWarps * 32)
+prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+               const PrefillArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int Hkv = a.num_kv_heads;
+  const int G = a.num_q_heads / Hkv;
+  const int s = blockIdx.y / Hkv;
+  const int g = blockIdx.y - s * Hkv;
+  const int tile = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // latest first
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+
+  // ---- the tile's queries and keys (uniform over the CTA) --------------------------------
+  const int q0 = a.q_start[s];
+  const int n = a.q_start[s + 1] - q0;
+  const int ctx = a.context_lens[s];
+  if (q0 < 0 || n < 0 || q0 + n > a.num_tokens || n > a.max_query_len || ctx < n ||
+      ctx > a.max_context_len) {
+    if (threadIdx.x == 0 && tile == 0 && g == 0) raise_flag(a.status, PA_FLAG_CONTEXT_LEN_OOB);
+    return;
+  }
+  const int i0 = tile * kQTile;
+  if (i0 >= n) return;
+  const int rows = min(kQTile, n - i0);
+  const int pos0 = ctx - n + i0;                    // position of the tile's first query
+  const int nblocks = (pos0 + rows - 1) / kBlockSize + 1;
+
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t full = raw;                        // kPfStages x 8 bytes
+  const uint32_t empty = raw + 8 * kPfStages;
+  int* present = reinterpret_cast<int*>(smem_raw + 16 * kPfStages);
+  const uint32_t stages = (raw + kPfHeader + 1023u) & ~1023u;
+  const uint32_t qtiles = stages + kPfStages * kPfStageBytes;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPfStages; ++i) {
+      mbar_init(full + 8 * i, 1);
+      mbar_init(empty + 8 * i, static_cast<uint32_t>(G));
+    }
+    fence_mbar_init();
+    prefetch_tensor_map(&tm_k);
+    prefetch_tensor_map(&tm_v);
+  }
+  __syncthreads();
+
+  // Thread 0 brings key block b into stage b % kPfStages.
+  const int32_t* bt_row = a.block_tables + static_cast<size_t>(s) * a.max_blocks;
+  auto issue = [&](int b) {
+    const int st = b % kPfStages;
+    const int blk = bt_row[b];
+    const bool ok = blk >= 0 && blk < a.num_blocks;
+    present[st] = ok ? 1 : 0;
+    const uint32_t bar = full + 8 * st;
+    const uint32_t dst = stages + st * kPfStageBytes;
+    fence_proxy_async_smem();
+    if (ok) {
+      mbar_arrive_expect_tx(bar, kPfStageBytes);
+      const int y = (blk * Hkv + g) * kBlockSize;
+      tma_load_2d(dst, &tm_k, 0, y, bar);
+      tma_load_2d(dst + kPfHalf, &tm_k, 64, y, bar);
+      tma_load_2d(dst + 2 * kPfHalf, &tm_v, 0, y, bar);
+      tma_load_2d(dst + 3 * kPfHalf, &tm_v, 64, y, bar);
+    } else {
+      raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
+      mbar_arrive(bar);
+    }
+  };
+  int issued = 0;
+  if (threadIdx.x == 0)
+    for (; issued < min(kPfStages, nblocks); ++issued) issue(issued);
+
+  // ---- this warp's Q tile (query head g * G + warp) as A fragments ------------------------
+  const int h = g * G + warp;
+  const int gq = lane >> 2, cq = lane & 3;          // fragment row group / column pair
+  const int mi = lane >> 3, r = lane & 7;           // ldmatrix: matrix / row this lane addresses
+  const uint32_t qs = qtiles + warp * kPfQBytes;
+  {
+    // row = query i0 + row (zero past the tile), 16 chunks of 16 bytes, chunk c at c ^ (row % 8)
+    unsigned char* qgen = smem_raw + (qs - raw);
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int idx = it * 32 + lane;
+      const int row = idx >> 4, c = idx & 15;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (row < rows)
+        v = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(q0 + i0 + row) * a.num_q_heads + h) *
+                                                     kHeadDim)[c];
+      *reinterpret_cast<uint4*>(qgen + row * 256 + ((c ^ (row & 7)) << 4)) = v;
+    }
+  }
+  __syncwarp();
+  uint32_t qa[8][4];
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const int row = r + 8 * (mi & 1);
+    const int c = 2 * kk + (mi >> 1);
+    ldsm_x4(qs + row * 256 + ((c ^ r) << 4), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+  }
+
+  float o[16][4];
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows gq, gq + 8
+  const int p0 = pos0 + gq, p1 = pos0 + gq + 8;               // their positions
+  bool failed = false;
+  int seen = 0;                                               // blocks this warp waited for
+
+  for (int b = 0; b < nblocks; ++b) {
+    const int st = b % kPfStages;
+    if (!mbar_wait_bounded(full + 8 * st, (b / kPfStages) & 1)) {
+      failed = true;
+      break;
+    }
+    seen = b + 1;
+    const uint32_t kt = stages + st * kPfStageBytes;
+    const uint32_t vt = kt + 2 * kPfHalf;
+    if (present[st]) {
+      // S = Q K^T for keys 16b .. 16b + 15 (two n8 tiles)
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t b0, b1, b2, b3;
+        const int key = r + 8 * (mi >> 1);
+        const int chunk = (2 * kk + (mi & 1)) & 7;
+        ldsm_x4(kt + (kk >> 2) * kPfHalf + key * 128 + ((chunk ^ r) << 4), b0, b1, b2, b3);
+        mma_bf16_16816(sc[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+        mma_bf16_16816(sc[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+      }
+      // scale, causal mask; sc[nt]: [0] (row gq, key 8nt+2cq), [1] (gq, +1), [2] (gq+8, ..), [3]
+      const int t0 = kBlockSize * b + 2 * cq;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int t = t0 + 8 * nt + j;
+          sc[nt][j] = t <= p0 ? sc[nt][j] * a.scale_log2 : -INFINITY;
+          sc[nt][2 + j] = t <= p1 ? sc[nt][2 + j] * a.scale_log2 : -INFINITY;
+        }
+      float bm0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+      float bm1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+#pragma unroll
+      for (int x = 1; x < 4; x <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(kFullMask, bm0, x));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(kFullMask, bm1, x));
+      }
+      const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+      // a row with no key yet keeps the shift 0 (only rows past the tile can stay that way)
+      const float sh0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float sh1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = exp2f(m0 - sh0), al1 = exp2f(m1 - sh1);
+      m0 = mn0;
+      m1 = mn1;
+      // P rounded to bf16 (the MMA operand); the running sums add the same rounded values
+      const uint32_t pa0 = pack_bf16x2(exp2f(sc[0][0] - sh0), exp2f(sc[0][1] - sh0));
+      const uint32_t pa1 = pack_bf16x2(exp2f(sc[0][2] - sh1), exp2f(sc[0][3] - sh1));
+      const uint32_t pa2 = pack_bf16x2(exp2f(sc[1][0] - sh0), exp2f(sc[1][1] - sh0));
+      const uint32_t pa3 = pack_bf16x2(exp2f(sc[1][2] - sh1), exp2f(sc[1][3] - sh1));
+      l0 = fmaf(l0, al0, bf16lo(pa0) + bf16hi(pa0) + bf16lo(pa2) + bf16hi(pa2));
+      l1 = fmaf(l1, al1, bf16lo(pa1) + bf16hi(pa1) + bf16lo(pa3) + bf16hi(pa3));
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        o[nt][0] *= al0;
+        o[nt][1] *= al0;
+        o[nt][2] *= al1;
+        o[nt][3] *= al1;
+      }
+      // keys past the context may hold anything (even NaN): zero their V rows in the operand
+      const int valid = ctx - kBlockSize * b;
+      uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+      if (valid < kBlockSize) {
+        vm_lo = (2 * cq < valid ? 0x0000ffffu : 0u) | (2 * cq + 1 < valid ? 0xffff0000u : 0u);
+        vm_hi = (2 * cq + 8 < valid ? 0x0000ffffu : 0u) | (2 * cq + 9 < valid ? 0xffff0000u : 0u);
+      }
+      // O += P V, two n8 dim tiles per transposing ldmatrix
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t v0, v1, v2, v3;
+        const int key = r + 8 * (mi & 1);
+        const int chunk = (2 * j + (mi >> 1)) & 7;
+        ldsm_x4_trans(vt + (j >> 2) * kPfHalf + key * 128 + ((chunk ^ r) << 4), v0, v1, v2, v3);
+        mma_bf16_16816(o[2 * j], pa0, pa1, pa2, pa3, v0 & vm_lo, v1 & vm_hi);
+        mma_bf16_16816(o[2 * j + 1], pa0, pa1, pa2, pa3, v2 & vm_lo, v3 & vm_hi);
+      }
+    }
+    // release the stage; thread 0 refills it once every warp has
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + 8 * st);
+    if (threadIdx.x == 0 && issued < nblocks) {
+      if (!mbar_wait_bounded(empty + 8 * st, (b / kPfStages) & 1)) {
+        failed = true;
+        break;
+      }
+      issue(issued++);
+    }
+    __syncwarp();
+  }
+  if (failed && lane == 0) raise_flag(a.status, PA_FLAG_TIMEOUT);
+  // Let every copy thread 0 issued land (bounded) before the CTA can exit.
+  if (threadIdx.x == 0)
+    for (int j = seen; j < issued; ++j) mbar_wait_bounded(full + 8 * (j % kPfStages), (j / kPfStages) & 1);
+  if (failed) return;
+
+  // ---- out = O / l for the tile's real rows -----------------------------------------------
+  float L0 = l0, L1 = l1;
+#pragma unroll
+  for (int x = 1; x < 4; x <<= 1) {
+    L0 += __shfl_xor_sync(kFullMask, L0, x);
+    L1 += __shfl_xor_sync(kFullMask, L1, x);
+  }
+  const float i0f = 1.f / L0, i1f = 1.f / L1;
+  uint32_t* out0 = reinterpret_cast<uint32_t*>(
+      a.out + (static_cast<size_t>(q0 + i0 + gq) * a.num_q_heads + h) * kHeadDim);
+  uint32_t* out1 = reinterpret_cast<uint32_t*>(
+      a.out + (static_cast<size_t>(q0 + i0 + gq + 8) * a.num_q_heads + h) * kHeadDim);
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) {
+    if (gq < rows) out0[4 * nt + cq] = pack_bf16x2(o[nt][0] * i0f, o[nt][1] * i0f);
+    if (gq + 8 < rows) out1[4 * nt + cq] = pack_bf16x2(o[nt][2] * i1f, o[nt][3] * i1f);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  const int G = a.num_q_heads / a.num_kv_heads;
+  if (G < 1 || G > kPfMaxWarps) return cudaErrorInvalidValue;
+  const long long rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * kBlockSize;
+  CUtensorMap tm_k, tm_v;
+  if (!cache_tensor_map(a.k_cache, rows, false, &tm_k) || !cache_tensor_map(a.v_cache, rows, false, &tm_v))
+    return cudaErrorInvalidValue;
+  {  // opt in to the shared-memory size once per device
+    static std::mutex mu;
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+      err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+      if (err != cudaSuccess) return err;
+      done[dev] = true;
+    }
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((a.max_query_len + kQTile - 1) / kQTile),
+                     static_cast<unsigned>(a.num_seqs * a.num_kv_heads));
+  cfg.blockDim = dim3(static_cast<unsigned>(G * 32));
+  cfg.dynamicSmemBytes = kPfSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_kernel, tm_k, tm_v, a);
+}
+
+}  // namespace pa

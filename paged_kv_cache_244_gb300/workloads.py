@@ -284,6 +284,111 @@ def make(name: str, seed: int | None = None) -> Workload:
     raise KeyError(name)
 
 
+@dataclass
+class PrefillWorkload:
+    """One layer's inputs of a paged (chunked) prefill: sequence s brings q_lens[s] new tokens
+    at the end of its context_lens[s] cached tokens, all of which are in the cache."""
+
+    name: str
+    context_lens: np.ndarray            # int32 [S], cached tokens including the new ones
+    q_start: np.ndarray                 # int32 [S + 1], rows of q per sequence
+    block_tables: np.ndarray            # int32 [S, max_blocks]; unused entries -1
+    num_blocks: int
+    q: np.ndarray                       # uint16 [T, Hq, D], already rotated
+    k_cache: np.ndarray                 # uint16 [num_blocks, Hkv, B, D]
+    v_cache: np.ndarray
+    seed: int = 0
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.context_lens.shape[0])
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.q_start[-1])
+
+    @property
+    def q_lens(self) -> np.ndarray:
+        return np.diff(self.q_start).astype(np.int32)
+
+    @property
+    def max_query_len(self) -> int:
+        return int(self.q_lens.max()) if self.num_seqs else 0
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.num_seqs else 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(HEAD_DIM))
+
+    def attention_flops(self) -> int:
+        """Multiply-adds x 2 of q.K and p.V over the causal pairs: query i of s sees
+        context_lens[s] - n_s + i + 1 keys; 4 * Hq * D flops per (query, key) pair."""
+        total = 0
+        Hq = int(self.q.shape[1])
+        for ctx, n in zip(self.context_lens.astype(np.int64), self.q_lens.astype(np.int64)):
+            first = ctx - n + 1                          # keys seen by the first new query
+            total += n * first + n * (n - 1) // 2
+        return int(total) * 4 * Hq * HEAD_DIM
+
+
+def build_prefill(name: str, context_lens, q_lens, num_blocks: int, seed: int, *,
+                  sigma: float = 1.0, num_q_heads: int = NUM_Q_HEADS,
+                  num_kv_heads: int = NUM_KV_HEADS, canary: int = BF16_NAN) -> PrefillWorkload:
+    """Seeded prefill inputs: blocks from one shuffle of the pool, every cached token N(0, sigma)
+    in bf16, every other slot the canary, q N(0, sigma) for the new tokens."""
+    rng = SplitMix64(seed)
+    ctx = np.asarray(context_lens, np.int32)
+    ql = np.asarray(q_lens, np.int32)
+    assert ctx.shape == ql.shape and (ql <= ctx).all() and (ql >= 0).all()
+    S = ctx.shape[0]
+    nblk = (ctx.astype(np.int64) + BLOCK_SIZE - 1) // BLOCK_SIZE
+    maxb = max(int(nblk.max()) if S else 1, 1)
+    assert int(nblk.sum()) <= num_blocks, "pool too small"
+    pool = rng.permutation(num_blocks)
+    bt = np.full((S, maxb), -1, np.int32)
+    cur = 0
+    for s_ in range(S):
+        bt[s_, :nblk[s_]] = pool[cur:cur + nblk[s_]]
+        cur += int(nblk[s_])
+    shape = (num_blocks, num_kv_heads, BLOCK_SIZE, HEAD_DIM)
+    kc = np.full(shape, canary, np.uint16)
+    vc = np.full(shape, canary, np.uint16)
+    tile = num_kv_heads * BLOCK_SIZE * HEAD_DIM
+    for cache in (kc, vc):
+        for s_ in range(S):
+            ids = bt[s_, :nblk[s_]].astype(np.int64)
+            if ids.shape[0] == 0:
+                continue
+            cache[ids] = rng.normal_bf16(ids.shape[0] * tile, sigma).reshape(ids.shape[0], num_kv_heads,
+                                                                             BLOCK_SIZE, HEAD_DIM)
+            tail = int(ctx[s_]) - (int(nblk[s_]) - 1) * BLOCK_SIZE   # valid slots in the last block
+            cache[int(bt[s_, nblk[s_] - 1]), :, tail:, :] = canary
+    qs = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    T = int(qs[-1])
+    q = rng.normal_bf16(T * num_q_heads * HEAD_DIM, sigma).reshape(T, num_q_heads, HEAD_DIM)
+    return PrefillWorkload(name=name, context_lens=ctx, q_start=qs, block_tables=bt,
+                           num_blocks=num_blocks, q=q, k_cache=kc, v_cache=vc, seed=seed)
+
+
+PREFILL_WORKLOADS = ("prefill4x2048", "chunked16")
+
+
+def make_prefill(name: str, seed: int | None = None) -> PrefillWorkload:
+    """Named prefill workloads: prefill4x2048 = 4 prompts of 2048 tokens prefilled whole;
+    chunked16 = 16 sequences each adding a 256-token chunk to 1792 prefilled tokens."""
+    idx = PREFILL_WORKLOADS.index(name)
+    if seed is None:
+        seed = 0x2440 + idx
+    if name == "prefill4x2048":
+        return build_prefill(name, [2048] * 4, [2048] * 4, 4 * 128 + 64, seed)
+    if name == "chunked16":
+        return build_prefill(name, [2048] * 16, [256] * 16, 16 * 128 + 64, seed)
+    raise KeyError(name)
+
+
 def shard(w: Workload, rank: int, world: int) -> Workload:
     """Rank `rank`'s share of a workload's sequences (contiguous split; caches shared)."""
     S = w.num_seqs

@@ -32,7 +32,8 @@ def test_header_declares_the_entry_points():
     for must in ("pa_rope_kv_store", "pa_decode", "pa_decode_workspace_size",
                  "pa_decode_partition_tokens", "pa_get_device_status", "pa_status_string",
                  "pa_selftest_wait_timeout", "pa_decode_static_workspace", "pa_decode_step",
-                 "pa_copy_blocks", "pa_rope_kv_store_fp8", "pa_decode_fp8", "pa_decode_step_fp8"):
+                 "pa_copy_blocks", "pa_rope_kv_store_fp8", "pa_decode_fp8", "pa_decode_step_fp8",
+                 "pa_prefill"):
         assert must in names
 
 
@@ -167,6 +168,29 @@ def test_fp8_entry_points_reject_bad_arguments_on_the_host(L):
     assert step(S=0) == b.PA_OK
     assert step(ks=None) == b.PA_ERR_NULL and step(vs=MIS_PTR) == b.PA_ERR_ALIGN
     assert step(k=None) == b.PA_ERR_NULL
+
+
+def test_prefill_rejects_bad_arguments_on_the_host(L):
+    from paged_kv_cache_244_gb300 import binding as b
+
+    def call(d=None, S=2, T=40, maxq=32, maxctx=64, maxb=4, scale=0.088, **ptrs):
+        a = dict(q=OK_PTR, qs=OK_PTR, kc=OK_PTR, vc=OK_PTR, bt=OK_PTR, ctx=OK_PTR, out=OK_PTR)
+        a.update(ptrs)
+        d = dims() if d is None else d
+        return L.pa_prefill(ctypes.byref(d), S, T, a["q"], a["qs"], maxq, a["kc"], a["vc"], 16,
+                            a["bt"], maxb, a["ctx"], maxctx, scale, a["out"], None)
+
+    assert call(d=dims(d=64)) == b.PA_ERR_SHAPE
+    assert call(S=-1) == b.PA_ERR_RANGE and call(T=-1) == b.PA_ERR_RANGE
+    assert call(S=0) == b.PA_OK and call(T=0) == b.PA_OK
+    for kw in ("q", "qs", "kc", "vc", "bt", "ctx", "out"):
+        assert call(**{kw: None}) == b.PA_ERR_NULL, kw
+        assert call(**{kw: MIS_PTR}) == b.PA_ERR_ALIGN, kw
+    assert call(maxq=0) == b.PA_ERR_RANGE
+    assert call(maxq=65) == b.PA_ERR_RANGE                  # above max_context_len
+    assert call(maxctx=65) == b.PA_ERR_RANGE                # above max_blocks * 16
+    assert call(S=40000) == b.PA_ERR_RANGE                  # S * Hkv > 65535
+    assert call(scale=0.0) == b.PA_ERR_RANGE
 
 
 def test_rope_kv_store_rejects_bad_arguments_on_the_host(L):
