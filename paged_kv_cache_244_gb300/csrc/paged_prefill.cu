@@ -12,15 +12,16 @@
 // CTA = (sequence, KV head g, tile of 16 query tokens), one warp per query head of the group
 // (G <= 8 warps), so every K/V tile brought in is used by all G heads.  Each warp holds its
 // 16 x 128 Q tile as MMA A fragments and walks the key blocks 0 .. p_last / 16:
-//   S (16 x 16) = Q K^T      16 mma.sync m16n8k16 (bf16 -> fp32), B = K via ldmatrix
+//   S (16 x 64) = Q K^T      64 mma.sync m16n8k16 (bf16 -> fp32), B = K via ldmatrix
 //   online softmax           per row, in the log2 domain; causal mask t > p_i; V rows past
 //                            the context zeroed in the operand (they may hold anything)
-//   O (16 x 128) += P V      16 MMAs; P is the S accumulators rounded to bf16 (the C layout of
+//   O (16 x 128) += P V      64 MMAs; P is the S accumulators rounded to bf16 (the C layout of
 //                            two n8 tiles is the A layout of one k16 step), B = V via
 //                            transposing ldmatrix
-// Key blocks come through a 3-stage ring: thread 0 issues the TMA tensor loads of block b + 3
-// (two 64-column halves each of the K and V tile, 128-byte swizzle) once every warp has
-// released block b (an mbarrier with one arrival per warp).  All waits are bounded.
+// Keys come 64 at a time (4 blocks) through a 2-stage ring, so the softmax bookkeeping and the
+// barrier handshakes are paid once per 128 MMAs: thread 0 issues the TMA tensor loads of stage
+// j + 2 (two 64-column halves each of every K and V tile, 128-byte swizzle) once every warp has
+// released stage j (an mbarrier with one arrival per warp).  All waits are bounded.
 // Tiles are scheduled latest first: the last tiles of a sequence see the most keys.
 
 #include <mutex>
@@ -34,16 +35,18 @@ namespace pa {
 namespace {
 
 constexpr int kQTile = 16;                          // query tokens per CTA
-constexpr int kPfStages = 3;
+constexpr int kKB = 4;                              // key blocks (16 tokens each) per stage
+constexpr int kPfStages = 2;
 constexpr int kPfMaxWarps = 8;                      // G <= 8
 constexpr int kPfHalf = kBlockSize * 128;           // 16 rows x 64 bf16
-constexpr int kPfStageBytes = 2 * kTileBytes;       // K tile + V tile
+constexpr int kPfBlockBytes = 2 * kTileBytes;       // K tile + V tile of one key block
+constexpr int kPfStageBytes = kKB * kPfBlockBytes;  // 32 KiB
 constexpr int kPfQBytes = kQTile * kHeadDim * 2;    // one warp's Q tile: 4 KiB
-// header: full[3], empty[3] mbarriers, block-present flags; then 1024-aligned stages, Q tiles
+// header: full[2], empty[2] mbarriers, block-present masks; then 1024-aligned stages, Q tiles
 constexpr int kPfHeader = 1024;
 constexpr int kPfSmem = kPfHeader + kPfStages * kPfStageBytes + kPfMaxWarps * kPfQBytes + 1024;
 
-__global__ void __launch_bounds__(kPfMaxWarps * 32)
+__global__ void __maxnreg__(168)  // two CTAs of up to 6 warps per SM; 8 warps still fit one
 prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const PrefillArgs a) {
   extern __shared__ unsigned char smem_raw[];
@@ -71,11 +74,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const int rows = min(kQTile, n - i0);
   const int pos0 = ctx - n + i0;                    // position of the tile's first query
   const int nblocks = (pos0 + rows - 1) / kBlockSize + 1;
+  const int nst = (nblocks + kKB - 1) / kKB;        // stages of kKB key blocks
 
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t full = raw;                        // kPfStages x 8 bytes
   const uint32_t empty = raw + 8 * kPfStages;
-  int* present = reinterpret_cast<int*>(smem_raw + 16 * kPfStages);
+  int* present = reinterpret_cast<int*>(smem_raw + 16 * kPfStages);  // bit i: block i loaded
   const uint32_t stages = (raw + kPfHeader + 1023u) & ~1023u;
   const uint32_t qtiles = stages + kPfStages * kPfStageBytes;
   if (threadIdx.x == 0) {
@@ -89,31 +93,42 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   }
   __syncthreads();
 
-  // Thread 0 brings key block b into stage b % kPfStages.
+  // Thread 0 brings key blocks kKB j .. kKB j + kKB - 1 into stage j % kPfStages.
   const int32_t* bt_row = a.block_tables + static_cast<size_t>(s) * a.max_blocks;
-  auto issue = [&](int b) {
-    const int st = b % kPfStages;
-    const int blk = bt_row[b];
-    const bool ok = blk >= 0 && blk < a.num_blocks;
-    present[st] = ok ? 1 : 0;
+  auto issue = [&](int j) {
+    const int st = j % kPfStages;
+    int blk[kKB];
+    int mask = 0;
+#pragma unroll
+    for (int i = 0; i < kKB; ++i) {
+      const int b = kKB * j + i;
+      blk[i] = b < nblocks ? bt_row[b] : -1;
+      if (b < nblocks && blk[i] >= 0 && blk[i] < a.num_blocks) mask |= 1 << i;
+      else if (b < nblocks) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
+    }
+    present[st] = mask;
     const uint32_t bar = full + 8 * st;
     const uint32_t dst = stages + st * kPfStageBytes;
     fence_proxy_async_smem();
-    if (ok) {
-      mbar_arrive_expect_tx(bar, kPfStageBytes);
-      const int y = (blk * Hkv + g) * kBlockSize;
-      tma_load_2d(dst, &tm_k, 0, y, bar);
-      tma_load_2d(dst + kPfHalf, &tm_k, 64, y, bar);
-      tma_load_2d(dst + 2 * kPfHalf, &tm_v, 0, y, bar);
-      tma_load_2d(dst + 3 * kPfHalf, &tm_v, 64, y, bar);
+    if (mask) {
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask)) * kPfBlockBytes);
+#pragma unroll
+      for (int i = 0; i < kKB; ++i) {
+        if (!(mask & (1 << i))) continue;
+        const int y = (blk[i] * Hkv + g) * kBlockSize;
+        const uint32_t d = dst + i * kPfBlockBytes;
+        tma_load_2d(d, &tm_k, 0, y, bar);
+        tma_load_2d(d + kPfHalf, &tm_k, 64, y, bar);
+        tma_load_2d(d + 2 * kPfHalf, &tm_v, 0, y, bar);
+        tma_load_2d(d + 3 * kPfHalf, &tm_v, 64, y, bar);
+      }
     } else {
-      raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
       mbar_arrive(bar);
     }
   };
   int issued = 0;
   if (threadIdx.x == 0)
-    for (; issued < min(kPfStages, nblocks); ++issued) issue(issued);
+    for (; issued < min(kPfStages, nst); ++issued) issue(issued);
 
   // ---- this warp's Q tile (query head g * G + warp) as A fragments ------------------------
   const int h = g * G + warp;
@@ -149,60 +164,82 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows gq, gq + 8
   const int p0 = pos0 + gq, p1 = pos0 + gq + 8;               // their positions
   bool failed = false;
-  int seen = 0;                                               // blocks this warp waited for
+  int seen = 0;                                               // stages this warp waited for
 
-  for (int b = 0; b < nblocks; ++b) {
-    const int st = b % kPfStages;
-    if (!mbar_wait_bounded(full + 8 * st, (b / kPfStages) & 1)) {
+  for (int j = 0; j < nst; ++j) {
+    const int st = j % kPfStages;
+    if (!mbar_wait_bounded(full + 8 * st, (j / kPfStages) & 1)) {
       failed = true;
       break;
     }
-    seen = b + 1;
-    const uint32_t kt = stages + st * kPfStageBytes;
-    const uint32_t vt = kt + 2 * kPfHalf;
-    if (present[st]) {
-      // S = Q K^T for keys 16b .. 16b + 15 (two n8 tiles)
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    seen = j + 1;
+    const int mask = present[st];
+    const uint32_t stage = stages + st * kPfStageBytes;
+    // S = Q K^T for the stage's 64 keys: n8 tile 2i (+1) = keys 0-7 (8-15) of block i
+    float sc[2 * kKB][4];
+#pragma unroll
+    for (int nt = 0; nt < 2 * kKB; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kKB; ++i) {
+      if (!(mask & (1 << i))) continue;
+      const uint32_t kt = stage + i * kPfBlockBytes;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         uint32_t b0, b1, b2, b3;
         const int key = r + 8 * (mi >> 1);
         const int chunk = (2 * kk + (mi & 1)) & 7;
         ldsm_x4(kt + (kk >> 2) * kPfHalf + key * 128 + ((chunk ^ r) << 4), b0, b1, b2, b3);
-        mma_bf16_16816(sc[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-        mma_bf16_16816(sc[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+        mma_bf16_16816(sc[2 * i], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+        mma_bf16_16816(sc[2 * i + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
       }
-      // scale, causal mask; sc[nt]: [0] (row gq, key 8nt+2cq), [1] (gq, +1), [2] (gq+8, ..), [3]
-      const int t0 = kBlockSize * b + 2 * cq;
+    }
+    // scale; causal mask and missing blocks -> -inf.  sc[nt]: [0] (row gq, key 8nt+2cq),
+    // [1] (gq, +1), [2] (gq+8, 8nt+2cq), [3] (gq+8, +1)
+    const int tbase = kKB * kBlockSize * j + 2 * cq;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < 2 * kKB; ++nt) {
+      const bool here = (mask >> (nt >> 1)) & 1;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int t = t0 + 8 * nt + j;
-          sc[nt][j] = t <= p0 ? sc[nt][j] * a.scale_log2 : -INFINITY;
-          sc[nt][2 + j] = t <= p1 ? sc[nt][2 + j] * a.scale_log2 : -INFINITY;
-        }
-      float bm0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-      float bm1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-#pragma unroll
-      for (int x = 1; x < 4; x <<= 1) {
-        bm0 = fmaxf(bm0, __shfl_xor_sync(kFullMask, bm0, x));
-        bm1 = fmaxf(bm1, __shfl_xor_sync(kFullMask, bm1, x));
+      for (int e = 0; e < 2; ++e) {
+        const int t = tbase + 8 * nt + e;
+        sc[nt][e] = here && t <= p0 ? sc[nt][e] * a.scale_log2 : -INFINITY;
+        sc[nt][2 + e] = here && t <= p1 ? sc[nt][2 + e] * a.scale_log2 : -INFINITY;
       }
-      const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-      // a row with no key yet keeps the shift 0 (only rows past the tile can stay that way)
-      const float sh0 = mn0 == -INFINITY ? 0.f : mn0;
-      const float sh1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = exp2f(m0 - sh0), al1 = exp2f(m1 - sh1);
-      m0 = mn0;
-      m1 = mn1;
-      // P rounded to bf16 (the MMA operand); the running sums add the same rounded values
-      const uint32_t pa0 = pack_bf16x2(exp2f(sc[0][0] - sh0), exp2f(sc[0][1] - sh0));
-      const uint32_t pa1 = pack_bf16x2(exp2f(sc[0][2] - sh1), exp2f(sc[0][3] - sh1));
-      const uint32_t pa2 = pack_bf16x2(exp2f(sc[1][0] - sh0), exp2f(sc[1][1] - sh0));
-      const uint32_t pa3 = pack_bf16x2(exp2f(sc[1][2] - sh1), exp2f(sc[1][3] - sh1));
-      l0 = fmaf(l0, al0, bf16lo(pa0) + bf16hi(pa0) + bf16lo(pa2) + bf16hi(pa2));
-      l1 = fmaf(l1, al1, bf16lo(pa1) + bf16hi(pa1) + bf16lo(pa3) + bf16hi(pa3));
+    }
+    float bm0 = -INFINITY, bm1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2 * kKB; ++nt) {
+      bm0 = fmaxf(bm0, fmaxf(sc[nt][0], sc[nt][1]));
+      bm1 = fmaxf(bm1, fmaxf(sc[nt][2], sc[nt][3]));
+    }
+#pragma unroll
+    for (int x = 1; x < 4; x <<= 1) {
+      bm0 = fmaxf(bm0, __shfl_xor_sync(kFullMask, bm0, x));
+      bm1 = fmaxf(bm1, __shfl_xor_sync(kFullMask, bm1, x));
+    }
+    const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+    // a row with no key yet keeps the shift 0 (only rows past the tile can stay that way)
+    const float sh0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float sh1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(m0 - sh0), al1 = exp2f(m1 - sh1);
+    m0 = mn0;
+    m1 = mn1;
+    // P rounded to bf16 (the MMA operand), as A fragments of one k16 step per block; the
+    // running sums add the same rounded values
+    uint32_t pa[kKB][4];
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < kKB; ++i) {
+      pa[i][0] = pack_bf16x2(exp2f(sc[2 * i][0] - sh0), exp2f(sc[2 * i][1] - sh0));
+      pa[i][1] = pack_bf16x2(exp2f(sc[2 * i][2] - sh1), exp2f(sc[2 * i][3] - sh1));
+      pa[i][2] = pack_bf16x2(exp2f(sc[2 * i + 1][0] - sh0), exp2f(sc[2 * i + 1][1] - sh0));
+      pa[i][3] = pack_bf16x2(exp2f(sc[2 * i + 1][2] - sh1), exp2f(sc[2 * i + 1][3] - sh1));
+      ps0 += bf16lo(pa[i][0]) + bf16hi(pa[i][0]) + bf16lo(pa[i][2]) + bf16hi(pa[i][2]);
+      ps1 += bf16lo(pa[i][1]) + bf16hi(pa[i][1]) + bf16lo(pa[i][3]) + bf16hi(pa[i][3]);
+    }
+    l0 = fmaf(l0, al0, ps0);
+    l1 = fmaf(l1, al1, ps1);
+    if (__any_sync(kFullMask, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
         o[nt][0] *= al0;
@@ -210,29 +247,34 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         o[nt][2] *= al1;
         o[nt][3] *= al1;
       }
+    }
+    // O += P V, block by block; two n8 dim tiles per transposing ldmatrix
+#pragma unroll
+    for (int i = 0; i < kKB; ++i) {
+      if (!(mask & (1 << i))) continue;
+      const uint32_t vt = stage + i * kPfBlockBytes + 2 * kPfHalf;
       // keys past the context may hold anything (even NaN): zero their V rows in the operand
-      const int valid = ctx - kBlockSize * b;
+      const int valid = ctx - kBlockSize * (kKB * j + i);
       uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
       if (valid < kBlockSize) {
         vm_lo = (2 * cq < valid ? 0x0000ffffu : 0u) | (2 * cq + 1 < valid ? 0xffff0000u : 0u);
         vm_hi = (2 * cq + 8 < valid ? 0x0000ffffu : 0u) | (2 * cq + 9 < valid ? 0xffff0000u : 0u);
       }
-      // O += P V, two n8 dim tiles per transposing ldmatrix
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int d2 = 0; d2 < 8; ++d2) {
         uint32_t v0, v1, v2, v3;
         const int key = r + 8 * (mi & 1);
-        const int chunk = (2 * j + (mi >> 1)) & 7;
-        ldsm_x4_trans(vt + (j >> 2) * kPfHalf + key * 128 + ((chunk ^ r) << 4), v0, v1, v2, v3);
-        mma_bf16_16816(o[2 * j], pa0, pa1, pa2, pa3, v0 & vm_lo, v1 & vm_hi);
-        mma_bf16_16816(o[2 * j + 1], pa0, pa1, pa2, pa3, v2 & vm_lo, v3 & vm_hi);
+        const int chunk = (2 * d2 + (mi >> 1)) & 7;
+        ldsm_x4_trans(vt + (d2 >> 2) * kPfHalf + key * 128 + ((chunk ^ r) << 4), v0, v1, v2, v3);
+        mma_bf16_16816(o[2 * d2], pa[i][0], pa[i][1], pa[i][2], pa[i][3], v0 & vm_lo, v1 & vm_hi);
+        mma_bf16_16816(o[2 * d2 + 1], pa[i][0], pa[i][1], pa[i][2], pa[i][3], v2 & vm_lo, v3 & vm_hi);
       }
     }
     // release the stage; thread 0 refills it once every warp has
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + 8 * st);
-    if (threadIdx.x == 0 && issued < nblocks) {
-      if (!mbar_wait_bounded(empty + 8 * st, (b / kPfStages) & 1)) {
+    if (threadIdx.x == 0 && issued < nst) {
+      if (!mbar_wait_bounded(empty + 8 * st, (j / kPfStages) & 1)) {
         failed = true;
         break;
       }
