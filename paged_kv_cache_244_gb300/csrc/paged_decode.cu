@@ -832,8 +832,11 @@ bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* 
     bool fp8;
     CUtensorMap map;
   };
+  // Room for the K and V caches of every layer of a large model in both element types; the
+  // oldest entry is replaced when it is full.
+  constexpr int kEntries = 512;
   static std::mutex mu;
-  static Entry table[16];
+  static Entry table[kEntries];
   static int used = 0, next = 0;
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < used; ++i)
@@ -854,7 +857,7 @@ bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* 
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
-  const int slot = used < 16 ? used++ : (next++ & 15);
+  const int slot = used < kEntries ? used++ : (next++ % kEntries);
   table[slot] = Entry{cache, rows, fp8, m};
   *out = m;
   return true;
