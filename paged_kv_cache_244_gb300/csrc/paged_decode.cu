@@ -32,11 +32,22 @@
 //              partial (sum p V, (m, l)) to slot v + i.
 // decode_merge_kernel combines the pieces of split segments:
 //   M = max_p m_p,  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
+// Ranges are dealt to the CTAs round-robin (range v to warp v / grid of CTA v % grid).
 //
 // Shared memory per stage: [K cols 0-63 | K cols 64-127 | V cols 0-63 | V cols 64-127 | q rows],
 // the four tile halves 16 rows x 128 B each, swizzled so that 16-byte chunk c of row r sits at
 // chunk c ^ (r % 8); the ldmatrix row addresses apply the same XOR, so all eight rows of a
 // matrix hit distinct banks.
+//
+// Variants (template <kStep, kFp8>):
+//   kStep  the fused decode step ("Pico-vLLM" §2: RoPE fused with the KV cache store): the warp
+//          whose job holds a sequence's new token (position len - 1) stages the token's k, v and
+//          cos/sin row with the tiles, rotates k, writes both rows into the staged tiles before
+//          the MMAs and into the cache slot; each piece rotates its q fragments in registers.
+//   kFp8   E4M3 caches with one scale per KV head: 2 KiB tiles, one 128-byte box each, four
+//          stages; the byte tiles are read by ldmatrix as 16-bit pairs and widened exactly to
+//          f16 with cvt.f16x2.e4m3x2, the q.K k index permuted alike in both operands; f16 MMAs,
+//          the K scale folded into the softmax scale, the V scale into the output.
 
 #include <cmath>
 #include <mutex>
