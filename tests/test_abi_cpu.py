@@ -37,6 +37,37 @@ def test_header_declares_the_entry_points():
         assert must in names
 
 
+def test_header_is_plain_c_and_links(L, tmp_path):
+    """include/pa.h compiles as C99 with no CUDA, C++ or framework headers, and a C program
+    using every entry point links against the library."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_pa.c"
+    calls = "\n".join(f"  (void)&{name};" for name in declared_functions())
+    src.write_text(f"""#include "pa.h"
+#include <stdio.h>
+int main(void) {{
+{calls}
+  pa_dims d = {{12, 2, 128, 16}};
+  printf("%zu %s\\n", pa_decode_workspace_size(&d, 64, 4096, 0), pa_status_string(PA_ERR_RANGE));
+  return 0;
+}}
+""")
+    exe = tmp_path / "use_pa"
+    lib = Path(L._name)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic", f"-I{ROOT / 'include'}",
+                        str(src), str(lib), f"-Wl,-rpath,{lib.parent}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    size, status = out.stdout.split(maxsplit=1)
+    assert int(size) > 0 and status.startswith("PA_ERR_RANGE")
+
+
 def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), f"{name} declared in include/ but not exported"
