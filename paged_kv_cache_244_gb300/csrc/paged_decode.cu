@@ -14,14 +14,16 @@
 // A warp serves all G <= 8 query heads of a segment's KV head, so each (block, KV head) tile of
 // K and V is read from HBM exactly once.
 //
-// Each warp is its own producer and consumer over a ring of kStages shared-memory stages that
-// runs straight through piece boundaries:
+// Each warp is its own producer and consumer over a ring of shared-memory stages that runs
+// straight through piece boundaries.  The CTA's stages are shared out evenly among its warps that
+// have work, so that with fewer ranges than warps each busy warp keeps more tiles in flight:
 //   lookahead  the lanes of the warp resolve 32 jobs at a time -- segment (binary search over
 //              the CTA's shared prefix of block counts), block id from the block table, valid
 //              tokens, first / last / whole-segment flags -- one window ahead of use;
-//   producer   per job, lane 0 writes a small descriptor and issues four TMA tensor loads (two
-//              64-column halves of the K tile and of the V tile, 128-byte swizzle) on the
-//              stage's mbarrier, plus on a piece's first block a bulk copy of the q rows;
+//   producer   per job, lane 0 writes a small descriptor and issues two TMA tensor loads (the
+//              K tile and the V tile, each one box landing as two 64-column halves, 128-byte
+//              swizzle) on the stage's mbarrier, plus on a piece's first block a bulk copy of
+//              the q rows;
 //   consumer   waits on the stage (bounded), on a first block loads q^T fragments from the
 //              stage and resets the softmax state, computes S^T = K q^T (16 tokens x 8 head
 //              columns) with 8 m16n8k16 bf16 MMAs (A = K via ldmatrix), updates the online
@@ -134,22 +136,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
   using L = Layout<kStep, kFp8>;
-  constexpr int kStagesN = L::kStagesN;
+  constexpr int kPool = kWarps * L::kStagesN;  // stages of the CTA
   constexpr int kStageB = L::kStage;
+  static_assert(kPool <= kWarps * 32, "one initialising thread per stage");
   extern __shared__ unsigned char smem_raw[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t bars = raw + warp * kStagesN * 8;
-  int4* descs = reinterpret_cast<int4*>(smem_raw + L::kDescOff) + warp * kStagesN;
   int* prefix = reinterpret_cast<int*>(smem_raw + L::kPrefixOff);  // N_s, s = 0..S
   // 128-byte swizzled TMA destinations must sit on 1024-byte boundaries.
-  const uint32_t tiles =
-      ((raw + L::kPrefixOff + prefix_bytes(a.num_seqs) + 1023u) & ~1023u) + warp * kStagesN * kStageB;
-  if (lane == 0) {
-    for (int st = 0; st < kStagesN; ++st) mbar_init(bars + 8 * st, 1);
+  const uint32_t tile_base = (raw + L::kPrefixOff + prefix_bytes(a.num_seqs) + 1023u) & ~1023u;
+  if (tid < kPool) {
+    mbar_init(raw + 8 * tid, 1);
     fence_mbar_init();
+  }
+  if (tid == 0) {
     prefetch_tensor_map(&tm_k);
     prefetch_tensor_map(&tm_v);
   }
@@ -196,6 +198,18 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
   const long long T = static_cast<long long>(Hkv) * prefix[S];
   const Ranges R = make_ranges(T, a);
   const int NW = gridDim.x * kWarps;
+  // Stage pool: the CTA's kPool stages are shared out among its warps that have a range.  Range
+  // v goes to warp v / grid of CTA v % grid, so these are warps 0 .. active - 1 (the others have
+  // no work); with fewer ranges than warps (fixed-size partitions over a few long sequences)
+  // each of them runs a deeper pipeline.
+  const int active = R.V > static_cast<int>(blockIdx.x)
+                         ? min(kWarps, (R.V - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                           static_cast<int>(gridDim.x))
+                         : 1;
+  const int n_st = kPool / active;  // this warp's stages, used in ring order
+  const uint32_t bars = raw + warp * n_st * 8;
+  int4* descs = reinterpret_cast<int4*>(smem_raw + L::kDescOff) + warp * n_st;
+  const uint32_t tiles = tile_base + warp * n_st * kStageB;
   const int gq = lane >> 2;  // fragment row group
   const int cq = lane & 3;   // fragment column pair
   const int mi = lane >> 3;  // ldmatrix: matrix this lane addresses
@@ -203,17 +217,17 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
 
   // ---------------------------------------------------------------- lookahead windows --
   // Window = up to 32 consecutive jobs of one range; lane j resolves job j.  Fields per lane:
-  // physical block id, segment, flags | valid << 8, partial slot.
+  // first cache row of the tile (physical block * Hkv + KV head) * 16, segment, flags | valid
+  // << 8 (kHasData when the block id is in range), partial slot.
   struct Window {
     int v;                // range
     long long x;          // first position
     int n;                // jobs in the window (0: none left)
-    int blk, seg, fl, slot;
+    int y, seg, fl, slot;
     int pos;              // fused step: position of the sequence's new token
   };
   auto resolve = [&](Window& W) {
-    W.blk = -1;
-    W.seg = W.fl = W.slot = W.pos = 0;
+    W.y = W.seg = W.fl = W.slot = W.pos = 0;
     if (W.n == 0 || lane >= W.n) return;
     const long long x0 = R.begin(W.v), x1 = R.begin(W.v + 1);
     const long long p = W.x + lane;
@@ -231,7 +245,9 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int j = static_cast<int>(off - static_cast<long long>(g) * ns);
     const long long Xi = static_cast<long long>(Hkv) * prefix[s] + static_cast<long long>(g) * ns;
     const int len = clamp_len(a.context_lens[s], a.max_context_len);
-    W.blk = a.block_tables[static_cast<size_t>(s) * a.max_blocks + j];
+    const int blk = a.block_tables[static_cast<size_t>(s) * a.max_blocks + j];
+    const bool ok = blk >= 0 && blk < a.num_blocks;
+    W.y = ok ? (blk * Hkv + g) * kBlockSize : 0;
     W.seg = s * Hkv + g;
     const int valid = min(kBlockSize, len - j * kBlockSize);
     uint32_t flags = ((p == x0 || j == 0) ? kFirst : 0u) | ((p == x1 - 1 || j == ns - 1) ? kLast : 0u) |
@@ -241,6 +257,7 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (j == ns - 1) flags |= kNew;
       if (W.pos < a.max_pos) flags |= kRope;  // len >= 1 here, so pos >= 0
     }
+    if (ok) flags |= kHasData;
     W.fl = static_cast<int>(flags | (static_cast<uint32_t>(valid) << 8));
     W.slot = W.v + W.seg;
   };
@@ -275,13 +292,13 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
       next_of(cur, nxt);
       resolve(nxt);
     }
-    const int blk = __shfl_sync(kFullMask, cur.blk, pk);
+    const int y = __shfl_sync(kFullMask, cur.y, pk);
     const int seg = __shfl_sync(kFullMask, cur.seg, pk);
     const int fl = __shfl_sync(kFullMask, cur.fl, pk);
     const int slot = __shfl_sync(kFullMask, cur.slot, pk);
     const int pos = kStep ? __shfl_sync(kFullMask, cur.pos, pk) : 0;
     ++pk;
-    const bool ok = blk >= 0 && blk < a.num_blocks;
+    const bool ok = (fl & kHasData) != 0;
     const bool first = (fl & kFirst) != 0;
     if (lane == 0) {
       if (!ok) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
@@ -291,36 +308,31 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (kStep && (fl & kNew) && !rope) raise_flag(a.status, PA_FLAG_POSITION_OOB);
       const bool fresh = rope && ok && (fl & kNew);  // the new token's K and V land in this tile
       const bool trig = rope && (first || fresh);    // stage the cos/sin row
-      descs[st] = make_int4(seg, fl | (ok ? static_cast<int>(kHasData) : 0), slot, blk);
+      descs[st] = make_int4(seg, fl, slot, y);
       const uint32_t bar = bars + 8 * st;
       const uint32_t dst = tiles + st * kStageB;
       const uint32_t bytes = (ok ? 2u * L::kTile : 0u) + (first ? static_cast<uint32_t>(G) * 256u : 0u) +
                              (trig ? kHeadDim * 4u : 0u) + (fresh ? kHeadDim * 4u : 0u);
-      const int s = seg / Hkv;
-      const int g = seg - s * Hkv;
       fence_proxy_async_smem();
       if (bytes) {
         mbar_arrive_expect_tx(bar, bytes);
         if (ok) {
-          const int y = (blk * Hkv + g) * kBlockSize;
-          if constexpr (kFp8) {  // one 128-byte x 16-row box per tile
+          if constexpr (kFp8) {
             tma_load_2d(dst, &tm_k, 0, y, bar);
             tma_load_2d(dst + L::kTile, &tm_v, 0, y, bar);
-          } else {               // two 64-column halves per tile
-            tma_load_2d(dst, &tm_k, 0, y, bar);
-            tma_load_2d(dst + kHalfBytes, &tm_k, 64, y, bar);
-            tma_load_2d(dst + 2 * kHalfBytes, &tm_v, 0, y, bar);
-            tma_load_2d(dst + 3 * kHalfBytes, &tm_v, 64, y, bar);
+          } else {
+            tma_load_3d(dst, &tm_k, 0, y, 0, bar);
+            tma_load_3d(dst + L::kTile, &tm_v, 0, y, 0, bar);
           }
         }
-        if (first) {
-          const size_t head0 = static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(g) * G;
+        if (first) {  // the segment's G query heads: heads seg * G .. seg * G + G - 1 of q
+          const size_t head0 = static_cast<size_t>(seg) * G;
           bulk_copy_g2s(dst + L::kQOff, a.q + head0 * kHeadDim, static_cast<uint32_t>(G) * 256u, bar);
         }
         if (trig)
           bulk_copy_g2s(dst + L::kCosSinOff, a.cos_sin + static_cast<size_t>(pos) * kHeadDim, kHeadDim * 4u, bar);
-        if (fresh) {
-          const size_t row = (static_cast<size_t>(s) * Hkv + g) * kHeadDim;
+        if (fresh) {  // row seg of the [S, Hkv] new-token rows
+          const size_t row = static_cast<size_t>(seg) * kHeadDim;
           bulk_copy_g2s(dst + L::kNewKOff, a.k_new + row, kHeadDim * 2u, bar);
           bulk_copy_g2s(dst + L::kNewVOff, a.v_new + row, kHeadDim * 2u, bar);
         }
@@ -422,11 +434,10 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
         rope_rotate_pairs(klo, khi, reinterpret_cast<const float2*>(cs)[lane],
                           reinterpret_cast<const float2*>(cs + 64)[lane]);
         const uint32_t vlo = vn[lane], vhi = vn[32 + lane];
-        const int s = d.x / Hkv;
-        const int g = d.x - s * Hkv;
-        const size_t crow = ((static_cast<size_t>(d.w) * Hkv + g) * kBlockSize + row) * kHeadDim;
+        const size_t crow = (static_cast<size_t>(d.w) + row) * kHeadDim;  // d.w: the tile's first cache row
         if constexpr (kFp8) {
           // E4M3 codes of k_rot / k_scale and v / v_scale, as the FP8 store kernel makes them.
+          const int g = d.x % Hkv;
           const float ik = __frcp_rn(a.k_scale[g]), iv = __frcp_rn(a.v_scale[g]);
           const uint16_t ck0 = e4m3x2_of(klo, ik), ck1 = e4m3x2_of(khi, ik);
           const uint16_t cv0 = e4m3x2_of(vlo, iv), cv1 = e4m3x2_of(vhi, iv);
@@ -574,10 +585,7 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
       }
     }
     if (fl & kLast) {
-      const int seg = d.x;
-      const int s = seg / Hkv;
-      const int g = seg - s * Hkv;
-      const size_t head0 = static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(g) * G;
+      const size_t head0 = static_cast<size_t>(d.x) * G;  // first query head of the segment
       // Full row sums: the 8 lanes sharing cq hold disjoint token shares of the same heads.
       float L0 = l0, L1 = l1;
 #pragma unroll
@@ -654,27 +662,48 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
   };
 
   // ---------------------------------------------------------------- pipeline --------
+  // The k-th use of a stage completes phase k & 1 of its mbarrier.
+  auto advance = [&](int& st, uint32_t& ph) {
+    if (++st == n_st) {
+      st = 0;
+      ph ^= 1u;
+    }
+  };
   int produced = 0, consumed = 0;
+  int pst = 0, cst = 0;    // stages of the next job produced / consumed
+  uint32_t pph = 0, cph = 0;
   bool more = true;
-  while (more && produced < kStagesN) {
-    if (produce(produced % kStagesN)) ++produced;
-    else more = false;
+  while (more && produced < n_st) {
+    if (produce(pst)) {
+      ++produced;
+      advance(pst, pph);
+    } else {
+      more = false;
+    }
   }
   while (consumed < produced) {
-    const int st = consumed % kStagesN;
-    if (!mbar_wait_bounded(bars + 8 * st, (consumed / kStagesN) & 1)) {
+    if (!mbar_wait_bounded(bars + 8 * cst, cph)) {
       if (lane == 0) raise_flag(a.status, PA_FLAG_TIMEOUT);
       // Let the other copies in flight land (bounded) before the CTA can exit.
-      for (int j = consumed + 1; j < produced; ++j)
-        mbar_wait_bounded(bars + 8 * (j % kStagesN), (j / kStagesN) & 1);
+      int st = cst;
+      uint32_t ph = cph;
+      for (int j = consumed + 1; j < produced; ++j) {
+        advance(st, ph);
+        mbar_wait_bounded(bars + 8 * st, ph);
+      }
       break;
     }
-    consume(st);
+    consume(cst);
     ++consumed;
+    advance(cst, cph);
     __syncwarp();
     if (more) {
-      if (produce(produced % kStagesN)) ++produced;
-      else more = false;
+      if (produce(pst)) {
+        ++produced;
+        advance(pst, pph);
+      } else {
+        more = false;
+      }
     }
   }
 }
@@ -833,9 +862,12 @@ cudaError_t launch_partition(DecodeArgs& a, const CUtensorMap& tm_k, const CUten
 
 }  // namespace
 
-// Tensor map of one cache viewed as a 2-D array [num_blocks * Hkv * 16 rows][128 cols] with
-// 128-byte swizzle: bf16 in boxes of 64 cols x 16 rows (two per tile), E4M3 bytes in boxes of
-// 128 cols x 16 rows (one per tile).  Encoded maps are cached by (address, rows, type).
+// Tensor map of one cache, 128-byte swizzle, one box per (block, KV head) tile.  The cache is
+// [num_blocks * Hkv * 16 rows][128 cols].  E4M3: a 2-D map, box 128 cols x 16 rows.  bf16: a
+// 128-col row is 256 bytes, wider than the swizzle span, so the map is 3-D -- (col within a
+// 64-col half, row, half) with strides 256 bytes (row) and 128 bytes (half) -- and the box
+// (64, 16, 2) lands a tile in shared memory as its two 2 KiB halves, cols 0-63 of the 16 rows
+// followed by cols 64-127.  Encoded maps are cached by (address, rows, type).
 bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* out) {
   struct Entry {
     const void* ptr;
@@ -858,16 +890,26 @@ bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* 
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return false;
   CUtensorMap m;
-  const cuuint64_t elem = fp8 ? 1 : 2;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * elem};
-  cuuint32_t box[2] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(kBlockSize)};
-  cuuint32_t estr[2] = {1, 1};
-  if (encode(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-             const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return false;
+  const cuuint64_t n = static_cast<cuuint64_t>(rows);
+  CUresult rc;
+  if (fp8) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), n};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim)};
+    cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(kBlockSize)};
+    cuuint32_t estr[2] = {1, 1};
+    rc = encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[3] = {64, n, 2};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2, 128};
+    cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(kBlockSize), 2u};
+    cuuint32_t estr[3] = {1, 1, 1};
+    rc = encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(cache), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (rc != CUDA_SUCCESS) return false;
   const int slot = used < kEntries ? used++ : (next++ % kEntries);
   table[slot] = Entry{cache, rows, fp8, m};
   *out = m;

@@ -117,10 +117,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (!(mask & (1 << i))) continue;
         const int y = (blk[i] * Hkv + g) * kBlockSize;
         const uint32_t d = dst + i * kPfBlockBytes;
-        tma_load_2d(d, &tm_k, 0, y, bar);
-        tma_load_2d(d + kPfHalf, &tm_k, 64, y, bar);
-        tma_load_2d(d + 2 * kPfHalf, &tm_v, 0, y, bar);
-        tma_load_2d(d + 3 * kPfHalf, &tm_v, 64, y, bar);
+        tma_load_3d(d, &tm_k, 0, y, 0, bar);              // both 64-col halves of the K tile
+        tma_load_3d(d + 2 * kPfHalf, &tm_v, 0, y, 0, bar);
       }
     } else {
       mbar_arrive(bar);
