@@ -44,9 +44,9 @@
  *      out          [num_seqs][num_q_heads][head_dim]
  *    With block_size 16 and head_dim 128 each (block, KV head) tile is 4 KiB contiguous.
  *  - Slot of a token: physical_block * block_size + offset_in_block.
- *  - Supported shape: head_dim == 128, block_size == 16, num_q_heads a multiple of
- *    num_kv_heads with group size num_q_heads / num_kv_heads in [1, 8].  Anything else
- *    returns PA_ERR_SHAPE.
+ *  - Supported shape: head_dim == 128, block_size == 16, num_kv_heads <= 4096,
+ *    num_q_heads a multiple of num_kv_heads with group size num_q_heads / num_kv_heads in
+ *    [1, 8].  Anything else returns PA_ERR_SHAPE.
  *  - Memory: every pointer is device memory owned by the caller (cudaMalloc, PyTorch, ...)
  *    and must be 16-byte aligned (PA_ERR_ALIGN otherwise).  The library allocates nothing.
  *    Its only global state is one 32-bit device status word per GPU, and the fixed scratch

@@ -24,7 +24,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_dims(const pa_dims* d) {
   if (!d) return PA_ERR_NULL;
   if (d->head_dim != 128 || d->block_size != 16) return PA_ERR_SHAPE;
-  if (d->num_q_heads <= 0 || d->num_kv_heads <= 0) return PA_ERR_SHAPE;
+  if (d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->num_kv_heads > pa::kMaxKvHeads) return PA_ERR_SHAPE;
   if (d->num_q_heads % d->num_kv_heads != 0) return PA_ERR_SHAPE;
   const int G = d->num_q_heads / d->num_kv_heads;
   if (G < 1 || G > 8) return PA_ERR_SHAPE;

@@ -27,6 +27,8 @@ namespace pa {
 // warps of the persistent grid (bounds the partial slots the workspace must hold).
 constexpr int kMaxDecodeSeqs = 8192;
 constexpr int kMaxDecodeWarps = 2048;
+// KV heads per layer (the decode kernel packs the KV head index into 16 bits of a job word).
+constexpr int kMaxKvHeads = 4096;
 
 struct RopeArgs {
   __nv_bfloat16* q;                 // [T][Hq][128], rotated in place

@@ -94,7 +94,8 @@ struct Layout {
   }
 };
 
-// Job flags (low bits of a descriptor's flag word; valid tokens sit at bits 8-12).
+// Job flags (low bits of a descriptor's flag word; valid tokens sit at bits 8-12, the KV head
+// at bits 16-31).
 constexpr uint32_t kFirst = 1u, kLast = 2u, kWhole = 4u, kHasData = 8u;
 constexpr uint32_t kNew = 16u;   // fused step: the block holding the segment's new token
 constexpr uint32_t kRope = 32u;  // fused step: the sequence's position has a cos/sin row
@@ -217,17 +218,19 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
 
   // ---------------------------------------------------------------- lookahead windows --
   // Window = up to 32 consecutive jobs of one range; lane j resolves job j.  Fields per lane:
-  // first cache row of the tile (physical block * Hkv + KV head) * 16, segment, flags | valid
-  // << 8 (kHasData when the block id is in range), partial slot.
+  // physical block id, segment, flags | valid << 8 | KV head << 16, partial slot.  The block
+  // id is left as loaded -- nothing here waits for the block-table load, so the two windows
+  // resolved up front have their loads in flight together; the producer uses it.
   struct Window {
     int v;                // range
     long long x;          // first position
     int n;                // jobs in the window (0: none left)
-    int y, seg, fl, slot;
+    int blk, seg, fl, slot;
     int pos;              // fused step: position of the sequence's new token
   };
   auto resolve = [&](Window& W) {
-    W.y = W.seg = W.fl = W.slot = W.pos = 0;
+    W.blk = -1;
+    W.seg = W.fl = W.slot = W.pos = 0;
     if (W.n == 0 || lane >= W.n) return;
     const long long x0 = R.begin(W.v), x1 = R.begin(W.v + 1);
     const long long p = W.x + lane;
@@ -245,9 +248,7 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int j = static_cast<int>(off - static_cast<long long>(g) * ns);
     const long long Xi = static_cast<long long>(Hkv) * prefix[s] + static_cast<long long>(g) * ns;
     const int len = clamp_len(a.context_lens[s], a.max_context_len);
-    const int blk = a.block_tables[static_cast<size_t>(s) * a.max_blocks + j];
-    const bool ok = blk >= 0 && blk < a.num_blocks;
-    W.y = ok ? (blk * Hkv + g) * kBlockSize : 0;
+    W.blk = a.block_tables[static_cast<size_t>(s) * a.max_blocks + j];
     W.seg = s * Hkv + g;
     const int valid = min(kBlockSize, len - j * kBlockSize);
     uint32_t flags = ((p == x0 || j == 0) ? kFirst : 0u) | ((p == x1 - 1 || j == ns - 1) ? kLast : 0u) |
@@ -257,8 +258,7 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (j == ns - 1) flags |= kNew;
       if (W.pos < a.max_pos) flags |= kRope;  // len >= 1 here, so pos >= 0
     }
-    if (ok) flags |= kHasData;
-    W.fl = static_cast<int>(flags | (static_cast<uint32_t>(valid) << 8));
+    W.fl = static_cast<int>(flags | (static_cast<uint32_t>(valid) << 8) | (static_cast<uint32_t>(g) << 16));
     W.slot = W.v + W.seg;
   };
   // The window after W: the rest of W's range, else the start of this warp's next range.
@@ -292,13 +292,13 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
       next_of(cur, nxt);
       resolve(nxt);
     }
-    const int y = __shfl_sync(kFullMask, cur.y, pk);
+    const int blk = __shfl_sync(kFullMask, cur.blk, pk);
     const int seg = __shfl_sync(kFullMask, cur.seg, pk);
     const int fl = __shfl_sync(kFullMask, cur.fl, pk);
     const int slot = __shfl_sync(kFullMask, cur.slot, pk);
     const int pos = kStep ? __shfl_sync(kFullMask, cur.pos, pk) : 0;
     ++pk;
-    const bool ok = (fl & kHasData) != 0;
+    const bool ok = blk >= 0 && blk < a.num_blocks;
     const bool first = (fl & kFirst) != 0;
     if (lane == 0) {
       if (!ok) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
@@ -308,7 +308,9 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (kStep && (fl & kNew) && !rope) raise_flag(a.status, PA_FLAG_POSITION_OOB);
       const bool fresh = rope && ok && (fl & kNew);  // the new token's K and V land in this tile
       const bool trig = rope && (first || fresh);    // stage the cos/sin row
-      descs[st] = make_int4(seg, fl, slot, y);
+      // first cache row of the tile: (physical block * Hkv + KV head) * 16
+      const int y = ok ? (blk * Hkv + (fl >> 16)) * kBlockSize : 0;
+      descs[st] = make_int4(seg, fl | (ok ? static_cast<int>(kHasData) : 0), slot, y);
       const uint32_t bar = bars + 8 * st;
       const uint32_t dst = tiles + st * kStageB;
       const uint32_t bytes = (ok ? 2u * L::kTile : 0u) + (first ? static_cast<uint32_t>(G) * 256u : 0u) +
@@ -422,7 +424,7 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
       for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     }
     if (fl & kHasData) {
-      const int valid = static_cast<int>(fl >> 8);
+      const int valid = static_cast<int>((fl >> 8) & 0xffu);
       if (kStep && (fl & kNew) && (fl & kRope)) {
         // The new token (row valid - 1 of this tile): rotate its k, write k and v into the
         // staged tiles before they are read, and store both into the cache slot.

@@ -97,6 +97,7 @@ def test_decode_rejects_bad_arguments_on_the_host(L):
     assert decode_call(L, d=dims(b=32)) == b.PA_ERR_SHAPE
     assert decode_call(L, d=dims(hq=12, hkv=5)) == b.PA_ERR_SHAPE
     assert decode_call(L, d=dims(hq=18, hkv=2)) == b.PA_ERR_SHAPE      # group of 9 > 8
+    assert decode_call(L, d=dims(hq=8194, hkv=4097)) == b.PA_ERR_SHAPE  # more KV heads than 4096
     assert decode_call(L, S=-1) == b.PA_ERR_RANGE
     assert decode_call(L, S=0) == b.PA_OK                              # no-op
     for kw in ("q", "kc", "vc", "bt", "ctx", "out"):
