@@ -59,7 +59,7 @@ METRIC = "paged GQA decode: KV-cache HBM GB/s (% of GB300 peak) and attention to
 # the step form and a hash of the CUDA sources it was taken on: once a kernel changes, the
 # hash no longer matches and roofline.traffic is reported as null until it is captured again.
 MEASURED_TRAFFIC = {
-    ("mix64", "fused", "552d96ac4d3e7533"): 122116864 + 3461632 + 4183040,
+    ("mix64", "fused", "05e0742c5cfe9914"): 122112768 + 3245312 + 4183040,
 }
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
