@@ -166,8 +166,8 @@ class ClockSampler:
 class DeviceStep:
     """A workload resident on the GPU and one step of the hot path over it."""
 
-    def __init__(self, w: W.Workload, torch, binding, fused: bool = True):
-        self.w, self.torch, self.pa, self.fused = w, torch, binding, fused
+    def __init__(self, w: W.Workload, torch, binding, fused: bool = True, early: bool = True):
+        self.w, self.torch, self.pa, self.fused, self.early = w, torch, binding, fused, early
         dev = torch.device("cuda")
 
         def bf(a):
@@ -204,11 +204,15 @@ class DeviceStep:
                        workspace=self.workspace, out=self.out[i])
 
     def decode_step(self, i):
+        # Early metadata: the lengths and block table are written before the timed steps and
+        # never by a kernel, so each layer's kernel may resolve its work while the previous
+        # kernel finishes.
         w = self.w
         self.pa.decode_step(self.q[i], self.k[i], self.v[i], self.cos_sin, self.k_cache[i],
                             self.v_cache[i], self.block_tables, self.context_lens,
                             w.max_context_len, w.scale, partition_tokens=self.P,
-                            workspace=self.workspace, out=self.out[i])
+                            workspace=self.workspace, out=self.out[i],
+                            early_metadata=self.early)
 
     def step(self):
         for i in range(self.w.num_layers):
@@ -234,7 +238,7 @@ def run_gpu(args, rank, world, dist):
     w = base if rank == 0 else W.make(args.workload, seed=base.seed + 1000 * rank)
     if args.partition_tokens is not None:
         w.partition_tokens = args.partition_tokens
-    st = DeviceStep(w, torch, binding, fused=not args.split_step)
+    st = DeviceStep(w, torch, binding, fused=not args.split_step, early=not args.no_early_metadata)
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     sink = torch.empty(1, dtype=torch.float32, device="cuda")
@@ -558,9 +562,12 @@ def run_e2e(args, st, torch, binding, flush_l2):
         d_in.copy_(h_in, non_blocking=True)
         for i in range(L):
             if st.fused:
+                # layers after the first follow a decode kernel, and the copy that wrote the
+                # tables precedes them all: they may start early
                 binding.decode_step(q[i], k[i], v[i], st.cos_sin, st.k_cache[i], st.v_cache[i], bt,
                                     ctx, w.max_context_len, w.scale, partition_tokens=st.P,
-                                    workspace=st.workspace, out=d_out[i])
+                                    workspace=st.workspace, out=d_out[i],
+                                    early_metadata=st.early and i > 0)
                 continue
             binding.rope_kv_store(q[i], k[i], v[i], pos, st.cos_sin, slots, st.k_cache[i],
                                   st.v_cache[i])
@@ -601,6 +608,8 @@ def config_of(w, st, world):
     if st is not None:
         c["step"] = ("pa_decode_step (RoPE + KV store fused into the decode launch)" if st.fused
                      else "pa_rope_kv_store then pa_decode")
+        if st.fused:
+            c["early_metadata"] = bool(st.early)
     if w.meta.get("shared_prefix_blocks"):
         c["unique_kv_bytes_per_step_per_gpu"] = w.unique_kv_bytes_per_layer() * w.num_layers
     return c
@@ -696,6 +705,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each call instead of a CUDA graph")
+    ap.add_argument("--no-early-metadata", action="store_true",
+                    help="run the step without PA_STEP_EARLY_METADATA")
     ap.add_argument("--no-fp8", action="store_true", help="skip the E4M3-cache decode measurement")
     ap.add_argument("--no-prefill", action="store_true", help="skip the pa_prefill measurement")
     ap.add_argument("--no-block-ops", action="store_true",

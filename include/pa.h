@@ -216,6 +216,7 @@ int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_ca
  *   k, v              [S][Hkv][D] bf16, the new token's key and value, read only
  *   cos_sin, max_pos  as for pa_rope_kv_store
  *   k_cache, v_cache  [num_blocks][Hkv][16][D] bf16, read, and written at the new slots
+ *   flags             0 or PA_STEP_EARLY_METADATA (below); other bits -> PA_ERR_RANGE
  *   everything else   as for pa_decode (same workspace size: pa_decode_workspace_size)
  * Returns PA_OK or a PA_ERR_* code (nothing launched on error).  Launches one kernel, plus
  * one merge kernel.
@@ -224,7 +225,24 @@ int pa_decode_step(const pa_dims* dims, int num_seqs, const void* q, const void*
                    const float* cos_sin, int max_pos, void* k_cache, void* v_cache, int num_blocks,
                    const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                    int max_context_len, float scale, int partition_tokens, void* workspace,
-                   size_t workspace_bytes, void* out, void* stream);
+                   size_t workspace_bytes, void* out, unsigned flags, void* stream);
+
+/*
+ * PA_STEP_EARLY_METADATA -- flag of pa_decode_step / pa_decode_step_fp8.  The caller promises
+ * that no kernel which can still be running when the call is made on `stream` writes
+ * context_lens or block_tables: they were written earlier (by the host, a copy, or kernels
+ * that have completed).  The decode kernel then starts while the preceding kernel on the
+ * stream is still finishing (programmatic dependent launch): it reads the lengths, builds its
+ * block-count prefix and resolves its first jobs through the block table, and waits for that
+ * kernel before its first copy into shared memory (q, k, v, cos_sin, cache tiles) and before
+ * any write.  The decode entry points (pa_decode*) let the next launch on the stream start
+ * only once they no longer need the preceding work, so a step may follow another step with
+ * this flag; a step right after a kernel that rewrites the tables must not set it.  A
+ * multi-layer decode step whose layers follow one another on one stream is the intended use:
+ * layer l + 1 resolves its work while layer l finishes.  Breaking the promise gives stale
+ * lengths or block ids, never out-of-range accesses (both are still checked).
+ */
+#define PA_STEP_EARLY_METADATA 0x1u
 
 /*
  * pa_prefill -- paged (chunked) prefill attention ([PV] §2: the PagedAttention prefill kernel;
@@ -307,14 +325,14 @@ int pa_decode_fp8(const pa_dims* dims, int num_seqs, const void* q, const void* 
 /*
  * pa_decode_step_fp8 -- pa_decode_step over E4M3 caches: equals pa_rope_kv_store_fp8 (position
  * context_lens[s] - 1, that position's slot) followed by pa_decode_fp8, with q left unchanged.
- * Arguments as pa_decode_step plus k_scale, v_scale.
+ * Arguments as pa_decode_step plus k_scale, v_scale (flags included).
  */
 int pa_decode_step_fp8(const pa_dims* dims, int num_seqs, const void* q, const void* k,
                        const void* v, const float* cos_sin, int max_pos, void* k_cache,
                        void* v_cache, const float* k_scale, const float* v_scale, int num_blocks,
                        const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                        int max_context_len, float scale, int partition_tokens, void* workspace,
-                       size_t workspace_bytes, void* out, void* stream);
+                       size_t workspace_bytes, void* out, unsigned flags, void* stream);
 
 /* Most caches one pa_copy_blocks call can name (K and V of up to 128 layers). */
 #define PA_MAX_BLOCK_CACHES 256

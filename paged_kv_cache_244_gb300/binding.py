@@ -26,6 +26,7 @@ PA_ERR_TIMEOUT = -7
 PA_ERR_ALIGN = -8
 PA_ERR_MEMORY = -9
 PA_MAX_BLOCK_CACHES = 256
+PA_STEP_EARLY_METADATA = 0x1
 
 PA_FLAG_BLOCK_ID_OOB = 0x1
 PA_FLAG_CONTEXT_LEN_OOB = 0x2
@@ -67,7 +68,7 @@ def lib():
         L.pa_decode.argtypes = [pd, i, p, p, p, i, p, i, p, i, f, i, p, ctypes.c_size_t, p, p]
         L.pa_decode.restype = i
         L.pa_decode_step.argtypes = [pd, i, p, p, p, p, i, p, p, i, p, i, p, i, f, i, p,
-                                     ctypes.c_size_t, p, p]
+                                     ctypes.c_size_t, p, ctypes.c_uint, p]
         L.pa_decode_step.restype = i
         L.pa_rope_kv_store_fp8.argtypes = [pd, i, p, p, p, p, p, i, p, p, p, i, p, p, p]
         L.pa_rope_kv_store_fp8.restype = i
@@ -75,7 +76,7 @@ def lib():
                                     p, p]
         L.pa_decode_fp8.restype = i
         L.pa_decode_step_fp8.argtypes = [pd, i, p, p, p, p, i, p, p, p, p, i, p, i, p, i, f, i, p,
-                                         ctypes.c_size_t, p, p]
+                                         ctypes.c_size_t, p, ctypes.c_uint, p]
         L.pa_decode_step_fp8.restype = i
         L.pa_prefill.argtypes = [pd, i, i, p, p, i, p, p, i, p, i, p, i, f, p, p]
         L.pa_prefill.restype = i
@@ -205,12 +206,16 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len, sca
 
 
 def decode_step(q, k, v, cos_sin, k_cache, v_cache, block_tables, context_lens, max_context_len,
-                scale, partition_tokens=0, workspace=None, out=None, stream=None):
+                scale, partition_tokens=0, workspace=None, out=None, stream=None,
+                early_metadata=False):
     """One fused decode step (pa_decode_step): RoPE + KV store of each sequence's new token at
     position context_lens[s] - 1, then decode attention, in one launch.  Returns out.
 
     q [S, Hq, D] bf16, NOT rotated (left unchanged); k, v [S, Hkv, D] bf16 (the new token);
     cos_sin [max_pos, D] fp32; the rest as for decode().  The caches get the new K and V.
+    early_metadata sets PA_STEP_EARLY_METADATA: the caller promises that no kernel still
+    running on the stream writes context_lens or block_tables, and the kernel resolves its
+    work from them before the preceding kernel has finished.
     """
     S, Hq, D = q.shape
     nb, Hkv, B, D2 = k_cache.shape
@@ -236,7 +241,7 @@ def decode_step(q, k, v, cos_sin, k_cache, v_cache, block_tables, context_lens, 
         _dev_ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
         _dev_ptr(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
         int(partition_tokens), _dev_ptr(workspace, "workspace"), ws_bytes, _dev_ptr(out, "out", bf),
-        _stream(stream))
+        PA_STEP_EARLY_METADATA if early_metadata else 0, _stream(stream))
     _check(rc, "pa_decode_step")
     return out
 
@@ -328,8 +333,9 @@ def decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens
 
 def decode_step_fp8(q, k, v, cos_sin, k_cache, v_cache, k_scale, v_scale, block_tables,
                     context_lens, max_context_len, scale, partition_tokens=0, workspace=None,
-                    out=None, stream=None):
-    """pa_decode_step_fp8: the fused step over E4M3 caches (q left unchanged)."""
+                    out=None, stream=None, early_metadata=False):
+    """pa_decode_step_fp8: the fused step over E4M3 caches (q left unchanged); early_metadata
+    as for decode_step."""
     S, Hq, D = q.shape
     nb, Hkv, B, D2, kc, vc, ks, vs = _fp8_args(k_cache, v_cache, k_scale, v_scale)
     if D2 != D or tuple(k.shape) != (S, Hkv, D) or tuple(v.shape) != (S, Hkv, D):
@@ -348,7 +354,8 @@ def decode_step_fp8(q, k, v, cos_sin, k_cache, v_cache, k_scale, v_scale, block_
         _dev_ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
         _dev_ptr(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
         int(partition_tokens), _dev_ptr(workspace, "workspace"),
-        workspace.numel() * workspace.element_size(), _dev_ptr(out, "out", bf), _stream(stream))
+        workspace.numel() * workspace.element_size(), _dev_ptr(out, "out", bf),
+        PA_STEP_EARLY_METADATA if early_metadata else 0, _stream(stream))
     _check(rc, "pa_decode_step_fp8")
     return out
 

@@ -198,9 +198,10 @@ int decode_step(const pa_dims* dims, int num_seqs, const void* q, const void* k,
                 const float* k_scale, const float* v_scale, int num_blocks,
                 const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                 int max_context_len, float scale, int partition_tokens, void* workspace,
-                size_t workspace_bytes, void* out, void* stream) {
+                size_t workspace_bytes, void* out, unsigned flags, void* stream) {
   // The new token's arguments first (host checks only), then everything pa_decode checks.
   if (const int rc = check_dims(dims)) return rc;
+  if (flags & ~PA_STEP_EARLY_METADATA) return PA_ERR_RANGE;
   if (num_seqs < 0 || num_seqs > pa::kMaxDecodeSeqs) return PA_ERR_RANGE;
   if (num_seqs == 0) return PA_OK;
   if (!k || !v || !cos_sin) return PA_ERR_NULL;
@@ -219,6 +220,7 @@ int decode_step(const pa_dims* dims, int num_seqs, const void* q, const void* k,
   a.v_store = static_cast<__nv_bfloat16*>(v_cache);
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  a.early_metadata = (flags & PA_STEP_EARLY_METADATA) ? 1 : 0;
   return pa::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
                                                                                  : PA_ERR_CUDA;
 }
@@ -288,10 +290,10 @@ int pa_decode_step(const pa_dims* dims, int num_seqs, const void* q, const void*
                    const float* cos_sin, int max_pos, void* k_cache, void* v_cache, int num_blocks,
                    const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                    int max_context_len, float scale, int partition_tokens, void* workspace,
-                   size_t workspace_bytes, void* out, void* stream) {
+                   size_t workspace_bytes, void* out, unsigned flags, void* stream) {
   return decode_step(dims, num_seqs, q, k, v, cos_sin, max_pos, k_cache, v_cache, nullptr, nullptr,
                      num_blocks, block_tables, max_blocks, context_lens, max_context_len, scale,
-                     partition_tokens, workspace, workspace_bytes, out, stream);
+                     partition_tokens, workspace, workspace_bytes, out, flags, stream);
 }
 
 int pa_decode_step_fp8(const pa_dims* dims, int num_seqs, const void* q, const void* k,
@@ -299,11 +301,11 @@ int pa_decode_step_fp8(const pa_dims* dims, int num_seqs, const void* q, const v
                        void* v_cache, const float* k_scale, const float* v_scale, int num_blocks,
                        const int32_t* block_tables, int max_blocks, const int32_t* context_lens,
                        int max_context_len, float scale, int partition_tokens, void* workspace,
-                       size_t workspace_bytes, void* out, void* stream) {
+                       size_t workspace_bytes, void* out, unsigned flags, void* stream) {
   if (const int rc = scales_ok(dims, num_seqs, k_scale, v_scale)) return rc;
   return decode_step(dims, num_seqs, q, k, v, cos_sin, max_pos, k_cache, v_cache, k_scale, v_scale,
                      num_blocks, block_tables, max_blocks, context_lens, max_context_len, scale,
-                     partition_tokens, workspace, workspace_bytes, out, stream);
+                     partition_tokens, workspace, workspace_bytes, out, flags, stream);
 }
 
 int pa_decode_fp8(const pa_dims* dims, int num_seqs, const void* q, const void* k_cache,

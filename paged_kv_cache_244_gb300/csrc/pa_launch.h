@@ -73,6 +73,9 @@ struct DecodeArgs {
   // code * scale of its KV head.
   const float* k_scale;             // [Hkv]
   const float* v_scale;             // [Hkv]
+  // Lengths and block table are read before the preceding kernel on the stream has finished
+  // (the caller's promise that it writes neither).
+  int early_metadata;
 };
 
 // Whole-block copies between pools (copy-on-write, swap out / in).  Pool pointers are device

@@ -156,7 +156,11 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     prefetch_tensor_map(&tm_k);
     prefetch_tensor_map(&tm_v);
   }
-  pdl_wait_prior_grid();
+  // With early metadata the lengths and block table are read, and the work resolved, before
+  // the preceding kernel has finished; the first copy into shared memory and every write
+  // wait for it (below, before the pipeline's first fill).
+  const bool early = a.early_metadata != 0;
+  if (!early) pdl_wait_prior_grid();
   pdl_allow_next_grid();
 
   const int S = a.num_seqs;
@@ -675,6 +679,10 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
   int pst = 0, cst = 0;    // stages of the next job produced / consumed
   uint32_t pph = 0, cph = 0;
   bool more = true;
+  // Early metadata: the prologue and the lookahead above ran beside the preceding kernel; wait
+  // for it before the first copy.  (Waiting only after issuing the first tile copies, so that
+  // they too overlap it, measured slower: the wait then also sits out those copies.)
+  if (early) pdl_wait_prior_grid();
   while (more && produced < n_st) {
     if (produce(pst)) {
       ++produced;
@@ -723,13 +731,25 @@ constexpr int kMergeWarps = 8;
 constexpr int kMergeSplit = 4;   // warps per (sequence, query head)
 constexpr int kMergeBatch = 32;  // pieces loaded per round trip
 
+// Every merge warp waits for the partition kernel before it exits or lets the next grid on
+// the stream launch, so that a following launch that reads ahead of its own wait (a decode
+// step with early metadata) never runs beside a partition kernel still writing its new-token
+// slots.
+__device__ __forceinline__ void wait_then_release() {
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+}
+
 __global__ void __launch_bounds__(kMergeWarps * 32, 2) decode_merge_kernel(const DecodeArgs a) {
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int w = gw / kMergeSplit;                  // (sequence, query head)
   const int quarter = gw - w * kMergeSplit;        // dims 32 quarter .. 32 quarter + 31
   const int S = a.num_seqs;
-  if (w >= S * a.num_q_heads) return;
+  if (w >= S * a.num_q_heads) {
+    wait_then_release();
+    return;
+  }
   const int Hkv = a.num_kv_heads;
   const int G = a.num_q_heads / Hkv;
   const int s = w / a.num_q_heads;
@@ -752,7 +772,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) decode_merge_kernel(const
   const int dim = quarter * 32 + lane;
   __nv_bfloat16* orow = a.out + static_cast<size_t>(w) * kHeadDim + dim;
   if (ns == 0) {  // empty context: zero row (after the partition kernel, which may read `out`)
-    pdl_wait_prior_grid();
+    wait_then_release();
     *orow = __float2bfloat16_rn(0.f);
     return;
   }
@@ -760,13 +780,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) decode_merge_kernel(const
   const long long Xi = static_cast<long long>(Hkv) * before + static_cast<long long>(g) * ns;
   const int v_first = R.owner(Xi);
   const int npieces = R.owner(Xi + ns - 1) - v_first + 1;
-  if (npieces <= 1) return;  // written directly by the partition kernel
+  if (npieces <= 1) {  // written directly by the partition kernel
+    wait_then_release();
+    return;
+  }
   // piece p lives in slot v_first + p + segment; its row for this head is slot * G + hl
   const size_t row_base = (static_cast<size_t>(v_first) + s * Hkv + g) * G + hl;
   const float2* ml = a.ws_ml + row_base;                               // stride G per piece
   const float* rows = a.ws_o + row_base * kHeadDim + dim;              // stride G * 128
   const size_t stride = static_cast<size_t>(G) * kHeadDim;
-  pdl_wait_prior_grid();
+  wait_then_release();
 
   float M = -INFINITY, L = 0.f, acc = 0.f;
   for (int base = 0; base < npieces; base += kMergeBatch) {

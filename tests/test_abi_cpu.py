@@ -120,14 +120,17 @@ def test_decode_step_rejects_bad_arguments_on_the_host(L):
     from paged_kv_cache_244_gb300 import binding as b
 
     def call(d=None, S=2, maxpos=64, nb=16, maxb=4, maxctx=40, scale=0.088, part=0, wsb=1 << 30,
-             **ptrs):
+             flags=0, **ptrs):
         a = dict(q=OK_PTR, k=OK_PTR, v=OK_PTR, cs=OK_PTR, kc=OK_PTR, vc=OK_PTR, bt=OK_PTR,
                  ctx=OK_PTR, ws=OK_PTR, out=OK_PTR)
         a.update(ptrs)
         d = dims() if d is None else d
         return L.pa_decode_step(ctypes.byref(d), S, a["q"], a["k"], a["v"], a["cs"], maxpos,
                                 a["kc"], a["vc"], nb, a["bt"], maxb, a["ctx"], maxctx, scale, part,
-                                a["ws"], wsb, a["out"], None)
+                                a["ws"], wsb, a["out"], flags, None)
+
+    assert call(flags=2) == b.PA_ERR_RANGE                              # unknown flag bit
+    assert call(flags=b.PA_STEP_EARLY_METADATA | 0x100) == b.PA_ERR_RANGE
 
     assert call(d=dims(d=64)) == b.PA_ERR_SHAPE
     assert call(S=-1) == b.PA_ERR_RANGE
@@ -192,10 +195,12 @@ def test_fp8_entry_points_reject_bad_arguments_on_the_host(L):
     assert store(T=0) == b.PA_OK
     assert store(ks=None) == b.PA_ERR_NULL and store(vs=MIS_PTR) == b.PA_ERR_ALIGN
 
-    def step(ks=OK_PTR, vs=OK_PTR, S=2, k=OK_PTR):
+    def step(ks=OK_PTR, vs=OK_PTR, S=2, k=OK_PTR, flags=0):
         return L.pa_decode_step_fp8(ctypes.byref(d), S, OK_PTR, k, OK_PTR, OK_PTR, 64, OK_PTR, OK_PTR,
                                     ks, vs, 16, OK_PTR, 4, OK_PTR, 40, 0.088, 0, OK_PTR, 1 << 30,
-                                    OK_PTR, None)
+                                    OK_PTR, flags, None)
+
+    assert step(flags=4) == b.PA_ERR_RANGE
 
     assert step(S=0) == b.PA_OK
     assert step(ks=None) == b.PA_ERR_NULL and step(vs=MIS_PTR) == b.PA_ERR_ALIGN
