@@ -7,8 +7,11 @@ decode over the paged cache.
 A step is one pass of the whole hot path over one batch, for each layer of the workload:
 pa_decode_step, which rotates and stores every sequence's new token and attends over every
 cached context in one launch (plus the merge of split contexts); or, with --split-step,
-pa_rope_kv_store followed by pa_decode.  The metric is KV-cache bytes read per second: sum(context_lens) * Hkv * D * 2 B
-(K and V) per layer per step, over the step's device time.  L2 is flushed between timed steps,
+pa_rope_kv_store followed by pa_decode.  The fused step sets PA_STEP_EARLY_METADATA (lengths
+and block tables are written before the timed steps, never by a kernel), so each layer's
+kernel resolves its work while the previous one finishes.  The metric is KV-cache bytes read
+per second: sum(context_lens) * Hkv * D * 2 B (K and V) per layer per step, over the step's
+device time.  L2 is flushed between timed steps,
 outside the timed events, because the workloads' caches fit in L2: a 512 MiB write, then a
 read of the same buffer so that no dirty flush lines are written back inside the timed step.
 
@@ -16,7 +19,8 @@ The printed JSON line carries:
   value / ms_per_step  from CUDA events around each step, inputs resident in HBM;
   e2e                  the same metric when every step also copies its inputs (new-token
                        q/k/v, positions, slots, block tables, lengths) from pinned host
-                       memory and reads the output back, all inside the timed region;
+                       memory and reads the output back, all inside the timed region (the
+                       copies and calls replayed as one CUDA graph, like the device step);
   roofline             the step's decode call (its partition kernel plus the merge kernel)
                        on one layer, timed alone with CUDA events, against the measured HBM
                        copy bandwidth;
@@ -374,7 +378,7 @@ def run_gpu(args, rank, world, dist):
         "pa_decode_us": round(1e3 * float(np.mean(plain_ms)), 3),
         "e2e": {"value": round(all_bytes * args.steps / (e2e_ms_max * 1e-3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "ms_per_step": round(e2e_ms_max / args.steps, 6)},
+                "ms_per_step": round(e2e_ms_max / args.steps, 6), "launch": e2e["launch"]},
         "gpu_launches": st.launches_per_step * args.steps,
         "block_ops": blocks,
         "fp8_kv": fp8,
@@ -577,16 +581,31 @@ def run_e2e(args, st, torch, binding, flush_l2):
 
     for _ in range(2):
         one()
+    torch.cuda.synchronize()
+    # As for the device-only step: the whole step -- the H2D copy, every layer's call, the D2H
+    # copy -- recorded once as a CUDA graph and replayed, unless --no-graph.
+    step_fn, how = one, "eager calls"
+    if not args.no_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                one()
+            graph.replay()
+            torch.cuda.synchronize()
+            step_fn, how = graph.replay, "CUDA graph of the H2D copy, the calls and the D2H copy"
+        except Exception as e:  # capture unsupported here: keep eager calls
+            how = f"eager calls (graph capture failed: {type(e).__name__})"
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     for a, b in evs:
         flush_l2()
         a.record(stream)
-        one()
+        step_fn()
         b.record(stream)
     torch.cuda.synchronize()
     ms = float(np.sum([a.elapsed_time(b) for a, b in evs]))
-    return {"ms": ms, "h2d": int(total), "d2h": int(h_out.numel() * h_out.element_size())}
+    return {"ms": ms, "h2d": int(total), "d2h": int(h_out.numel() * h_out.element_size()),
+            "launch": how}
 
 
 def config_of(w, st, world):
