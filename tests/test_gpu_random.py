@@ -4,7 +4,7 @@ Each case draws a batch size, context lengths (short, block-aligned, ragged and 
 a GQA shape, a split size and a pool layout from a seeded generator. It then checks, with the
 same bars as the targeted tests:
 - decode;
-- the fused step;
+- the fused step (every other case with early metadata);
 - the E4M3 decode;
 - prefill.
 """
@@ -72,10 +72,12 @@ def test_random_decode_and_step(pa, orc, seed):
                     w.scale, partition_tokens=P)
     torch.cuda.synchronize()
     assert_out_close(host_bits(out), ref, f"decode seed {seed} P={P} {hq}/{hkv}")
-    # the fused step from the unrotated inputs
+    # the fused step from the unrotated inputs; odd seeds with early metadata (the tables were
+    # uploaded by copies, and the decode above does not write them)
     e = DeviceLayer(w)
     got = pa.decode_step(e.q, e.k, e.v, e.cos_sin, e.k_cache, e.v_cache, e.block_tables,
-                         e.context_lens, w.max_context_len, w.scale, partition_tokens=P)
+                         e.context_lens, w.max_context_len, w.scale, partition_tokens=P,
+                         early_metadata=bool(seed % 2))
     torch.cuda.synchronize()
     assert np.array_equal(host_bits(e.v_cache), vc)
     assert bf16_ulp_distance(host_bits(e.k_cache), kc).max() <= 1
