@@ -46,8 +46,8 @@
 //          whose job holds a sequence's new token (position len - 1) stages the token's k, v and
 //          cos/sin row with the tiles, rotates k, writes both rows into the staged tiles before
 //          the MMAs and into the cache slot; each piece rotates its q fragments in registers.
-//   kFp8   E4M3 caches with one scale per KV head: 2 KiB tiles, one 128-byte box each, four
-//          stages; the byte tiles are read by ldmatrix as 16-bit pairs and widened exactly to
+//   kFp8   E4M3 caches with one scale per KV head: 2 KiB tiles, one 128-byte box each, CTAs of
+//          12 warps with 2 stages; the byte tiles are read by ldmatrix as 16-bit pairs and widened exactly to
 //          f16 with cvt.f16x2.e4m3x2, the q.K k index permuted alike in both operands; f16 MMAs,
 //          the K scale folded into the softmax scale, the V scale into the output.
 
@@ -63,7 +63,7 @@
 namespace pa {
 namespace {
 
-constexpr int kWarps = PA_DECODE_WARPS;
+constexpr int kWarps = PA_DECODE_WARPS;     // warps per CTA, bf16 caches
 constexpr int kStages = PA_DECODE_STAGES;
 constexpr int kHalfBytes = kBlockSize * 128;                // 16 rows x 64 bf16
 constexpr int kQBytes = 8 * kHeadDim * 2;                   // q rows of up to 8 heads
@@ -71,26 +71,28 @@ constexpr int kQBytes = 8 * kHeadDim * 2;                   // q rows of up to 8
 __host__ __device__ inline int prefix_bytes(int num_seqs) { return ((num_seqs + 1) * 4 + 15) & ~15; }
 
 // Shared-memory layout of one kernel variant.  kStep fuses the new token's RoPE + store; kFp8
-// reads E4M3 caches, whose (block, KV head) tiles are 2 KiB instead of 4 KiB, so more stages
-// fit.  Header: the mbarriers (8 bytes each), the int4 job descriptors on a 16-byte boundary,
+// reads E4M3 caches, whose (block, KV head) tiles are 2 KiB instead of 4 KiB: there the CTA
+// runs 12 warps of 2 stages, since its per-job work (widening the codes) is heavier and more
+// independent warps hide it better than deeper rings (measured: 12 x 2 beat 8 x 4 and 8 x 3).  Header: the mbarriers (8 bytes each), the int4 job descriptors on a 16-byte boundary,
 // the prefix of block counts.  Stage: [K tile | V tile | q rows | (kStep) the new token's
 // cos/sin row (fp32), k row and v row (bf16)], a multiple of 1024 bytes so that every tile
 // stays on the 1024-byte boundary its 128-byte swizzle needs.
 template <bool kStep, bool kFp8>
 struct Layout {
   static constexpr int kTile = kFp8 ? kTileBytes / 2 : kTileBytes;
-  static constexpr int kStagesN = kFp8 ? (kStep ? 3 : 4) : kStages;
+  static constexpr int kWarpsN = kFp8 ? 12 : kWarps;
+  static constexpr int kStagesN = kFp8 ? 2 : kStages;
   static constexpr int kQOff = 2 * kTile;
   static constexpr int kCosSinOff = kQOff + kQBytes;
   static constexpr int kNewKOff = kCosSinOff + kHeadDim * 4;
   static constexpr int kNewVOff = kNewKOff + kHeadDim * 2;
   static constexpr int kStage = kStep ? kNewVOff + kHeadDim * 2 : kQOff + kQBytes;
-  static constexpr int kDescOff = (kWarps * kStagesN * 8 + 15) & ~15;
-  static constexpr int kPrefixOff = kDescOff + kWarps * kStagesN * 16;
+  static constexpr int kDescOff = (kWarpsN * kStagesN * 8 + 15) & ~15;
+  static constexpr int kPrefixOff = kDescOff + kWarpsN * kStagesN * 16;
   static_assert(kStage % 1024 == 0 && kTile % 1024 == 0, "tiles on 1024-byte boundaries");
   static_assert(kDescOff % 16 == 0 && kPrefixOff % 16 == 0, "descriptor alignment");
   __host__ __device__ static int smem(int num_seqs) {
-    return kPrefixOff + prefix_bytes(num_seqs) + 1024 + kWarps * kStagesN * kStage;  // + pad
+    return kPrefixOff + prefix_bytes(num_seqs) + 1024 + kWarpsN * kStagesN * kStage;  // + pad
   }
 };
 
@@ -133,10 +135,11 @@ __device__ __forceinline__ int clamp_len(int len, int max_len) {
 }
 
 template <bool kStep, bool kFp8>
-__global__ void __launch_bounds__(kWarps * 32, 1)
+__global__ void __launch_bounds__(Layout<kStep, kFp8>::kWarpsN * 32, 1)
 decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
   using L = Layout<kStep, kFp8>;
+  constexpr int kWarps = L::kWarpsN;           // warps of this variant's CTA
   constexpr int kPool = kWarps * L::kStagesN;  // stages of the CTA
   constexpr int kStageB = L::kStage;
   static_assert(kPool <= kWarps * 32, "one initialising thread per stage");
@@ -853,10 +856,10 @@ cudaError_t persistent_ctas(int* ctas) {
     int sms = 0, per_sm = 0;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kWarps * 32, smem);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, Layout<kStep, kFp8>::kWarpsN * 32, smem);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    cached[dev] = min(sms * per_sm, kMaxDecodeWarps / kWarps);
+    cached[dev] = min(sms * per_sm, kMaxDecodeWarps / Layout<kStep, kFp8>::kWarpsN);
   }
   *ctas = cached[dev];
   return cudaSuccess;
@@ -874,10 +877,11 @@ cudaError_t launch_partition(DecodeArgs& a, const CUtensorMap& tm_k, const CUten
   const long long want = a.chunk_blocks ? (jobs_bound + a.chunk_blocks - 1) / a.chunk_blocks
                                         : (jobs_bound + kMinRangeBlocks - 1) / kMinRangeBlocks;
   const long long ctas = min(static_cast<long long>(max_ctas), want);
-  a.num_warps = static_cast<int>(ctas) * kWarps;
+  constexpr int kWarpsN = Layout<kStep, kFp8>::kWarpsN;
+  a.num_warps = static_cast<int>(ctas) * kWarpsN;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas));
-  cfg.blockDim = dim3(kWarps * 32);
+  cfg.blockDim = dim3(kWarpsN * 32);
   cfg.dynamicSmemBytes = Layout<kStep, kFp8>::smem(a.num_seqs);
   cfg.stream = stream;
   cfg.attrs = const_cast<cudaLaunchAttribute*>(attr);
