@@ -702,12 +702,14 @@ def run_reference(args, world):
     value = nbytes / dt / 1e9
     sample = (f"fp64 oracle RoPE+store and decode of the first {n} of {w.num_seqs} sequences x "
               f"{w.num_layers} layer(s) per step, on {cores} host threads")
+    cfg = config_of(w, None, world)
+    cfg["l2"] = "not flushed (host cores)"
     return {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * dt / max(1, args.steps), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "impl": "reference", "config": config_of(w, None, world),
+        "impl": "reference", "config": cfg,
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
