@@ -729,8 +729,9 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
 // dependents launch and does everything that needs no partial result first: where the
 // segment's pieces are comes from N_s and N_S, computed from the sequence lengths (inputs of
 // the partition kernel, not outputs).  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
-// Empty sequences get zeros.
-constexpr int kMergeWarps = 8;
+// Empty sequences get zeros.  CTAs have 8 warps beside the bf16 partition kernel and 4 beside
+// the 12-warp E4M3 one, so that at least one fits next to it (registers).
+constexpr int kMergeWarps = 8;   // most warps per CTA
 constexpr int kMergeSplit = 4;   // warps per (sequence, query head)
 constexpr int kMergeBatch = 32;  // pieces loaded per round trip
 
@@ -745,7 +746,7 @@ __device__ __forceinline__ void wait_then_release() {
 
 __global__ void __launch_bounds__(kMergeWarps * 32, 2) decode_merge_kernel(const DecodeArgs a) {
   const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  const int gw = blockIdx.x * static_cast<int>(blockDim.x >> 5) + static_cast<int>(threadIdx.x >> 5);
   const int w = gw / kMergeSplit;                  // (sequence, query head)
   const int quarter = gw - w * kMergeSplit;        // dims 32 quarter .. 32 quarter + 31
   const int S = a.num_seqs;
@@ -966,9 +967,10 @@ cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
 
   const long long merge_warps = static_cast<long long>(a.num_seqs) * a.num_q_heads * kMergeSplit;
+  const int per_cta = fp8 ? kMergeWarps / 2 : kMergeWarps;
   cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(static_cast<unsigned>((merge_warps + kMergeWarps - 1) / kMergeWarps));
-  mcfg.blockDim = dim3(kMergeWarps * 32);
+  mcfg.gridDim = dim3(static_cast<unsigned>((merge_warps + per_cta - 1) / per_cta));
+  mcfg.blockDim = dim3(per_cta * 32);
   mcfg.stream = stream;
   mcfg.attrs = attr;
   mcfg.numAttrs = 1;
