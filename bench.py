@@ -28,7 +28,8 @@ The printed JSON line carries:
   fp8_kv               the step's decode on E4M3 caches (pa_decode_fp8, pa_decode_step_fp8),
                        bandwidth counted on the E4M3 bytes (--no-fp8 skips it);
   prefill              pa_prefill on two prefill workloads, TFLOP/s against the measured bf16
-                       dense peak (--no-prefill skips it);
+                       dense peak, and pa_rope_kv_store of their new tokens against the HBM
+                       copy bandwidth (--no-prefill skips it);
   block_ops            pa_copy_blocks over K and V of 28 layers: copy-on-write inside the
                        device pools, swap out / in of a 2048-token sequence to page-locked
                        host pools, beside a plain memcpy of the same bytes (--no-block-ops
@@ -512,7 +513,39 @@ def prefill_runs(torch, binding, timed_loop, steps):
                      "roofline": {"bound": "tensor", "peak": peak, "peak_kind": f"{kind} bf16_tflops",
                                   "unit": "TFLOP/s", "frac": round(tf / peak, 4)},
                      "new_tokens_per_s": round(w.num_tokens / (ms * 1e-3), 1)}
+        res[name]["rope_kv_store"] = prefill_store(torch, binding, timed_loop, steps, w, kc, vc, bt)
     return res
+
+
+def prefill_store(torch, binding, timed_loop, steps, w, kc, vc, bt):
+    """pa_rope_kv_store of a prefill workload's new tokens (their k and v drawn from a seeded
+    generator, each at its position ctx - n + i and that position's slot), timed after the
+    prefill runs: bytes = q read and written, k and v read and written to the caches, one
+    cos/sin row read, per token, over the measured HBM copy bandwidth."""
+    dev = torch.device("cuda")
+    T, Hq, D = w.q.shape
+    Hkv = kc.shape[1]
+    pos = np.concatenate([np.arange(w.context_lens[s] - (w.q_start[s + 1] - w.q_start[s]),
+                                    w.context_lens[s]) for s in range(w.num_seqs)]).astype(np.int32)
+    seq = np.repeat(np.arange(w.num_seqs), np.diff(w.q_start))
+    slots = w.block_tables[seq, pos // W.BLOCK_SIZE].astype(np.int64) * W.BLOCK_SIZE + pos % W.BLOCK_SIZE
+    gen = torch.Generator(device="cpu").manual_seed(0x244)
+    q = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).view(torch.bfloat16).to(dev)
+    k = torch.randn(T, Hkv, D, generator=gen).to(torch.bfloat16).to(dev)
+    v = torch.randn(T, Hkv, D, generator=gen).to(torch.bfloat16).to(dev)
+    cs = torch.from_numpy(W.rope_cos_sin_table(int(w.max_context_len))).to(dev)
+    pos_d, slots_d = torch.from_numpy(pos).to(dev), torch.from_numpy(slots).to(dev)
+    call = lambda: binding.rope_kv_store(q, k, v, pos_d, cs, slots_d, kc, vc)
+    call()
+    ms = float(np.mean(timed_loop(call, steps)))
+    rc, flags = binding.get_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after pa_rope_kv_store: {rc} flags {flags:#x}")
+    nbytes = T * ((2 * Hq + 4 * Hkv) * D * 2 + D * 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, _ = hbm_peak()
+    return {"tokens": int(T), "us": round(ms * 1e3, 2), "bytes": int(nbytes), "GB/s": round(gbs, 1),
+            "frac_of_hbm_copy_peak": round(gbs / peak, 4)}
 
 
 def reduce_over_ranks(maxes, sums, dist, device):
