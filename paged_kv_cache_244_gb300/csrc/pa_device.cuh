@@ -222,16 +222,28 @@ __device__ __forceinline__ uint16_t e4m3x2_of(uint32_t bf16_pair, float inv) {
   return r;
 }
 
+// a b - c d in fp32 with the rounding error of c d recovered by an FMA (the compensated
+// difference of products: w = c d rounded, e = w - c d exactly, result (a b - w) + e).  Within
+// about two fp32 ulps of the exact value even when a b and c d nearly cancel, where the plain
+// fma(a, b, -c d) can be off by many bf16 ulps of the (tiny) result.
+__device__ __forceinline__ float diff_of_products(float a, float b, float c, float d) {
+  const float w = __fmul_rn(c, d);
+  const float e = __fmaf_rn(-c, d, w);
+  const float f = __fmaf_rn(a, b, -w);
+  return __fadd_rn(f, e);
+}
+
 // rotate_half RoPE of two adjacent rotation pairs: lo holds x[i], x[i+1], hi holds x[i+64],
-// x[i+65] (bf16), c and s the cos and sin of angles i and i+1.  In fp32, rounded to bf16 RNE:
+// x[i+65] (bf16), c and s the cos and sin of angles i and i+1.  In fp32 (compensated, above),
+// rounded to bf16 RNE:
 //   x'[i] = x[i] c - x[i+64] s,   x'[i+64] = x[i+64] c + x[i] s.
 // Every kernel that rotates goes through this one function, so they all agree bit for bit.
 __device__ __forceinline__ void rope_rotate_pairs(uint32_t& lo, uint32_t& hi, float2 c, float2 s) {
   const float x0 = bf16lo(lo), x1 = bf16hi(lo), y0 = bf16lo(hi), y1 = bf16hi(hi);
-  const float r0 = __fmaf_rn(x0, c.x, -__fmul_rn(y0, s.x));
-  const float r1 = __fmaf_rn(x1, c.y, -__fmul_rn(y1, s.y));
-  const float r2 = __fmaf_rn(y0, c.x, __fmul_rn(x0, s.x));
-  const float r3 = __fmaf_rn(y1, c.y, __fmul_rn(x1, s.y));
+  const float r0 = diff_of_products(x0, c.x, y0, s.x);
+  const float r1 = diff_of_products(x1, c.y, y1, s.y);
+  const float r2 = diff_of_products(y0, c.x, -x0, s.x);
+  const float r3 = diff_of_products(y1, c.y, -x1, s.y);
   lo = pack_bf16x2(r0, r1);
   hi = pack_bf16x2(r2, r3);
 }
