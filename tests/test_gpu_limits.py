@@ -1,8 +1,9 @@
-"""The decode entry points at the limits pa.h states, against the fp64 oracle.
+"""The entry points at the limits pa.h states, against the fp64 oracle.
 
 - 8,192 sequences in one call: the block-count prefix fills its shared-memory area, in the
   bf16 and E4M3 layouts and in the fused step.
 - Many KV heads, up to the 4,096 allowed: the KV head index travels packed in a job word.
+- pa_copy_blocks over the most caches one call takes (256: K and V of 128 layers).
 Bars as everywhere: output within 1e-2 + 1e-2 |oracle|, V stores bit-exact, K within 1 ulp.
 """
 
@@ -91,4 +92,22 @@ def test_many_kv_heads(pa, orc, hq, hkv):
     assert np.array_equal(host_bits(e.v_cache), vc)
     assert bf16_ulp_distance(host_bits(e.k_cache), kc).max() <= 1
     assert_out_close(host_bits(got), ref, f"step {hq}/{hkv}")
+    check_status_clean(pa)
+
+
+def test_copy_blocks_most_caches(pa, orc):
+    """256 caches of 24 blocks, 10 copy-on-write pairs: every pool as the oracle's copy."""
+    rng = np.random.default_rng(256)
+    pools = [rng.integers(0, 1 << 16, (24, 2, W.BLOCK_SIZE, W.HEAD_DIM), dtype=np.uint16)
+             for _ in range(pa.PA_MAX_BLOCK_CACHES)]
+    frm = rng.permutation(12)[:10]
+    to = 12 + rng.permutation(12)[:10]
+    pairs = np.stack([frm, to], axis=1).astype(np.int64)
+    want = [p.copy() for p in pools]
+    assert orc.copy_blocks(want, want, pairs) == 0
+    devp = [torch.from_numpy(p.view(np.int16)).view(torch.bfloat16).cuda() for p in pools]
+    pa.copy_blocks(devp, devp, torch.from_numpy(pairs).cuda())
+    torch.cuda.synchronize()
+    for c in range(len(pools)):
+        assert np.array_equal(devp[c].view(torch.int16).cpu().numpy().view(np.uint16), want[c]), c
     check_status_clean(pa)
