@@ -12,10 +12,12 @@
 // CTA = (sequence, KV head g, tile of 16 query tokens), one warp per query head of the group
 // (G <= 8 warps), so every K/V tile brought in is used by all G heads.  Each warp holds its
 // 16 x 128 Q tile as MMA A fragments and walks the key blocks 0 .. p_last / 16:
-//   S (16 x 64) = Q K^T      64 mma.sync m16n8k16 (bf16 -> fp32), B = K via ldmatrix
-//   online softmax           per row, in the log2 domain; causal mask t > p_i; V rows past
-//                            the context zeroed in the operand (they may hold anything)
-//   O (16 x 128) += P V      64 MMAs; P is the S accumulators rounded to bf16 (the C layout of
+//   S (16 x 48) = Q K^T      48 mma.sync m16n8k16 (bf16 -> fp32), B = K via ldmatrix
+//   online softmax           per row, in the log2 domain, the scale folded into one FMA per
+//                            exponent; causal mask t > p_i only on the stages that reach the
+//                            tile's diagonal; V rows past the context zeroed in the operand
+//                            (they may hold anything), in the context's last block only
+//   O (16 x 128) += P V      48 MMAs; P is the S accumulators rounded to bf16 (the C layout of
 //                            two n8 tiles is the A layout of one k16 step), B = V via
 //                            transposing ldmatrix
 // Keys come 48 at a time (3 blocks) through a 3-stage ring, so the softmax bookkeeping and the
@@ -47,6 +49,14 @@ constexpr int kPfQBytes = kQTile * kHeadDim * 2;    // one warp's Q tile: 4 KiB
 // header: full[2], empty[2] mbarriers, block-present masks; then 1024-aligned stages, Q tiles
 constexpr int kPfHeader = 1024;
 constexpr int kPfSmem = kPfHeader + kPfStages * kPfStageBytes + kPfMaxWarps * kPfQBytes + 1024;
+
+// 2^x on the special-function unit (ex2.approx, subnormal results flushed to zero).  Every
+// argument here is <= 0 (a score minus its row maximum) and each result is rounded to bf16.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __global__ void __maxnreg__(168)  // two CTAs of up to 6 warps per SM; 8 warps still fit one
 prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -193,17 +203,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         mma_bf16_16816(sc[2 * i + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
       }
     }
-    // scale; causal mask and missing blocks -> -inf.  sc[nt]: [0] (row gq, key 8nt+2cq),
-    // [1] (gq, +1), [2] (gq+8, 8nt+2cq), [3] (gq+8, +1)
-    const int tbase = kKB * kBlockSize * j + 2 * cq;
+    // Scores stay unscaled until the exponent (scale > 0, so the row maxima are the same).
+    // Causal mask and missing blocks -> -inf, only on a stage that reaches past the tile's first
+    // query or lacks a block; the others lie wholly before every query of the tile.
+    // sc[nt]: [0] (row gq, key 8nt+2cq), [1] (gq, +1), [2] (gq+8, 8nt+2cq), [3] (gq+8, +1)
+    if (mask != (1 << kKB) - 1 || kKB * kBlockSize * (j + 1) - 1 > pos0) {
+      const int tbase = kKB * kBlockSize * j + 2 * cq;
 #pragma unroll
-    for (int nt = 0; nt < 2 * kKB; ++nt) {
-      const bool here = (mask >> (nt >> 1)) & 1;
+      for (int nt = 0; nt < 2 * kKB; ++nt) {
+        const bool here = (mask >> (nt >> 1)) & 1;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = tbase + 8 * nt + e;
-        sc[nt][e] = here && t <= p0 ? sc[nt][e] * a.scale_log2 : -INFINITY;
-        sc[nt][2 + e] = here && t <= p1 ? sc[nt][2 + e] * a.scale_log2 : -INFINITY;
+        for (int e = 0; e < 2; ++e) {
+          const int t = tbase + 8 * nt + e;
+          if (!(here && t <= p0)) sc[nt][e] = -INFINITY;
+          if (!(here && t <= p1)) sc[nt][2 + e] = -INFINITY;
+        }
       }
     }
     float bm0 = -INFINITY, bm1 = -INFINITY;
@@ -217,23 +231,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       bm0 = fmaxf(bm0, __shfl_xor_sync(kFullMask, bm0, x));
       bm1 = fmaxf(bm1, __shfl_xor_sync(kFullMask, bm1, x));
     }
-    const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+    // running maxima m0, m1 in the log2 domain (scale * log2(e) applied)
+    const float mn0 = fmaxf(m0, bm0 * a.scale_log2), mn1 = fmaxf(m1, bm1 * a.scale_log2);
     // a row with no key yet keeps the shift 0 (only rows past the tile can stay that way)
     const float sh0 = mn0 == -INFINITY ? 0.f : mn0;
     const float sh1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = exp2f(m0 - sh0), al1 = exp2f(m1 - sh1);
+    const float al0 = ex2_ftz(m0 - sh0), al1 = ex2_ftz(m1 - sh1);
     m0 = mn0;
     m1 = mn1;
-    // P rounded to bf16 (the MMA operand), as A fragments of one k16 step per block; the
-    // running sums add the same rounded values
+    // P = 2^(scale_log2 * s - shift), one FMA and one exp2 per score, rounded to bf16 (the MMA
+    // operand) as A fragments of one k16 step per block; the running sums add the same
+    // rounded values
+    const float sl = a.scale_log2;
     uint32_t pa[kKB][4];
     float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
     for (int i = 0; i < kKB; ++i) {
-      pa[i][0] = pack_bf16x2(exp2f(sc[2 * i][0] - sh0), exp2f(sc[2 * i][1] - sh0));
-      pa[i][1] = pack_bf16x2(exp2f(sc[2 * i][2] - sh1), exp2f(sc[2 * i][3] - sh1));
-      pa[i][2] = pack_bf16x2(exp2f(sc[2 * i + 1][0] - sh0), exp2f(sc[2 * i + 1][1] - sh0));
-      pa[i][3] = pack_bf16x2(exp2f(sc[2 * i + 1][2] - sh1), exp2f(sc[2 * i + 1][3] - sh1));
+      pa[i][0] = pack_bf16x2(ex2_ftz(fmaf(sc[2 * i][0], sl, -sh0)), ex2_ftz(fmaf(sc[2 * i][1], sl, -sh0)));
+      pa[i][1] = pack_bf16x2(ex2_ftz(fmaf(sc[2 * i][2], sl, -sh1)), ex2_ftz(fmaf(sc[2 * i][3], sl, -sh1)));
+      pa[i][2] = pack_bf16x2(ex2_ftz(fmaf(sc[2 * i + 1][0], sl, -sh0)), ex2_ftz(fmaf(sc[2 * i + 1][1], sl, -sh0)));
+      pa[i][3] = pack_bf16x2(ex2_ftz(fmaf(sc[2 * i + 1][2], sl, -sh1)), ex2_ftz(fmaf(sc[2 * i + 1][3], sl, -sh1)));
       ps0 += bf16lo(pa[i][0]) + bf16hi(pa[i][0]) + bf16lo(pa[i][2]) + bf16hi(pa[i][2]);
       ps1 += bf16lo(pa[i][1]) + bf16hi(pa[i][1]) + bf16lo(pa[i][3]) + bf16hi(pa[i][3]);
     }
@@ -249,17 +266,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       }
     }
     // O += P V, block by block; two n8 dim tiles per transposing ldmatrix
-#pragma unroll
-    for (int i = 0; i < kKB; ++i) {
-      if (!(mask & (1 << i))) continue;
+    auto pv = [&](int i, uint32_t vm_lo, uint32_t vm_hi) {
       const uint32_t vt = stage + i * kPfBlockBytes + 2 * kPfHalf;
-      // keys past the context may hold anything (even NaN): zero their V rows in the operand
-      const int valid = ctx - kBlockSize * (kKB * j + i);
-      uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-      if (valid < kBlockSize) {
-        vm_lo = (2 * cq < valid ? 0x0000ffffu : 0u) | (2 * cq + 1 < valid ? 0xffff0000u : 0u);
-        vm_hi = (2 * cq + 8 < valid ? 0x0000ffffu : 0u) | (2 * cq + 9 < valid ? 0xffff0000u : 0u);
-      }
 #pragma unroll
       for (int d2 = 0; d2 < 8; ++d2) {
         uint32_t v0, v1, v2, v3;
@@ -268,6 +276,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         ldsm_x4_trans(vt + (d2 >> 2) * kPfHalf + key * 128 + ((chunk ^ r) << 4), v0, v1, v2, v3);
         mma_bf16_16816(o[2 * d2], pa[i][0], pa[i][1], pa[i][2], pa[i][3], v0 & vm_lo, v1 & vm_hi);
         mma_bf16_16816(o[2 * d2 + 1], pa[i][0], pa[i][1], pa[i][2], pa[i][3], v2 & vm_lo, v3 & vm_hi);
+      }
+    };
+#pragma unroll
+    for (int i = 0; i < kKB; ++i) {
+      if (!(mask & (1 << i))) continue;
+      const int valid = ctx - kBlockSize * (kKB * j + i);
+      if (valid >= kBlockSize) {
+        pv(i, 0xffffffffu, 0xffffffffu);
+      } else {
+        // keys past the context may hold anything (even NaN): zero their V rows in the operand
+        pv(i, (2 * cq < valid ? 0x0000ffffu : 0u) | (2 * cq + 1 < valid ? 0xffff0000u : 0u),
+           (2 * cq + 8 < valid ? 0x0000ffffu : 0u) | (2 * cq + 9 < valid ? 0xffff0000u : 0u));
       }
     }
     // release the stage; thread 0 refills it once every warp has
