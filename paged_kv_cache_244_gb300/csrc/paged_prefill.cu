@@ -12,20 +12,20 @@
 // CTA = (sequence, KV head g, tile of 16 query tokens), one warp per query head of the group
 // (G <= 8 warps), so every K/V tile brought in is used by all G heads.  Each warp holds its
 // 16 x 128 Q tile as MMA A fragments and walks the key blocks 0 .. p_last / 16:
-//   S (16 x 48) = Q K^T      48 mma.sync m16n8k16 (bf16 -> fp32), B = K via ldmatrix
+//   S (16 x 64) = Q K^T      64 mma.sync m16n8k16 (bf16 -> fp32), B = K via ldmatrix
 //   online softmax           per row, in the log2 domain, the scale folded into one FMA per
 //                            exponent; causal mask t > p_i only on the stages that reach the
 //                            tile's diagonal; V rows past the context zeroed in the operand
 //                            (they may hold anything), in the context's last block only
-//   O (16 x 128) += P V      48 MMAs; P is the S accumulators rounded to bf16 (the C layout of
+//   O (16 x 128) += P V      64 MMAs; P is the S accumulators rounded to bf16 (the C layout of
 //                            two n8 tiles is the A layout of one k16 step), B = V via
 //                            transposing ldmatrix
-// Keys come 48 at a time (3 blocks) through a 3-stage ring, so the softmax bookkeeping and the
-// barrier handshakes are paid once per 96 MMAs: thread 0 issues the TMA tensor loads of stage
-// j + 3 (one box per K tile and per V tile, landing as two 64-column halves, 128-byte swizzle)
-// once every warp has released stage j (an mbarrier with one arrival per warp).  Three stages
-// of 48 keys measured 2% faster than two of 64 (more slack between the warps, and no register
-// spill) and four of 32 slower.  All waits are bounded.
+// Keys come 64 at a time (4 blocks) through a 2-stage ring, so the softmax bookkeeping and the
+// handshakes are paid once per 128 MMAs: the warp whose release of stage j is the last of the
+// G (a shared-memory count) issues at once the TMA tensor loads of stage j + 2 (one box per K
+// tile and per V tile, landing as two 64-column halves, 128-byte swizzle), so no warp waits
+// for the others.  Measured against 3 stages of 48 keys, 2 of 64 are 1-2% faster; 4 of 32
+// were slower.  All waits are bounded.
 // Tiles are scheduled latest first: the last tiles of a sequence see the most keys.
 
 #include <mutex>
@@ -39,14 +39,15 @@ namespace pa {
 namespace {
 
 constexpr int kQTile = 16;                          // query tokens per CTA
-constexpr int kKB = 3;                              // key blocks (16 tokens each) per stage
-constexpr int kPfStages = 3;
+constexpr int kKB = 4;                              // key blocks (16 tokens each) per stage
+constexpr int kPfStages = 2;
 constexpr int kPfMaxWarps = 8;                      // G <= 8
 constexpr int kPfHalf = kBlockSize * 128;           // 16 rows x 64 bf16
 constexpr int kPfBlockBytes = 2 * kTileBytes;       // K tile + V tile of one key block
-constexpr int kPfStageBytes = kKB * kPfBlockBytes;  // 24 KiB
+constexpr int kPfStageBytes = kKB * kPfBlockBytes;  // 32 KiB
 constexpr int kPfQBytes = kQTile * kHeadDim * 2;    // one warp's Q tile: 4 KiB
-// header: full[2], empty[2] mbarriers, block-present masks; then 1024-aligned stages, Q tiles
+// header: per stage a full mbarrier, a block-present mask and a release count; then the
+// 1024-aligned stages and the Q tiles
 constexpr int kPfHeader = 1024;
 constexpr int kPfSmem = kPfHeader + kPfStages * kPfStageBytes + kPfMaxWarps * kPfQBytes + 1024;
 
@@ -90,14 +91,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t full = raw;                        // kPfStages x 8 bytes
-  const uint32_t empty = raw + 8 * kPfStages;
-  int* present = reinterpret_cast<int*>(smem_raw + 16 * kPfStages);  // bit i: block i loaded
+  int* present = reinterpret_cast<int*>(smem_raw + 8 * kPfStages);   // bit i: block i loaded
+  // per stage: releases so far, G a round; the release that completes a round refills it
+  unsigned* released = reinterpret_cast<unsigned*>(smem_raw + 12 * kPfStages);
   const uint32_t stages = (raw + kPfHeader + 1023u) & ~1023u;
   const uint32_t qtiles = stages + kPfStages * kPfStageBytes;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPfStages; ++i) {
       mbar_init(full + 8 * i, 1);
-      mbar_init(empty + 8 * i, static_cast<uint32_t>(G));
+      released[i] = 0u;
     }
     fence_mbar_init();
     prefetch_tensor_map(&tm_k);
@@ -105,7 +107,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   }
   __syncthreads();
 
-  // Thread 0 brings key blocks kKB j .. kKB j + kKB - 1 into stage j % kPfStages.
+  // Bring key blocks kKB j .. kKB j + kKB - 1 into stage j % kPfStages (one thread).
   const int32_t* bt_row = a.block_tables + static_cast<size_t>(s) * a.max_blocks;
   auto issue = [&](int j) {
     const int st = j % kPfStages;
@@ -136,9 +138,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       mbar_arrive(bar);
     }
   };
-  int issued = 0;
   if (threadIdx.x == 0)
-    for (; issued < min(kPfStages, nst); ++issued) issue(issued);
+    for (int j = 0; j < min(kPfStages, nst); ++j) issue(j);
 
   // ---- this warp's Q tile (query head g * G + warp) as A fragments ------------------------
   const int h = g * G + warp;
@@ -290,22 +291,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
            (2 * cq + 8 < valid ? 0x0000ffffu : 0u) | (2 * cq + 9 < valid ? 0xffff0000u : 0u));
       }
     }
-    // release the stage; thread 0 refills it once every warp has
+    // Release the stage.  The warp whose release is the G-th of this round refills it at once,
+    // so no warp waits for the others here.
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty + 8 * st);
-    if (threadIdx.x == 0 && issued < nst) {
-      if (!mbar_wait_bounded(empty + 8 * st, (j / kPfStages) & 1)) {
-        failed = true;
-        break;
+    if (lane == 0) {
+      __threadfence_block();  // this warp's reads of the stage before the refill's writes
+      const unsigned before = atomicAdd(&released[st], 1u);
+      if ((before + 1u) % static_cast<unsigned>(G) == 0u && j + kPfStages < nst) {
+        __threadfence_block();
+        issue(j + kPfStages);
       }
-      issue(issued++);
     }
     __syncwarp();
   }
-  if (failed && lane == 0) raise_flag(a.status, PA_FLAG_TIMEOUT);
-  // Let every copy thread 0 issued land (bounded) before the CTA can exit.
-  if (threadIdx.x == 0)
-    for (int j = seen; j < issued; ++j) mbar_wait_bounded(full + 8 * (j % kPfStages), (j / kPfStages) & 1);
+  if (failed && lane == 0) {
+    raise_flag(a.status, PA_FLAG_TIMEOUT);
+    // Only stages seen .. seen + kPfStages - 1 can have copies in flight (a stage is refilled
+    // after every warp released its previous round, and this warp released none from `seen`
+    // on): let them land (bounded; a stage never refilled gives up after 10 ms) before the
+    // CTA can exit.
+    for (int j = seen; j < min(nst, seen + kPfStages); ++j)
+      mbar_wait_bounded(full + 8 * (j % kPfStages), (j / kPfStages) & 1, 10000000ull);
+  }
   if (failed) return;
 
   // ---- out = O / l for the tile's real rows -----------------------------------------------
