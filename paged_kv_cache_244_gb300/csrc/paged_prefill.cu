@@ -14,9 +14,11 @@
 // 16 x 128 Q tile as MMA A fragments and walks the key blocks 0 .. p_last / 16:
 //   S (16 x 64) = Q K^T      64 mma.sync m16n8k16 (bf16 -> fp32), B = K via ldmatrix
 //   online softmax           per row, in the log2 domain, the scale folded into one FMA per
-//                            exponent; causal mask t > p_i only on the stages that reach the
-//                            tile's diagonal; V rows past the context zeroed in the operand
-//                            (they may hold anything), in the context's last block only
+//                            exponent; a row's shift moves only when its maximum passes it by
+//                            more than 8 (P <= 2^8, few O rescales); causal mask t > p_i only on
+//                            the stages that reach the tile's diagonal; V rows past the context
+//                            zeroed in the operand (they may hold anything), in the context's
+//                            last block only
 //   O (16 x 128) += P V      64 MMAs; P is the S accumulators rounded to bf16 (the C layout of
 //                            two n8 tiles is the A layout of one k16 step), B = V via
 //                            transposing ldmatrix
@@ -186,20 +188,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     seen = j + 1;
     const int mask = present[st];
     const uint32_t stage = stages + st * kPfStageBytes;
-    // S = Q K^T for the stage's 16 kKB keys: n8 tile 2i (+1) = keys 0-7 (8-15) of block i
+    // S = Q K^T for the stage's 16 kKB keys: n8 tile 2i (+1) = keys 0-7 (8-15) of block i.
+    // k steps outside, blocks inside: 2 kKB independent accumulator chains between two MMAs
+    // of one chain (the MMAs issue in program order).
     float sc[2 * kKB][4];
 #pragma unroll
     for (int nt = 0; nt < 2 * kKB; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    const int key = r + 8 * (mi >> 1);
 #pragma unroll
-    for (int i = 0; i < kKB; ++i) {
-      if (!(mask & (1 << i))) continue;
-      const uint32_t kt = stage + i * kPfBlockBytes;
+    for (int kk = 0; kk < 8; ++kk) {
+      const int chunk = (2 * kk + (mi & 1)) & 7;
+      const uint32_t ko = (kk >> 2) * kPfHalf + key * 128 + ((chunk ^ r) << 4);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int i = 0; i < kKB; ++i) {
+        if (!(mask & (1 << i))) continue;
         uint32_t b0, b1, b2, b3;
-        const int key = r + 8 * (mi >> 1);
-        const int chunk = (2 * kk + (mi & 1)) & 7;
-        ldsm_x4(kt + (kk >> 2) * kPfHalf + key * 128 + ((chunk ^ r) << 4), b0, b1, b2, b3);
+        ldsm_x4(stage + i * kPfBlockBytes + ko, b0, b1, b2, b3);
         mma_bf16_16816(sc[2 * i], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
         mma_bf16_16816(sc[2 * i + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
       }
@@ -232,8 +236,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       bm0 = fmaxf(bm0, __shfl_xor_sync(kFullMask, bm0, x));
       bm1 = fmaxf(bm1, __shfl_xor_sync(kFullMask, bm1, x));
     }
-    // running maxima m0, m1 in the log2 domain (scale * log2(e) applied)
-    const float mn0 = fmaxf(m0, bm0 * a.scale_log2), mn1 = fmaxf(m1, bm1 * a.scale_log2);
+    // Shifts m0, m1 in the log2 domain (scale * log2(e) applied): a row's shift moves to its
+    // maximum only when that exceeds it by more than 8, so P stays at most 2^8 and O is rescaled
+    // far less often.
+    const float bs0 = bm0 * a.scale_log2, bs1 = bm1 * a.scale_log2;
+    const float mn0 = bs0 > m0 + 8.f ? bs0 : m0, mn1 = bs1 > m1 + 8.f ? bs1 : m1;
     // a row with no key yet keeps the shift 0 (only rows past the tile can stay that way)
     const float sh0 = mn0 == -INFINITY ? 0.f : mn0;
     const float sh1 = mn1 == -INFINITY ? 0.f : mn1;
