@@ -512,17 +512,15 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
           ldsm_x4(kt + (kk >> 2) * kHalfBytes + k_row + ((chunk ^ r) << 4), a0, a1, a2, a3);
           mma_bf16_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) sc[i] *= a.scale_log2;
       }
-      // sc: [0] = (token gq, head 2cq), [1] = (gq, 2cq+1), [2] = (gq+8, 2cq), [3] = (gq+8, 2cq+1)
-      uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
-      if (valid < kBlockSize) {
+      // sc: [0] = (token gq, head 2cq), [1] = (gq, 2cq+1), [2] = (gq+8, 2cq), [3] = (gq+8, 2cq+1).
+      // bf16 caches: the scores stay unscaled until the exponent (scale > 0, so the maxima are
+      // the same) and each exponent is one FMA; E4M3 caches: already scaled above.
+      const float fold = kFp8 ? 1.f : a.scale_log2;
+      const bool partial = valid < kBlockSize;
+      if (partial) {
         if (gq >= valid) sc[0] = sc[1] = -INFINITY;
         if (gq + 8 >= valid) sc[2] = sc[3] = -INFINITY;
-        // V rows past the context may hold anything (even NaN): zero them in the operand.
-        vmask_lo = (2 * cq < valid ? 0x0000ffffu : 0u) | (2 * cq + 1 < valid ? 0xffff0000u : 0u);
-        vmask_hi = (2 * cq + 8 < valid ? 0x0000ffffu : 0u) | (2 * cq + 9 < valid ? 0xffff0000u : 0u);
       }
       float bm0 = fmaxf(sc[0], sc[2]);
       float bm1 = fmaxf(sc[1], sc[3]);
@@ -531,23 +529,28 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
         bm0 = fmaxf(bm0, __shfl_xor_sync(kFullMask, bm0, x));
         bm1 = fmaxf(bm1, __shfl_xor_sync(kFullMask, bm1, x));
       }
-      const float mn0 = fmaxf(m0, bm0);
-      const float mn1 = fmaxf(m1, bm1);
-      const float al0 = exp2f(m0 - mn0);
-      const float al1 = exp2f(m1 - mn1);
+      // Shifts m0, m1 in the log2 domain: a head's shift moves to its maximum only when that
+      // passes it by more than 8, so P stays at most 2^8 and O is rescaled far less often.
+      const float bs0 = bm0 * fold, bs1 = bm1 * fold;
+      const float mn0 = bs0 > m0 + 8.f ? bs0 : m0;
+      const float mn1 = bs1 > m1 + 8.f ? bs1 : m1;
+      const float al0 = ex2_ftz(m0 - mn0);
+      const float al1 = ex2_ftz(m1 - mn1);
       m0 = mn0;
       m1 = mn1;
       // P rounded to the MMA operand type (bf16, or f16 with E4M3 caches); the running sums
       // add the same rounded values.
+      const float e0 = ex2_ftz(fmaf(sc[0], fold, -mn0)), e1 = ex2_ftz(fmaf(sc[1], fold, -mn1));  // token gq
+      const float e2 = ex2_ftz(fmaf(sc[2], fold, -mn0)), e3 = ex2_ftz(fmaf(sc[3], fold, -mn1));  // token gq+8
       uint32_t p_lo, p_hi;
       if constexpr (kFp8) {
-        p_lo = pack_f16x2(exp2f(sc[0] - mn0), exp2f(sc[1] - mn1));  // token gq
-        p_hi = pack_f16x2(exp2f(sc[2] - mn0), exp2f(sc[3] - mn1));  // token gq+8
+        p_lo = pack_f16x2(e0, e1);
+        p_hi = pack_f16x2(e2, e3);
         l0 = fmaf(l0, al0, f16lo(p_lo) + f16lo(p_hi));
         l1 = fmaf(l1, al1, f16hi(p_lo) + f16hi(p_hi));
       } else {
-        p_lo = pack_bf16x2(exp2f(sc[0] - mn0), exp2f(sc[1] - mn1));  // token gq
-        p_hi = pack_bf16x2(exp2f(sc[2] - mn0), exp2f(sc[3] - mn1));  // token gq+8
+        p_lo = pack_bf16x2(e0, e1);
+        p_hi = pack_bf16x2(e2, e3);
         l0 = fmaf(l0, al0, bf16lo(p_lo) + bf16lo(p_hi));
         l1 = fmaf(l1, al1, bf16hi(p_lo) + bf16hi(p_hi));
       }
@@ -563,34 +566,43 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
           o[mt][3] *= al1;
         }
       }
-      if constexpr (kFp8) {
-        // O^T += V^T P^T.  The transposing ldmatrix of the E4M3 V tile gives lane (gq, cq) the
-        // bytes V[2cq][2gq], V[2cq][2gq+1], V[2cq+1][2gq], V[2cq+1][2gq+1] of one 16-dim chunk:
-        // regrouped by dim and widened they are the A fragments of rows gq (dim 2gq) and gq+8
-        // (dim 2gq+1), k = tokens 2cq, 2cq+1.  So accumulator row gq holds dim 16mt + 2gq and
-        // row gq+8 dim 16mt + 2gq + 1.
+      auto pv = [&](uint32_t vmask_lo, uint32_t vmask_hi) {
+        if constexpr (kFp8) {
+          // O^T += V^T P^T.  The transposing ldmatrix of the E4M3 V tile gives lane (gq, cq)
+          // the bytes V[2cq][2gq], V[2cq][2gq+1], V[2cq+1][2gq], V[2cq+1][2gq+1] of one 16-dim
+          // chunk: regrouped by dim and widened they are the A fragments of rows gq (dim 2gq)
+          // and gq+8 (dim 2gq+1), k = tokens 2cq, 2cq+1.  So accumulator row gq holds dim
+          // 16mt + 2gq and row gq+8 dim 16mt + 2gq + 1.
 #pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) {
-          uint32_t w0, w1, w2, w3;
-          const int chunk = 2 * c2 + k_col;
-          ldsm_x4_trans(vt + k_row + ((chunk ^ r) << 4), w0, w1, w2, w3);
-          uint32_t e0, d0, e1, d1;
-          e4m3x4_pairs_to_f16(w0, e0, d0);  // tokens 2cq, 2cq+1: dims 2gq (e), 2gq+1 (d)
-          e4m3x4_pairs_to_f16(w1, e1, d1);  // tokens 2cq+8, 2cq+9
-          mma_f16_16816(o[2 * c2], e0 & vmask_lo, d0 & vmask_lo, e1 & vmask_hi, d1 & vmask_hi, pb0, pb1);
-          e4m3x4_pairs_to_f16(w2, e0, d0);
-          e4m3x4_pairs_to_f16(w3, e1, d1);
-          mma_f16_16816(o[2 * c2 + 1], e0 & vmask_lo, d0 & vmask_lo, e1 & vmask_hi, d1 & vmask_hi, pb0, pb1);
+          for (int c2 = 0; c2 < 4; ++c2) {
+            uint32_t w0, w1, w2, w3;
+            const int chunk = 2 * c2 + k_col;
+            ldsm_x4_trans(vt + k_row + ((chunk ^ r) << 4), w0, w1, w2, w3);
+            uint32_t x0, y0, x1, y1;
+            e4m3x4_pairs_to_f16(w0, x0, y0);  // tokens 2cq, 2cq+1: dims 2gq (x), 2gq+1 (y)
+            e4m3x4_pairs_to_f16(w1, x1, y1);  // tokens 2cq+8, 2cq+9
+            mma_f16_16816(o[2 * c2], x0 & vmask_lo, y0 & vmask_lo, x1 & vmask_hi, y1 & vmask_hi, pb0, pb1);
+            e4m3x4_pairs_to_f16(w2, x0, y0);
+            e4m3x4_pairs_to_f16(w3, x1, y1);
+            mma_f16_16816(o[2 * c2 + 1], x0 & vmask_lo, y0 & vmask_lo, x1 & vmask_hi, y1 & vmask_hi, pb0, pb1);
+          }
+        } else {
+          // O^T += V^T P^T, one 16-dim slab at a time.
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            uint32_t v0, v1, v2, v3;
+            const int chunk = (2 * mt + v_col) & 7;
+            ldsm_x4_trans(vt + (mt >> 2) * kHalfBytes + v_row + ((chunk ^ r) << 4), v0, v1, v2, v3);
+            mma_bf16_16816(o[mt], v0 & vmask_lo, v1 & vmask_lo, v2 & vmask_hi, v3 & vmask_hi, pb0, pb1);
+          }
         }
+      };
+      if (partial) {
+        // V rows past the context may hold anything (even NaN): zero them in the operand.
+        pv((2 * cq < valid ? 0x0000ffffu : 0u) | (2 * cq + 1 < valid ? 0xffff0000u : 0u),
+           (2 * cq + 8 < valid ? 0x0000ffffu : 0u) | (2 * cq + 9 < valid ? 0xffff0000u : 0u));
       } else {
-        // O^T += V^T P^T, one 16-dim slab at a time.
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          uint32_t v0, v1, v2, v3;
-          const int chunk = (2 * mt + v_col) & 7;
-          ldsm_x4_trans(vt + (mt >> 2) * kHalfBytes + v_row + ((chunk ^ r) << 4), v0, v1, v2, v3);
-          mma_bf16_16816(o[mt], v0 & vmask_lo, v1 & vmask_lo, v2 & vmask_hi, v3 & vmask_hi, pb0, pb1);
-        }
+        pv(0xffffffffu, 0xffffffffu);
       }
     }
     if (fl & kLast) {

@@ -53,14 +53,6 @@ constexpr int kPfQBytes = kQTile * kHeadDim * 2;    // one warp's Q tile: 4 KiB
 constexpr int kPfHeader = 1024;
 constexpr int kPfSmem = kPfHeader + kPfStages * kPfStageBytes + kPfMaxWarps * kPfQBytes + 1024;
 
-// 2^x on the special-function unit (ex2.approx, subnormal results flushed to zero).  Every
-// argument here is <= 0 (a score minus its row maximum) and each result is rounded to bf16.
-__device__ __forceinline__ float ex2_ftz(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 __global__ void __maxnreg__(168)  // two CTAs of up to 6 warps per SM; 8 warps still fit one
 prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const PrefillArgs a) {
