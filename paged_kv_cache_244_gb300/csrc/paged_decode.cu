@@ -483,7 +483,7 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
         __syncwarp();
       }
       // S^T = K q^T: rows = tokens, columns = heads.
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      float sc[4] = {0.f, 0.f, 0.f, 0.f}, sc2[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (kFp8) {
         // E4M3 K tile: ldmatrix reads it as 16-bit pairs, so lane (gq, cq) of matrix (rows
         // 8h..8h+7, 16-byte chunk c) gets dims 16c + 4cq .. +3 of token 8h + gq.  Widened to two
@@ -510,8 +510,11 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
           uint32_t a0, a1, a2, a3;
           const int chunk = (2 * kk + k_col) & 7;
           ldsm_x4(kt + (kk >> 2) * kHalfBytes + k_row + ((chunk ^ r) << 4), a0, a1, a2, a3);
-          mma_bf16_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+          // two accumulator chains (even / odd k steps): the MMAs issue in program order
+          mma_bf16_16816((kk & 1) ? sc2 : sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sc[i] += sc2[i];
       }
       // sc: [0] = (token gq, head 2cq), [1] = (gq, 2cq+1), [2] = (gq+8, 2cq), [3] = (gq+8, 2cq+1).
       // bf16 caches: the scores stay unscaled until the exponent (scale > 0, so the maxima are
