@@ -64,7 +64,7 @@ METRIC = "paged GQA decode: KV-cache HBM GB/s (% of GB300 peak) and attention to
 # the step form and a hash of the CUDA sources it was taken on: once a kernel changes, the
 # hash no longer matches and roofline.traffic is reported as null until it is captured again.
 MEASURED_TRAFFIC = {
-    ("mix64", "fused", "e1ad90bc142fc43c"): 122117120 + 3360768 + 4185344,
+    ("mix64", "fused", "dfd3aa72056c7f5a"): 122116096 + 3210240 + 4185600,
 }
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
