@@ -28,7 +28,8 @@
 // tile and per V tile, landing as two 64-column halves, 128-byte swizzle), so no warp waits
 // for the others.  Measured against 3 stages of 48 keys, 2 of 64 are 1-2% faster; 4 of 32
 // were slower.  All waits are bounded.
-// Tiles are scheduled latest first: the last tiles of a sequence see the most keys.
+// Tiles are scheduled latest first over the whole grid: the last tiles of a sequence see the
+// most keys.
 
 #include <mutex>
 
@@ -61,9 +62,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const int lane = threadIdx.x & 31;
   const int Hkv = a.num_kv_heads;
   const int G = a.num_q_heads / Hkv;
-  const int s = blockIdx.y / Hkv;
-  const int g = blockIdx.y - s * Hkv;
-  const int tile = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // latest first
+  // CTAs start in the order of their linear index (x fastest).  Consecutive indices take the
+  // same query tile of every (sequence, KV head) pair, latest tile first, so the CTAs with the
+  // most keys start first across the whole grid and the last wave holds the cheapest ones.
+  const unsigned long long pairs = gridDim.y;  // sequences x KV heads
+  const unsigned long long lin = static_cast<unsigned long long>(blockIdx.y) * gridDim.x + blockIdx.x;
+  const int sg = static_cast<int>(lin % pairs);
+  const int tile = static_cast<int>(gridDim.x) - 1 - static_cast<int>(lin / pairs);
+  const int s = sg / Hkv;
+  const int g = sg - s * Hkv;
   pdl_wait_prior_grid();
   pdl_allow_next_grid();
 
