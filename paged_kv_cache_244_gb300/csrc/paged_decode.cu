@@ -26,14 +26,17 @@
 //              the q rows;
 //   consumer   waits on the stage (bounded), on a first block loads q^T fragments from the
 //              stage and resets the softmax state, computes S^T = K q^T (16 tokens x 8 head
-//              columns) with 8 m16n8k16 bf16 MMAs (A = K via ldmatrix), updates the online
-//              softmax in the log2 domain (scale * log2(e) applied to S), rounds P to bf16 and
-//              transposes it with movmatrix into the B operand, and accumulates O^T += V^T P^T
-//              (128 dims x 8 heads, fp32) with 8 MMAs (A = V via transposing ldmatrix); on a
-//              piece's last block it writes bf16 `out` (the piece is the whole segment) or the
-//              partial (sum p V, (m, l)) to slot v + i.
+//              columns) with 8 m16n8k16 bf16 MMAs in two accumulator chains (A = K via
+//              ldmatrix), updates the online softmax in the log2 domain (scale * log2(e) folded
+//              into one FMA per exponent; a head's shift moves only when its maximum passes it
+//              by more than 8), rounds P to bf16 and transposes it with movmatrix into the B
+//              operand, and accumulates O^T += V^T P^T (128 dims x 8 heads, fp32) with 8 MMAs
+//              (A = V via transposing ldmatrix); on a piece's last block it writes bf16 `out`
+//              (the piece is the whole segment) or the partial (sum p V, (shift, l)) to slot
+//              v + i.
 // decode_merge_kernel combines the pieces of split segments:
-//   M = max_p m_p,  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
+//   M = max_p m_p,  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p  (m_p: each piece's
+//   softmax shift, which serves as its maximum would).
 // Ranges are dealt to the CTAs round-robin (range v to warp v / grid of CTA v % grid).
 //
 // Shared memory per stage: [K cols 0-63 | K cols 64-127 | V cols 0-63 | V cols 64-127 | q rows],
@@ -360,7 +363,7 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
   uint32_t qb[8][2];                     // B operand q^T: head gq, dims 16kk + 2cq (+1), +8
                                          // (E4M3 caches: dims 16kk + 4cq .. +3, f16)
   float k_fold = 0.f, v_fold = 0.f;      // E4M3 caches: softmax scale * K scale, V scale
-  float m0 = -INFINITY, m1 = -INFINITY;  // running max of head columns 2cq, 2cq+1
+  float m0 = -INFINITY, m1 = -INFINITY;  // softmax shifts of head columns 2cq, 2cq+1
   float l0 = 0.f, l1 = 0.f;              // this lane's share of the running sums
   float o[8][4];                         // O^T: dims 16mt + gq (+8), heads 2cq, 2cq+1
 #pragma unroll
