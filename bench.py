@@ -354,6 +354,9 @@ def run_gpu(args, rank, world, dist):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(total_ms_max / args.steps, 6),
+        # spread of this rank's per-step event times (each step timed alone after the flush)
+        "step_us_percentiles": {k: round(1e3 * float(v), 3) for k, v in
+                                zip(("p10", "p50", "p90"), np.percentile(step_ms, [10, 50, 90]))},
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
