@@ -40,3 +40,23 @@ def test_reference_arm_prints_one_contract_line():
 def test_timing_rules_are_enforced_on_the_command_line():
     r = run_bench("--impl", "reference", "--steps", "1", "--warmup", "2")
     assert r.returncode != 0 and "--warmup must be >= 3" in r.stderr
+
+
+def test_traffic_key_ignores_comments_and_tracks_code(tmp_path, monkeypatch):
+    """roofline.traffic is keyed by a hash of the decode sources: editing a comment keeps the
+    hash, editing code changes it (so a stale ncu capture is reported as null, never as current)."""
+    import shutil
+    sys.path.insert(0, str(ROOT))
+    import bench
+    base = bench.kernel_source_hash()
+    fake = tmp_path / "paged_kv_cache_244_gb300" / "csrc"
+    fake.mkdir(parents=True)
+    for name in ("paged_decode.cu", "pa_device.cuh", "pa_launch.h"):
+        shutil.copy(ROOT / "paged_kv_cache_244_gb300" / "csrc" / name, fake / name)
+    monkeypatch.setattr(bench, "ROOT", tmp_path)
+    assert bench.kernel_source_hash() == base
+    src = fake / "paged_decode.cu"
+    src.write_text(src.read_text() + "\n// a comment\n/* and a block comment */\n")
+    assert bench.kernel_source_hash() == base
+    src.write_text(src.read_text() + "\nconstexpr int kUnused = 1;\n")
+    assert bench.kernel_source_hash() != base
