@@ -134,22 +134,26 @@ int pa_rope_kv_store(const pa_dims* dims, int num_tokens, void* q, const void* k
 /*
  * pa_decode_partition_tokens -- validate a partition request for pa_decode (Flash Decode,
  * [PV] §H200上的详细对比).  pa_decode lays the (sequence, KV head, block) jobs of the batch
- * on one axis and cuts it into contiguous ranges, one warp of its persistent grid at a time:
- * `partition_tokens` == 0 cuts the axis into equal ranges, one per warp (every warp gets the
- * same number of blocks +-1); > 0 cuts it every partition_tokens / block_size blocks.  Where a
- * range boundary falls inside a sequence, that sequence's pieces are merged by a second
- * kernel.  Returns the request (0 or a positive multiple of block_size) or a negative
- * PA_ERR_* code (PA_ERR_RANGE also for num_seqs > 8192 or max_context_len < 1).
+ * on one axis and cuts it into equal contiguous ranges, one per warp of its persistent grid
+ * (every warp gets the same number of blocks +-1).  A sequence's blocks for one KV head are
+ * computed in pieces: a piece ends at a range boundary, at the end of the sequence and, when
+ * `partition_tokens` P > 0, at every P-token partition boundary, so that each P-token
+ * partition yields its own partial softmax result (one piece, or more when range boundaries
+ * fall inside it).  The pieces of a split sequence are then reduced by a second kernel
+ * (log-sum-exp merge, in axis order).  P changes how the partial results are grouped, not how
+ * the work is spread over the GPU.  Returns the request (0 or a positive multiple of
+ * block_size) or a negative PA_ERR_* code (PA_ERR_RANGE also for num_seqs > 8192 or
+ * max_context_len < 1).
  */
 int pa_decode_partition_tokens(const pa_dims* dims, int num_seqs, int max_context_len,
                                int partition_tokens);
 
 /*
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for these
- * arguments: (R + num_seqs * Hkv) * (Hq / Hkv) * (D + 2) * 4, where R bounds the number of
- * ranges: min(2048, J) for partition_tokens == 0, ceil(J / (partition_tokens / 16)) otherwise,
- * with J = num_seqs * Hkv * ceil(max_context_len / 16).  Returns 0 for invalid arguments
- * (pa_decode then reports the error).
+ * arguments: (R + num_seqs * Hkv * M) * (Hq / Hkv) * (D + 2) * 4, where R = min(2048,
+ * ceil(J / 2)) bounds the ranges, J = num_seqs * Hkv * ceil(max_context_len / 16), and M = 1
+ * for partition_tokens == 0, else ceil(ceil(max_context_len / 16) / (partition_tokens / 16)).
+ * Returns 0 for invalid arguments (pa_decode then reports the error).
  */
 size_t pa_decode_workspace_size(const pa_dims* dims, int num_seqs, int max_context_len,
                                 int partition_tokens);

@@ -40,19 +40,27 @@ int check_partition(const pa_dims* d, int num_seqs, int max_context_len, int req
   return requested;
 }
 
-// Partial rows: G per piece, one piece per (range, segment) pair that meets, so at most
-// (#ranges + #segments) pieces.  Each row is D partial sums plus a (max, sum) pair.
+// Partitions of the longest segment: ceil(ceil(max_context_len / 16) / (P / 16)), 1 for P = 0.
+long long max_parts_for(const pa_dims* d, int max_context_len, int partition_tokens) {
+  if (partition_tokens <= 0) return 1;
+  const long long blocks = (max_context_len + d->block_size - 1) / d->block_size;
+  const long long chunk = partition_tokens / d->block_size;
+  return (blocks + chunk - 1) / chunk;
+}
+
+// Partial rows: every piece of a split segment owns a slot of G rows, and slots stay below
+// V + (#segments) * max_parts, with V <= min(ceil(J / PA_DECODE_MIN_RANGE), kMaxDecodeWarps)
+// the ranges of the even split (J = jobs).  Each row is D partial sums plus a (shift, sum)
+// pair.  0 when the rows would not fit in an int.
 size_t workspace_bytes_for(const pa_dims* d, int num_seqs, int max_context_len, int partition_tokens) {
   const long long segs = static_cast<long long>(num_seqs) * d->num_kv_heads;
   const long long jobs = segs * ((max_context_len + d->block_size - 1) / d->block_size);
-  long long ranges;
-  if (partition_tokens > 0) {
-    const long long chunk = partition_tokens / d->block_size;
-    ranges = (jobs + chunk - 1) / chunk;
-  } else {
-    ranges = jobs < pa::kMaxDecodeWarps ? jobs : pa::kMaxDecodeWarps;
-  }
-  const long long rows = (ranges + segs) * (d->num_q_heads / d->num_kv_heads);
+  if (jobs > 0x7fffffffll) return 0;  // positions on the job axis are 32-bit in the kernels
+  long long ranges = (jobs + PA_DECODE_MIN_RANGE - 1) / PA_DECODE_MIN_RANGE;
+  if (ranges > pa::kMaxDecodeWarps) ranges = pa::kMaxDecodeWarps;
+  const long long rows = (ranges + segs * max_parts_for(d, max_context_len, partition_tokens)) *
+                         (d->num_q_heads / d->num_kv_heads);
+  if (rows > 0x7fffffffll) return 0;
   return static_cast<size_t>(rows) * (static_cast<size_t>(d->head_dim) + 2) * sizeof(float);
 }
 
@@ -91,6 +99,7 @@ int decode_args(const pa_dims* dims, int num_seqs, const void* q, const void* k_
   const int P = check_partition(dims, num_seqs, max_context_len, partition_tokens);
   if (P < 0) return P;
   const size_t need = workspace_bytes_for(dims, num_seqs, max_context_len, P);
+  if (need == 0) return PA_ERR_RANGE;
   if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
   const void* ptrs[] = {q, k_cache, v_cache, block_tables, context_lens, out, workspace};
   for (const void* p : ptrs)
@@ -116,6 +125,7 @@ int decode_args(const pa_dims* dims, int num_seqs, const void* q, const void* k_
   a->max_blocks = max_blocks;
   a->max_context_len = max_context_len;
   a->chunk_blocks = P / dims->block_size;
+  a->max_parts = static_cast<int>(max_parts_for(dims, max_context_len, P));
   a->num_warps = 0;  // set by the launcher from the grid it picks
   a->scale_log2 = scale * 1.4426950408889634f;
   a->status = status;

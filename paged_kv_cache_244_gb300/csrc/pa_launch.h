@@ -56,7 +56,8 @@ struct DecodeArgs {
   float* ws_o;                      // [slots][G][128]  partial sum_t p_t V_t of each piece
   float2* ws_ml;                    // [slots][G]       partial (max, sum p), log2 domain
   int num_seqs, num_q_heads, num_kv_heads, num_blocks, max_blocks, max_context_len;
-  int chunk_blocks;                 // 0: even split over the grid's warps; else blocks per range
+  int chunk_blocks;                 // 0, or P / 16: no piece spans a P-token partition boundary
+  int max_parts;                    // partitions of the longest segment (1 without partitions)
   int num_warps;                    // warps of the partition kernel's grid (set at launch)
   float scale_log2;                 // softmax scale * log2(e)
   unsigned* status;

@@ -104,22 +104,20 @@ struct Layout {
 constexpr uint32_t kFirst = 1u, kLast = 2u, kWhole = 4u, kHasData = 8u;
 constexpr uint32_t kNew = 16u;   // fused step: the block holding the segment's new token
 constexpr uint32_t kRope = 32u;  // fused step: the sequence's position has a cos/sin row
+constexpr uint32_t kGap = 64u;   // the piece starts at a range boundary that is also a partition
+                                 // boundary inside the segment: the slot before it is a gap
 constexpr int kMinRangeBlocks = PA_DECODE_MIN_RANGE;
 
 
-// Flattened-axis ranges.  chunk > 0: range v = [v*chunk, (v+1)*chunk) clipped to T.  chunk == 0:
-// V = min(num_warps, ceil(T / kMinRangeBlocks)) ranges, range v = [floor(v T / V),
-// floor((v+1) T / V)): equal ranges, none shorter than kMinRangeBlocks blocks unless T is, so
-// that a small batch is not cut into one-block pieces that the merge must then gather.
+// Flattened-axis ranges: V = min(num_warps, ceil(T / kMinRangeBlocks)) equal ranges, range
+// v = [floor(v T / V), floor((v+1) T / V)), none shorter than kMinRangeBlocks blocks unless T
+// is, so that a small batch is not cut into one-block pieces that the merge must then gather.
+// With V <= #warps of the grid, every warp has at most one range.
 struct Ranges {
   long long T;
-  int V, chunk;
-  __device__ __forceinline__ long long begin(int v) const {
-    if (chunk) return min(static_cast<long long>(v) * chunk, T);
-    return (static_cast<long long>(v) * T) / V;
-  }
+  int V;
+  __device__ __forceinline__ long long begin(int v) const { return (static_cast<long long>(v) * T) / V; }
   __device__ __forceinline__ int owner(long long x) const {
-    if (chunk) return static_cast<int>(x / chunk);
     return static_cast<int>(((x + 1) * V - 1) / T);
   }
 };
@@ -127,10 +125,20 @@ struct Ranges {
 __device__ __forceinline__ Ranges make_ranges(long long T, const DecodeArgs& a) {
   Ranges r;
   r.T = T;
-  r.chunk = a.chunk_blocks;
-  if (r.chunk) r.V = static_cast<int>((T + r.chunk - 1) / r.chunk);
-  else r.V = static_cast<int>(min(static_cast<long long>(a.num_warps), (T + kMinRangeBlocks - 1) / kMinRangeBlocks));
+  r.V = static_cast<int>(min(static_cast<long long>(a.num_warps), (T + kMinRangeBlocks - 1) / kMinRangeBlocks));
   return r;
+}
+
+// Partial slot of the piece of segment `seg` in range v and P-token partition `part` (0
+// without partitions; max_parts = partitions of the longest segment, 1 without).  Along the
+// job axis consecutive pieces differ in range, partition or segment, and each such step
+// raises the slot by at least one, so slots are distinct and below V + (#segments) * max_parts.
+// Within one segment a step raises it by exactly one, except where a range boundary is also a
+// partition boundary: there it skips one slot, which the warp whose range starts there marks
+// empty (shift -inf, sum 0).  So a segment's pieces, with those gaps, fill the slots from
+// v_first + seg * max_parts to v_last + seg * max_parts + (its last partition), in axis order.
+__device__ __forceinline__ long long piece_slot(int v, int seg, int part, int max_parts) {
+  return static_cast<long long>(v) + static_cast<long long>(seg) * max_parts + part;
 }
 
 __device__ __forceinline__ int clamp_len(int len, int max_len) {
@@ -261,15 +269,22 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     W.blk = a.block_tables[static_cast<size_t>(s) * a.max_blocks + j];
     W.seg = s * Hkv + g;
     const int valid = min(kBlockSize, len - j * kBlockSize);
-    uint32_t flags = ((p == x0 || j == 0) ? kFirst : 0u) | ((p == x1 - 1 || j == ns - 1) ? kLast : 0u) |
-                     ((Xi >= x0 && Xi + ns <= x1) ? kWhole : 0u);
+    // Pieces end at range, segment and (P-token partitions) partition boundaries.
+    const int chunk = a.chunk_blocks;
+    const int part = chunk ? j / chunk : 0;
+    const bool p_first = chunk && j == part * chunk;
+    const bool p_last = chunk && j == part * chunk + chunk - 1;
+    uint32_t flags = ((p == x0 || j == 0 || p_first) ? kFirst : 0u) |
+                     ((p == x1 - 1 || j == ns - 1 || p_last) ? kLast : 0u) |
+                     ((Xi >= x0 && Xi + ns <= x1 && (chunk == 0 || ns <= chunk)) ? kWhole : 0u) |
+                     ((p == x0 && j > 0 && p_first) ? kGap : 0u);
     if (kStep) {
       W.pos = len - 1;
       if (j == ns - 1) flags |= kNew;
       if (W.pos < a.max_pos) flags |= kRope;  // len >= 1 here, so pos >= 0
     }
     W.fl = static_cast<int>(flags | (static_cast<uint32_t>(valid) << 8) | (static_cast<uint32_t>(g) << 16));
-    W.slot = W.v + W.seg;
+    W.slot = static_cast<int>(piece_slot(W.v, W.seg, part, a.max_parts));
   };
   // The window after W: the rest of W's range, else the start of this warp's next range.
   auto next_of = [&](const Window& W, Window& N) {
@@ -432,6 +447,8 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
       l0 = l1 = 0.f;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      if ((fl & kGap) && lane < G)  // mark the skipped slot before this piece empty
+        a.ws_ml[(static_cast<size_t>(d.z) - 1) * G + lane] = make_float2(-INFINITY, 0.f);
     }
     if (fl & kHasData) {
       const int valid = static_cast<int>((fl >> 8) & 0xffu);
@@ -749,9 +766,10 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
 // the partition kernel, not outputs).  out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
 // Empty sequences get zeros.  CTAs have 8 warps beside the bf16 partition kernel and 4 beside
 // the 12-warp E4M3 one, so that at least one fits next to it (registers).
-constexpr int kMergeWarps = 8;   // most warps per CTA
-constexpr int kMergeSplit = 4;   // warps per (sequence, query head)
+constexpr int kMergeWarps = 8;   // warps per CTA of the narrow merge
+constexpr int kMergeSplit = 4;   // warps per (sequence, query head) and piece group: 32 dims each
 constexpr int kMergeBatch = 32;  // pieces loaded per round trip
+constexpr int kWideGroups = 4;   // piece groups per (sequence, query head) in the wide merge
 
 // Every merge warp waits for the partition kernel before it exits or lets the next grid on
 // the stream launch, so that a following launch that reads ahead of its own wait (a decode
@@ -762,12 +780,20 @@ __device__ __forceinline__ void wait_then_release() {
   pdl_allow_next_grid();
 }
 
-__global__ void __launch_bounds__(kMergeWarps * 32, 2) decode_merge_kernel(const DecodeArgs a) {
+// kGroups == 1 (narrow): CTAs of 8 (or 4) warps, 4 warps per (sequence, query head).
+// kGroups > 1 (wide, for batches with fewer (sequence, query head) pairs than SMs): one CTA of
+// kGroups x 4 warps per pair; piece group q takes the q-th contiguous share of the segment's
+// pieces, and the groups' (M, L, acc) are combined in group order through shared memory.
+template <int kGroups>
+__global__ void __launch_bounds__(kGroups == 1 ? kMergeWarps * 32 : kGroups * kMergeSplit * 32, kGroups == 1 ? 2 : 1)
+decode_merge_kernel(const DecodeArgs a) {
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * static_cast<int>(blockDim.x >> 5) + static_cast<int>(threadIdx.x >> 5);
-  const int w = gw / kMergeSplit;                  // (sequence, query head)
-  const int quarter = gw - w * kMergeSplit;        // dims 32 quarter .. 32 quarter + 31
+  const int w = gw / (kGroups * kMergeSplit);          // (sequence, query head)
+  const int grp = (gw / kMergeSplit) % kGroups;        // piece group
+  const int quarter = gw % kMergeSplit;                // dims 32 quarter .. 32 quarter + 31
   const int S = a.num_seqs;
+  // Every exit below depends on w alone, which is one per CTA in the wide form.
   if (w >= S * a.num_q_heads) {
     wait_then_release();
     return;
@@ -795,28 +821,36 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) decode_merge_kernel(const
   __nv_bfloat16* orow = a.out + static_cast<size_t>(w) * kHeadDim + dim;
   if (ns == 0) {  // empty context: zero row (after the partition kernel, which may read `out`)
     wait_then_release();
-    *orow = __float2bfloat16_rn(0.f);
+    if (grp == 0) *orow = __float2bfloat16_rn(0.f);
     return;
   }
   const Ranges R = make_ranges(static_cast<long long>(Hkv) * total, a);
   const long long Xi = static_cast<long long>(Hkv) * before + static_cast<long long>(g) * ns;
   const int v_first = R.owner(Xi);
-  const int npieces = R.owner(Xi + ns - 1) - v_first + 1;
-  if (npieces <= 1) {  // written directly by the partition kernel
-    wait_then_release();
+  const int v_last = R.owner(Xi + ns - 1);
+  // Pieces in slot order: slot_first + k, k < npieces, gaps included (see piece_slot).
+  const int chunk = a.chunk_blocks;
+  const int part_last = chunk ? (ns - 1) / chunk : 0;
+  const int npieces = v_last - v_first + part_last + 1;
+  if (npieces == 1) {
+    wait_then_release();  // one piece: written directly by the partition kernel
     return;
   }
-  // piece p lives in slot v_first + p + segment; its row for this head is slot * G + hl
-  const size_t row_base = (static_cast<size_t>(v_first) + s * Hkv + g) * G + hl;
-  const float2* ml = a.ws_ml + row_base;                               // stride G per piece
-  const float* rows = a.ws_o + row_base * kHeadDim + dim;              // stride G * 128
+  const int seg = s * Hkv + g;
+  const int k0 = static_cast<int>(static_cast<long long>(grp) * npieces / kGroups);
+  const int k1 = static_cast<int>(static_cast<long long>(grp + 1) * npieces / kGroups);
+  const size_t row_base = static_cast<size_t>(piece_slot(v_first, seg, 0, a.max_parts)) * G + hl;
+  const float2* ml = a.ws_ml + row_base;
+  const float* rows = a.ws_o + row_base * kHeadDim + dim;
   const size_t stride = static_cast<size_t>(G) * kHeadDim;
   wait_then_release();
 
+  // One round trip per batch: this lane's (m, l) of the batch's piece `lane`, and its dim of
+  // every piece row of the batch, combined into (M, L, acc) in piece order.  A gap (m = -inf,
+  // l = 0) gets weight 0 and its row, never written, is not used.
   float M = -INFINITY, L = 0.f, acc = 0.f;
-  for (int base = 0; base < npieces; base += kMergeBatch) {
-    const int n = min(kMergeBatch, npieces - base);
-    // one round trip: this lane's (m, l) of piece base + lane, and its dim of every piece row
+  for (int base = k0; base < k1; base += kMergeBatch) {
+    const int n = min(kMergeBatch, k1 - base);
     const float2 mine = lane < n ? ml[(base + lane) * G] : make_float2(-INFINITY, 0.f);
     float r[kMergeBatch];
 #pragma unroll
@@ -825,18 +859,43 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) decode_merge_kernel(const
 #pragma unroll
     for (int x = 16; x > 0; x >>= 1) Mb = fmaxf(Mb, __shfl_xor_sync(kFullMask, Mb, x));
     const float Mn = fmaxf(M, Mb);
-    const float rescale = exp2f(M - Mn);  // 0 on the first batch (M = -inf)
+    const float rescale = M == -INFINITY ? 0.f : exp2f(M - Mn);
     M = Mn;
-    const float wmine = exp2f(mine.x - M);  // 0 for lanes past the last piece
+    const float wmine = mine.x == -INFINITY ? 0.f : exp2f(mine.x - M);
     float lb = wmine * mine.y;
 #pragma unroll
     for (int x = 16; x > 0; x >>= 1) lb += __shfl_xor_sync(kFullMask, lb, x);
     L = fmaf(L, rescale, lb);
     acc *= rescale;
 #pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) acc = fmaf(__shfl_sync(kFullMask, wmine, u), r[u], acc);
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const float wu = __shfl_sync(kFullMask, wmine, u);
+      if (wu != 0.f) acc = fmaf(wu, r[u], acc);
+    }
   }
-  *orow = __float2bfloat16_rn(acc / L);
+  if constexpr (kGroups > 1) {
+    __shared__ float s_acc[kGroups][kMergeSplit][32];
+    __shared__ float2 s_ml[kGroups][kMergeSplit];
+    s_acc[grp][quarter][lane] = acc;
+    if (lane == 0) s_ml[grp][quarter] = make_float2(M, L);
+    __syncthreads();
+    if (grp != 0) return;
+    // the groups in order (a group with no piece has L == 0 and is skipped)
+    float Mt = -INFINITY, Lt = 0.f, At = 0.f;
+#pragma unroll
+    for (int q = 0; q < kGroups; ++q) {
+      const float2 ml = s_ml[q][quarter];
+      if (ml.y == 0.f) continue;
+      const float Mn = fmaxf(Mt, ml.x);
+      const float al = exp2f(Mt - Mn), be = exp2f(ml.x - Mn);
+      Mt = Mn;
+      Lt = fmaf(Lt, al, ml.y * be);
+      At = fmaf(At, al, s_acc[q][quarter][lane] * be);
+    }
+    *orow = __float2bfloat16_rn(At / Lt);
+  } else {
+    *orow = __float2bfloat16_rn(acc / L);
+  }
 }
 
 // ---- host side ------------------------------------------------------------------------
@@ -893,8 +952,7 @@ cudaError_t launch_partition(DecodeArgs& a, const CUtensorMap& tm_k, const CUten
   // No more CTAs than there can be ranges (ranges are dealt to the CTAs one at a time).
   const long long jobs_bound = static_cast<long long>(a.num_seqs) * a.num_kv_heads *
                                ((a.max_context_len + kBlockSize - 1) / kBlockSize);
-  const long long want = a.chunk_blocks ? (jobs_bound + a.chunk_blocks - 1) / a.chunk_blocks
-                                        : (jobs_bound + kMinRangeBlocks - 1) / kMinRangeBlocks;
+  const long long want = (jobs_bound + kMinRangeBlocks - 1) / kMinRangeBlocks;
   const long long ctas = min(static_cast<long long>(max_ctas), want);
   constexpr int kWarpsN = Layout<kStep, kFp8>::kWarpsN;
   a.num_warps = static_cast<int>(ctas) * kWarpsN;
@@ -984,15 +1042,27 @@ cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {
                   : launch_partition<false, false>(a, tm_k, tm_v, attr, stream);
   if (err != cudaSuccess) return err;
 
-  const long long merge_warps = static_cast<long long>(a.num_seqs) * a.num_q_heads * kMergeSplit;
-  const int per_cta = fp8 ? kMergeWarps / 2 : kMergeWarps;
+  // Narrow merge beside the partition kernel; the wide one when the (sequence, query head)
+  // pairs are fewer than the partition kernel's CTAs, so that long segments' many pieces are
+  // spread over more warps.
+  const long long pairs = static_cast<long long>(a.num_seqs) * a.num_q_heads;
+  int part_ctas = 0;
+  err = fp8 ? persistent_ctas<false, true>(&part_ctas) : persistent_ctas<false, false>(&part_ctas);
+  if (err != cudaSuccess) return err;
   cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(static_cast<unsigned>((merge_warps + per_cta - 1) / per_cta));
-  mcfg.blockDim = dim3(per_cta * 32);
   mcfg.stream = stream;
   mcfg.attrs = attr;
   mcfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&mcfg, decode_merge_kernel, a);
+  if (pairs <= part_ctas) {
+    mcfg.gridDim = dim3(static_cast<unsigned>(pairs));
+    mcfg.blockDim = dim3(kWideGroups * kMergeSplit * 32);
+    return cudaLaunchKernelEx(&mcfg, decode_merge_kernel<kWideGroups>, a);
+  }
+  const long long merge_warps = pairs * kMergeSplit;
+  const int per_cta = fp8 ? kMergeWarps / 2 : kMergeWarps;
+  mcfg.gridDim = dim3(static_cast<unsigned>((merge_warps + per_cta - 1) / per_cta));
+  mcfg.blockDim = dim3(per_cta * 32);
+  return cudaLaunchKernelEx(&mcfg, decode_merge_kernel<1>, a);
 }
 
 }  // namespace pa

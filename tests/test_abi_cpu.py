@@ -261,11 +261,16 @@ def test_partition_choice_and_workspace_size(L):
             b.decode_partition_tokens(12, 2, 4, 32768, bad)
     with pytest.raises(b.PaError):
         b.decode_partition_tokens(12, 2, 8193, 64)              # more sequences than supported
-    # workspace: (ranges + segments) * G rows of (D + 2) floats
+    # workspace: (ranges + segments * partitions) * G rows of (D + 2) floats, ranges <=
+    # min(2048, ceil(jobs / 2))
     row = 130 * 4
-    assert b.decode_workspace_size(12, 2, 4, 32768, 512) == (512 + 8) * 6 * row
-    assert b.decode_workspace_size(12, 2, 2, 40, 64) == (3 + 4) * 6 * row
-    assert b.decode_workspace_size(12, 2, 2, 40) == (12 + 4) * 6 * row
+    # 4 x 32768 tokens, 512-token partitions: 2048 ranges + 8 segments x 64 partitions
+    assert b.decode_workspace_size(12, 2, 4, 32768, 512) == (2048 + 8 * 64) * 6 * row
+    # 2 x 40 tokens: 12 jobs -> 6 ranges; 64-token partitions: one per segment
+    assert b.decode_workspace_size(12, 2, 2, 40, 64) == (6 + 4) * 6 * row
+    assert b.decode_workspace_size(12, 2, 2, 40) == (6 + 4) * 6 * row
+    # 16-token partitions: 3 per segment
+    assert b.decode_workspace_size(12, 2, 2, 40, 16) == (6 + 4 * 3) * 6 * row
     assert b.decode_workspace_size(12, 2, 64, 4096) == (2048 + 128) * 6 * row
     assert b.decode_workspace_size(12, 2, 4, 32768, 100) == 0
 
