@@ -23,7 +23,11 @@ The printed JSON line carries:
                        copies and calls replayed as one CUDA graph, like the device step);
   roofline             the step's decode call (its partition kernel plus the merge kernel)
                        on one layer, timed alone with CUDA events, against the measured HBM
-                       copy bandwidth;
+                       copy bandwidth; beside it gather_floor_*: pa_gather_checksum on the same
+                       layer, the same tile gather with no attention and no merge;
+  configs              every named workload's step (tiny, qwen_b1 with its 28 layers, mix64,
+                       prefix32, long4 with 512-token partitions): time, GB/s, fraction of the
+                       HBM peak, decode tokens/s (--no-configs skips it);
   cpu_baseline         the fp64 oracle on the host cores over a bounded sample;
   fp8_kv               the step's decode on E4M3 caches (pa_decode_fp8, pa_decode_step_fp8),
                        bandwidth counted on the E4M3 bytes (--no-fp8 skips it);
@@ -316,9 +320,17 @@ def run_gpu(args, rank, world, dist):
     dec_avg = float(np.mean(dec_ms))
     rope_ms = timed_loop(lambda: st.rope_store(0), max(3, args.steps // 4))
     plain_ms = timed_loop(lambda: st.decode(0), max(3, args.steps // 4))
+    # the floor of the decode's access pattern: the same gather of K/V tiles (same kernel shape,
+    # block tables, TMA boxes, stage ring, persistent grid) with no attention and no merge
+    xor_buf = torch.zeros((w.num_seqs, w.num_kv_heads), dtype=torch.int32, device="cuda")
+    floor_ms = timed_loop(lambda: binding.gather_checksum(st.k_cache[0], st.v_cache[0], st.block_tables,
+                                                          st.context_lens, w.max_context_len,
+                                                          w.num_q_heads, out_xor=xor_buf), args.steps)
+    floor_avg = float(np.mean(floor_ms))
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, st, torch, binding, flush_l2)
+    configs = None if args.no_configs else all_configs(args, torch, binding, flush_l2, timed_loop, world)
     blocks = None if args.no_block_ops else block_ops(torch, binding, flush_l2, timed_loop, w)
     fp8 = None if args.no_fp8 else fp8_kv(torch, binding, timed_loop, st, args.steps)
     pre = None if args.no_prefill else prefill_runs(torch, binding, timed_loop, max(5, args.steps // 4))
@@ -378,6 +390,11 @@ def run_gpu(args, rank, world, dist):
             "traffic_source": traffic_note,
             "algorithmic_bytes_per_launch": dec_bytes,
             "avg_launch_ms": round(dec_avg, 6),
+            # pa_gather_checksum on the same layer: the decode's tile gather alone
+            "gather_floor_us": round(floor_avg * 1e3, 3),
+            "gather_floor_GBps": round(dec_bytes / (floor_avg * 1e-3) / 1e9, 2),
+            "gather_floor_frac": round(dec_bytes / (floor_avg * 1e-3) / 1e9 / peak, 4),
+            "decode_over_floor": round(dec_avg / floor_avg, 4),
         },
         "rope_kv_store_us": round(1e3 * float(np.median(rope_ms)), 3),
         "pa_decode_us": round(1e3 * float(np.mean(plain_ms)), 3),
@@ -385,6 +402,7 @@ def run_gpu(args, rank, world, dist):
                 "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e_ms_max / args.steps, 6), "launch": e2e["launch"]},
         "gpu_launches": st.launches_per_step * args.steps,
+        "configs": configs,
         "block_ops": blocks,
         "fp8_kv": fp8,
         "prefill": pre,
@@ -393,6 +411,51 @@ def run_gpu(args, rank, world, dist):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     return line
+
+
+def all_configs(args, torch, binding, flush_l2, timed_loop, world):
+    """Every named workload's step (fused RoPE + store + decode for each of its layers, early
+    metadata on layers after the first, replayed as a CUDA graph), L2 flushed before each
+    step: step time, KV bytes per second against the measured HBM copy peak, and decode
+    tokens per second (sequences per step over the step time).  prefix32 also reports the
+    bandwidth over its unique KV bytes (the shared prefix is read once from HBM, then from L2)."""
+    peak, kind = hbm_peak()
+    res = {}
+    for name in W.WORKLOADS:
+        w = W.make(name)
+        st = DeviceStep(w, torch, binding, fused=True, early=True)
+        for _ in range(3):
+            st.step()
+        fn = st.step
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                st.step()
+            graph.replay()
+            torch.cuda.synchronize()
+            fn = graph.replay
+        except Exception:
+            pass
+        ms = float(np.mean(timed_loop(fn, max(10, args.steps // 4))))
+        rc, flags = binding.get_device_status()
+        if rc != 0:
+            raise RuntimeError(f"device status after the {name} step: {rc} flags {flags:#x}")
+        nbytes = w.kv_bytes_per_layer() * w.num_layers
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        entry = {"layers": w.num_layers, "num_seqs": w.num_seqs,
+                 "partition_tokens": st.P or "0 (even split)",
+                 "step_us": round(ms * 1e3, 3), "kv_bytes_per_step": nbytes,
+                 "GB/s": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
+                 "decode_tokens_per_s": round(world * w.num_seqs / (ms * 1e-3), 1)}
+        if w.meta.get("shared_prefix_blocks"):
+            ub = w.unique_kv_bytes_per_layer() * w.num_layers
+            entry["unique_kv_bytes_per_step"] = ub
+            entry["unique_GB/s"] = round(ub / (ms * 1e-3) / 1e9, 1)
+        res[name] = entry
+        del st, fn
+        torch.cuda.empty_cache()
+    res["peak"] = {"hbm_GB/s": peak, "kind": f"{kind} hbm_gbs"}
+    return res
 
 
 def block_ops(torch, binding, flush_l2, timed_loop, w, layers=28, pool_blocks=1024, reps=20):
@@ -780,6 +843,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the pa_prefill measurement")
     ap.add_argument("--no-block-ops", action="store_true",
                     help="skip the pa_copy_blocks measurements (copy-on-write, swap out / in)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the step measurement of every named workload")
     ap.add_argument("--split-step", action="store_true",
                     help="pa_rope_kv_store then pa_decode instead of the fused pa_decode_step")
     ap.add_argument("--partition-tokens", type=int, default=None,

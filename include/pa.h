@@ -396,6 +396,33 @@ int pa_get_device_status(void* stream, uint32_t* flags);
  */
 int pa_selftest_wait_timeout(uint32_t limit_us, void* stream);
 
+/*
+ * pa_gather_checksum -- the gather half of pa_decode alone: every (block, KV head) tile of K
+ * and V that pa_decode would read is brought into shared memory through the block tables, by
+ * the same kernel shape (persistent grid, even split of the jobs, lookahead over the block
+ * table, one TMA box per tile, the same stage ring), and folded into a checksum instead of
+ * attention; nothing is merged.  No counterpart in the source pages: it measures the floor
+ * that the decode's access pattern sets on this GPU, and checks cache contents after block
+ * copies or swaps.
+ *
+ * For each sequence s with n = min(context_lens[s], max_context_len) and each KV head g,
+ *   out_xor[s * Hkv + g] ^= XOR over t < n of the 64 32-bit words of k_cache row
+ *   [block_tables[s][t / 16]][g][t % 16] and of the same v_cache row,
+ * each word as stored (bf16 pairs).  XOR is order-free, so the result does not depend on how
+ * the work is split.  Table entries past ceil(n / 16) are never read.
+ *
+ *   k_cache, v_cache  [num_blocks][Hkv][16][128] bf16, read only
+ *   block_tables, context_lens, max_context_len, num_blocks, max_blocks  as for pa_decode
+ *   out_xor           [S][Hkv] uint32, device memory, 4-byte aligned; XORed into (zero-fill it
+ *                     first for the plain checksum)
+ * Device-side errors as for pa_decode.  Returns PA_OK or a PA_ERR_* code (nothing launched on
+ * error).  Launches one kernel.
+ */
+int pa_gather_checksum(const pa_dims* dims, int num_seqs, const void* k_cache, const void* v_cache,
+                       int num_blocks, const int32_t* block_tables, int max_blocks,
+                       const int32_t* context_lens, int max_context_len, uint32_t* out_xor,
+                       void* stream);
+
 /* Human-readable name of a PA_* return code (static storage, never NULL). */
 const char* pa_status_string(int status);
 

@@ -296,6 +296,46 @@ int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_ca
                                                                                  : PA_ERR_CUDA;
 }
 
+int pa_gather_checksum(const pa_dims* dims, int num_seqs, const void* k_cache, const void* v_cache,
+                       int num_blocks, const int32_t* block_tables, int max_blocks,
+                       const int32_t* context_lens, int max_context_len, uint32_t* out_xor,
+                       void* stream) {
+  if (const int rc = check_dims(dims)) return rc;
+  if (num_seqs < 0 || num_seqs > pa::kMaxDecodeSeqs) return PA_ERR_RANGE;
+  if (num_seqs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_tables || !context_lens || !out_xor) return PA_ERR_NULL;
+  if (num_blocks < 1 || max_blocks < 1 || max_context_len < 1) return PA_ERR_RANGE;
+  if (static_cast<long long>(max_context_len) > static_cast<long long>(max_blocks) * dims->block_size)
+    return PA_ERR_RANGE;
+  if (static_cast<long long>(num_blocks) * dims->num_kv_heads * dims->block_size > (1ll << 31))
+    return PA_ERR_RANGE;
+  if (static_cast<long long>(num_seqs) * dims->num_kv_heads *
+          ((max_context_len + dims->block_size - 1) / dims->block_size) > 0x7fffffffll)
+    return PA_ERR_RANGE;
+  const void* ptrs[] = {k_cache, v_cache, block_tables, context_lens};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return PA_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(out_xor) % 4 != 0) return PA_ERR_ALIGN;
+  unsigned* status = nullptr;
+  if (const int rc = status_word(&status)) return rc;
+  pa::DecodeArgs a{};
+  a.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  a.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = dims->num_q_heads;
+  a.num_kv_heads = dims->num_kv_heads;
+  a.num_blocks = num_blocks;
+  a.max_blocks = max_blocks;
+  a.max_context_len = max_context_len;
+  a.chunk_blocks = 0;
+  a.max_parts = 1;
+  a.status = status;
+  a.gather_xor = out_xor;
+  return pa::launch_gather(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 int pa_decode_step(const pa_dims* dims, int num_seqs, const void* q, const void* k, const void* v,
                    const float* cos_sin, int max_pos, void* k_cache, void* v_cache, int num_blocks,
                    const int32_t* block_tables, int max_blocks, const int32_t* context_lens,

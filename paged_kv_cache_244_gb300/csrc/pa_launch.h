@@ -77,6 +77,9 @@ struct DecodeArgs {
   // Lengths and block table are read before the preceding kernel on the stream has finished
   // (the caller's promise that it writes neither).
   int early_metadata;
+  // Gather checksum only: [S][Hkv] words that each (sequence, KV head)'s tile words are XORed
+  // into.
+  uint32_t* gather_xor;
 };
 
 // Whole-block copies between pools (copy-on-write, swap out / in).  Pool pointers are device
@@ -116,5 +119,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const BlockCopyArgs& a, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// The decode kernel's gather of K/V tiles alone (no attention, no merge): pa_gather_checksum.
+cudaError_t launch_gather(const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace pa

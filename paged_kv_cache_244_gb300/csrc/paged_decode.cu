@@ -71,7 +71,11 @@ constexpr int kStages = PA_DECODE_STAGES;
 constexpr int kHalfBytes = kBlockSize * 128;                // 16 rows x 64 bf16
 constexpr int kQBytes = 8 * kHeadDim * 2;                   // q rows of up to 8 heads
 
-__host__ __device__ inline int prefix_bytes(int num_seqs) { return ((num_seqs + 1) * 4 + 15) & ~15; }
+// Per CTA in shared memory: the block-count prefix N_s (S + 1 ints), then per sequence the
+// valid rows of its last block (1..16; one byte each).
+__host__ __device__ inline int prefix_bytes(int num_seqs) {
+  return (((num_seqs + 1) * 4 + 15) & ~15) + ((num_seqs + 15) & ~15);
+}
 
 // Shared-memory layout of one kernel variant.  kStep fuses the new token's RoPE + store; kFp8
 // reads E4M3 caches, whose (block, KV head) tiles are 2 KiB instead of 4 KiB: there the CTA
@@ -145,7 +149,7 @@ __device__ __forceinline__ int clamp_len(int len, int max_len) {
   return len < 0 ? 0 : (len > max_len ? max_len : len);
 }
 
-template <bool kStep, bool kFp8>
+template <bool kStep, bool kFp8, bool kGather = false>
 __global__ void __launch_bounds__(Layout<kStep, kFp8>::kWarpsN * 32, 1)
 decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
@@ -160,6 +164,7 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
   const int lane = tid & 31;
   const uint32_t raw = smem_addr(smem_raw);
   int* prefix = reinterpret_cast<int*>(smem_raw + L::kPrefixOff);  // N_s, s = 0..S
+  unsigned char* last_rows = smem_raw + L::kPrefixOff + (((a.num_seqs + 1) * 4 + 15) & ~15);
   // 128-byte swizzled TMA destinations must sit on 1024-byte boundaries.
   const uint32_t tile_base = (raw + L::kPrefixOff + prefix_bytes(a.num_seqs) + 1023u) & ~1023u;
   if (tid < kPool) {
@@ -170,6 +175,7 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     prefetch_tensor_map(&tm_k);
     prefetch_tensor_map(&tm_v);
   }
+
   // With early metadata the lengths and block table are read, and the work resolved, before
   // the preceding kernel has finished; the first copy into shared memory and every write
   // wait for it (below, before the pipeline's first fill).
@@ -205,7 +211,9 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int w = 0; w < warp; ++w) run += warp_sums[w];
     for (int s = lo; s < hi; ++s) {
       prefix[s] = run;
-      run += (clamp_len(a.context_lens[s], a.max_context_len) + kBlockSize - 1) / kBlockSize;
+      const int len = clamp_len(a.context_lens[s], a.max_context_len);
+      run += (len + kBlockSize - 1) / kBlockSize;
+      last_rows[s] = static_cast<unsigned char>(((len - 1) & (kBlockSize - 1)) + 1);  // unused if len == 0
     }
     if (tid == kWarps * 32 - 1) {
       int total = 0;
@@ -216,7 +224,6 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
   }
   const long long T = static_cast<long long>(Hkv) * prefix[S];
   const Ranges R = make_ranges(T, a);
-  const int NW = gridDim.x * kWarps;
   // Stage pool: the CTA's kPool stages are shared out among its warps that have a range.  Range
   // v goes to warp v / grid of CTA v % grid, so these are warps 0 .. active - 1 (the others have
   // no work); with fewer ranges than warps (fixed-size partitions over a few long sequences)
@@ -246,11 +253,14 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     int blk, seg, fl, slot;
     int pos;              // fused step: position of the sequence's new token
   };
+  // This warp's range (at most one): its bounds, found once.
+  const int my_v = static_cast<int>(blockIdx.x) + warp * static_cast<int>(gridDim.x);
+  const long long x0 = my_v < R.V ? R.begin(my_v) : 0;
+  const long long x1 = my_v < R.V ? R.begin(my_v + 1) : 0;
   auto resolve = [&](Window& W) {
     W.blk = -1;
     W.seg = W.fl = W.slot = W.pos = 0;
     if (W.n == 0 || lane >= W.n) return;
-    const long long x0 = R.begin(W.v), x1 = R.begin(W.v + 1);
     const long long p = W.x + lane;
     // largest s with Hkv * N_s <= p (N_0 = 0 <= p < Hkv * N_S = T)
     int lo = 0, hi = S;
@@ -261,14 +271,15 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     const int s = lo;
     const int ns = prefix[s + 1] - prefix[s];
-    const long long off = p - static_cast<long long>(Hkv) * prefix[s];
-    const int g = static_cast<int>(off / ns);
-    const int j = static_cast<int>(off - static_cast<long long>(g) * ns);
+    const int off = static_cast<int>(p - static_cast<long long>(Hkv) * prefix[s]);  // < Hkv * ns
+    const int g = off / ns;
+    const int j = off - g * ns;
     const long long Xi = static_cast<long long>(Hkv) * prefix[s] + static_cast<long long>(g) * ns;
-    const int len = clamp_len(a.context_lens[s], a.max_context_len);
     W.blk = a.block_tables[static_cast<size_t>(s) * a.max_blocks + j];
     W.seg = s * Hkv + g;
-    const int valid = min(kBlockSize, len - j * kBlockSize);
+    const int tail = last_rows[s];
+    const int len = (ns - 1) * kBlockSize + tail;
+    const int valid = j == ns - 1 ? tail : kBlockSize;
     // Pieces end at range, segment and (P-token partitions) partition boundaries.
     const int chunk = a.chunk_blocks;
     const int part = chunk ? j / chunk : 0;
@@ -286,23 +297,19 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     W.fl = static_cast<int>(flags | (static_cast<uint32_t>(valid) << 8) | (static_cast<uint32_t>(g) << 16));
     W.slot = static_cast<int>(piece_slot(W.v, W.seg, part, a.max_parts));
   };
-  // The window after W: the rest of W's range, else the start of this warp's next range.
+  // The window after W: the rest of the range.
   auto next_of = [&](const Window& W, Window& N) {
     N.v = W.v;
     N.x = W.x + W.n;
-    if (W.n == 0 || N.x >= R.begin(W.v + 1)) {
-      N.v = W.v + NW;
-      N.x = N.v < R.V ? R.begin(N.v) : 0;
-    }
-    N.n = N.v < R.V ? static_cast<int>(min(32ll, R.begin(N.v + 1) - N.x)) : 0;
+    N.n = W.n == 0 ? 0 : static_cast<int>(min(32ll, x1 - N.x));
   };
 
   // Range v goes to warp v / gridDim.x of CTA v % gridDim.x: when there are fewer ranges than
   // warps they spread over all SMs (one warp each) rather than filling a few SMs.
   Window cur, nxt;
-  cur.v = warp * gridDim.x + blockIdx.x;
-  cur.x = cur.v < R.V ? R.begin(cur.v) : 0;
-  cur.n = cur.v < R.V ? static_cast<int>(min(32ll, R.begin(cur.v + 1) - cur.x)) : 0;
+  cur.v = my_v;
+  cur.x = x0;
+  cur.n = my_v < R.V ? static_cast<int>(min(32ll, x1 - x0)) : 0;
   resolve(cur);
   next_of(cur, nxt);
   resolve(nxt);
@@ -325,46 +332,45 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     ++pk;
     const bool ok = blk >= 0 && blk < a.num_blocks;
     const bool first = (fl & kFirst) != 0;
+    // Fused step: a position without a cos/sin row leaves the token as the store kernel would
+    // -- q unrotated, nothing stored.
+    const bool rope = kStep && (fl & kRope);
+    const bool fresh = rope && ok && (fl & kNew);  // the new token's K and V land in this tile
+    const bool trig = rope && (first || fresh);    // stage the cos/sin row
+    const bool q_rows = first && !kGather;         // the gather needs no q
+    // first cache row of the tile: (physical block * Hkv + KV head) * 16
+    const int y = ok ? (blk * Hkv + (fl >> 16)) * kBlockSize : 0;
+    const uint32_t bar = bars + 8 * st;
+    const uint32_t dst = tiles + st * kStageB;
+    const uint32_t bytes = (ok ? 2u * L::kTile : 0u) + (q_rows ? static_cast<uint32_t>(G) * 256u : 0u) +
+                           (trig ? kHeadDim * 4u : 0u) + (fresh ? kHeadDim * 4u : 0u);
     if (lane == 0) {
       if (!ok) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
-      // Fused step: a position without a cos/sin row leaves the token as the store kernel
-      // would -- q unrotated, nothing stored.
-      const bool rope = kStep && (fl & kRope);
       if (kStep && (fl & kNew) && !rope) raise_flag(a.status, PA_FLAG_POSITION_OOB);
-      const bool fresh = rope && ok && (fl & kNew);  // the new token's K and V land in this tile
-      const bool trig = rope && (first || fresh);    // stage the cos/sin row
-      // first cache row of the tile: (physical block * Hkv + KV head) * 16
-      const int y = ok ? (blk * Hkv + (fl >> 16)) * kBlockSize : 0;
       descs[st] = make_int4(seg, fl | (ok ? static_cast<int>(kHasData) : 0), slot, y);
-      const uint32_t bar = bars + 8 * st;
-      const uint32_t dst = tiles + st * kStageB;
-      const uint32_t bytes = (ok ? 2u * L::kTile : 0u) + (first ? static_cast<uint32_t>(G) * 256u : 0u) +
-                             (trig ? kHeadDim * 4u : 0u) + (fresh ? kHeadDim * 4u : 0u);
+      if (bytes) mbar_arrive_expect_tx(bar, bytes);
+      else mbar_arrive(bar);
+    }
+    // The copies of one job leave from different lanes at once (one thread issues its copies
+    // one after another), once lane 0 has armed the stage's barrier.
+    __syncwarp();
+    if (lane < 6 && bytes) {
       fence_proxy_async_smem();
-      if (bytes) {
-        mbar_arrive_expect_tx(bar, bytes);
-        if (ok) {
-          if constexpr (kFp8) {
-            tma_load_2d(dst, &tm_k, 0, y, bar);
-            tma_load_2d(dst + L::kTile, &tm_v, 0, y, bar);
-          } else {
-            tma_load_3d(dst, &tm_k, 0, y, 0, bar);
-            tma_load_3d(dst + L::kTile, &tm_v, 0, y, 0, bar);
-          }
-        }
-        if (first) {  // the segment's G query heads: heads seg * G .. seg * G + G - 1 of q
-          const size_t head0 = static_cast<size_t>(seg) * G;
-          bulk_copy_g2s(dst + L::kQOff, a.q + head0 * kHeadDim, static_cast<uint32_t>(G) * 256u, bar);
-        }
-        if (trig)
-          bulk_copy_g2s(dst + L::kCosSinOff, a.cos_sin + static_cast<size_t>(pos) * kHeadDim, kHeadDim * 4u, bar);
-        if (fresh) {  // row seg of the [S, Hkv] new-token rows
-          const size_t row = static_cast<size_t>(seg) * kHeadDim;
-          bulk_copy_g2s(dst + L::kNewKOff, a.k_new + row, kHeadDim * 2u, bar);
-          bulk_copy_g2s(dst + L::kNewVOff, a.v_new + row, kHeadDim * 2u, bar);
-        }
-      } else {
-        mbar_arrive(bar);
+      if (lane == 0 && ok) {
+        if constexpr (kFp8) tma_load_2d(dst, &tm_k, 0, y, bar);
+        else tma_load_3d(dst, &tm_k, 0, y, 0, bar);
+      } else if (lane == 1 && ok) {
+        if constexpr (kFp8) tma_load_2d(dst + L::kTile, &tm_v, 0, y, bar);
+        else tma_load_3d(dst + L::kTile, &tm_v, 0, y, 0, bar);
+      } else if (lane == 2 && q_rows) {  // the segment's G query heads: heads seg * G .. + G - 1
+        bulk_copy_g2s(dst + L::kQOff, a.q + static_cast<size_t>(seg) * G * kHeadDim,
+                      static_cast<uint32_t>(G) * 256u, bar);
+      } else if (lane == 3 && trig) {
+        bulk_copy_g2s(dst + L::kCosSinOff, a.cos_sin + static_cast<size_t>(pos) * kHeadDim, kHeadDim * 4u, bar);
+      } else if (lane == 4 && fresh) {  // row seg of the [S, Hkv] new-token rows
+        bulk_copy_g2s(dst + L::kNewKOff, a.k_new + static_cast<size_t>(seg) * kHeadDim, kHeadDim * 2u, bar);
+      } else if (lane == 5 && fresh) {
+        bulk_copy_g2s(dst + L::kNewVOff, a.v_new + static_cast<size_t>(seg) * kHeadDim, kHeadDim * 2u, bar);
       }
     }
     return true;
@@ -384,12 +390,37 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
+  uint32_t gx = 0;  // gather: this lane's XOR of the piece's tile words
   auto consume = [&](int st) {
     const int4 d = descs[st];
     const uint32_t fl = static_cast<uint32_t>(d.y);
     const uint32_t kt = tiles + st * kStageB;
     const uint32_t vt = kt + (kFp8 ? L::kTile : 2 * kHalfBytes);
     unsigned char* const stage = smem_raw + (kt - raw);  // generic address of the stage
+    if constexpr (kGather) {
+      // The stage's 8 KiB are [K cols 0-63 | K cols 64-127 | V cols 0-63 | V cols 64-127], each
+      // 16 rows of 128 bytes whose 16-byte chunks the swizzle permutes within the row: chunk c
+      // (16 bytes at 16 c) lies in row (c / 8) % 16.  XOR the words of the valid rows.
+      if (fl & kFirst) gx = 0;
+      if (fl & kHasData) {
+        const int valid = static_cast<int>((fl >> 8) & 0xffu);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = lane + 32 * i;
+          if (((c >> 3) & 15) < valid) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(stage + 16 * c);
+            gx ^= wv.x ^ wv.y ^ wv.z ^ wv.w;
+          }
+        }
+      }
+      if (fl & kLast) {
+        uint32_t x = gx;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x ^= __shfl_xor_sync(kFullMask, x, o);
+        if (lane == 0) atomicXor(a.gather_xor + d.x, x);
+      }
+      return;
+    }
     if (fl & kFirst) {
       if constexpr (kFp8) {
         // B fragments in the order the E4M3 K fragments come in (k index permuted, see
@@ -931,6 +962,11 @@ cudaError_t persistent_ctas(int* ctas) {
     auto kernel = decode_partition_kernel<kStep, kFp8>;
     err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
+    if (!kStep && !kFp8) {  // the gather runs the same kernel shape
+      err = cudaFuncSetAttribute(decode_partition_kernel<false, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (err != cudaSuccess) return err;
+    }
     int sms = 0, per_sm = 0;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
@@ -943,7 +979,7 @@ cudaError_t persistent_ctas(int* ctas) {
   return cudaSuccess;
 }
 
-template <bool kStep, bool kFp8>
+template <bool kStep, bool kFp8, bool kGather = false>
 cudaError_t launch_partition(DecodeArgs& a, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const cudaLaunchAttribute* attr, cudaStream_t stream) {
   int max_ctas = 0;
@@ -963,7 +999,7 @@ cudaError_t launch_partition(DecodeArgs& a, const CUtensorMap& tm_k, const CUten
   cfg.stream = stream;
   cfg.attrs = const_cast<cudaLaunchAttribute*>(attr);
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_partition_kernel<kStep, kFp8>, tm_k, tm_v, a);
+  return cudaLaunchKernelEx(&cfg, decode_partition_kernel<kStep, kFp8, kGather>, tm_k, tm_v, a);
 }
 
 }  // namespace
@@ -1020,6 +1056,19 @@ bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* 
   table[slot] = Entry{cache, rows, fp8, m};
   *out = m;
   return true;
+}
+
+cudaError_t launch_gather(const DecodeArgs& args, cudaStream_t stream) {
+  DecodeArgs a = args;
+  if (a.num_seqs > kMaxDecodeSeqs) return cudaErrorInvalidValue;
+  const long long rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * kBlockSize;
+  CUtensorMap tm_k, tm_v;
+  if (!cache_tensor_map(a.k_cache, rows, false, &tm_k) || !cache_tensor_map(a.v_cache, rows, false, &tm_v))
+    return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  return launch_partition<false, false, true>(a, tm_k, tm_v, attr, stream);
 }
 
 cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {

@@ -101,6 +101,17 @@ def test_prefill_full_size_sampled(pa, orc, name):
     check_status_clean(pa)
 
 
+@pytest.mark.parametrize("name", W.PREFILL_WORKLOADS)
+def test_prefill_full_size_every_row(pa, orc, name):
+    """Both full-size prefill workloads, every query row of every head against the oracle's
+    whole prefill: the last-wave tiles (the cheapest, scheduled last) included."""
+    w = W.make_prefill(name)
+    got = run_prefill(pa, w)
+    ref, _ = orc.prefill(w.q, w.q_start, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale)
+    assert_out_close(got, ref, name)
+    check_status_clean(pa)
+
+
 def test_prefill_bad_sequences_are_flagged_and_skipped(pa, orc):
     w = W.build_prefill("pf_bad", [40, 50, 30], [40, 20, 30], 32, 104)
     ctx = w.context_lens.copy()

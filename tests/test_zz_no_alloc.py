@@ -4,8 +4,9 @@ Some callers may not allocate while a decode step runs: an engine that has hande
 HBM to its KV-cache pool, a plugin whose enqueue path forbids allocation, a real-time loop
 that must not take allocator locks.  This entry point runs the same decode with the
 library's built-in scratch array instead of a caller-provided workspace.  The test calls it
-through the C ABI and checks it against pa_decode with a caller workspace, on two calls in a
-row with different inputs (the scratch keeps the previous call's contents), and checks that
+through the C ABI and checks it bit for bit against pa_decode with a caller workspace and
+against the fp64 oracle, on two calls in a row with different inputs after a call that left
+NaN partials in the scratch (the scratch keeps the previous call's contents), and checks that
 a call needing more scratch than the array holds is refused without launching anything.
 This file is collected last so that a failure here stops a -x run after every other test.
 """
@@ -57,7 +58,17 @@ def prepared(name, orc):
 
 
 def test_static_workspace_matches_decode_on_two_calls(pa):
+    """The static entry point runs the same kernels with the same split as pa_decode, so its
+    output is the same bits; both agree with the oracle.  Before the two calls, a call of a
+    different shape with a NaN query fills the scratch with NaN partial results, so a call that
+    read a partial it did not write itself would show NaN or differ."""
     orc = oracle.default()
+    w0, d0 = prepared("prefix32", orc)
+    d0.q.fill_(float("nan"))
+    poison = torch.empty_like(d0.q)
+    assert call_static(pa, d0, w0, 512, poison) == pa.PA_OK
+    torch.cuda.synchronize()
+    assert torch.isnan(poison.float()).all()
     for name in ("mix64", "long4"):               # two calls in a row, different shapes
         w, d = prepared(name, orc)
         P = w.partition_tokens            # mix64: even split; long4: 512-token partitions
@@ -70,11 +81,14 @@ def test_static_workspace_matches_decode_on_two_calls(pa):
         assert call_static(pa, d, w, P, out) == pa.PA_OK
         torch.cuda.synchronize()
         got = host_bits(out)
-        want = host_bits(ref)
+        assert np.array_equal(got, host_bits(ref)), name
+        q = W.bf16_bits_to_f32(host_bits(d.q)).astype(np.float64)
+        kc = host_bits(d.k_cache)
+        vc = host_bits(d.v_cache)
+        want, _ = orc.decode(host_bits(d.q), kc, vc, w.block_tables, w.context_lens, w.scale)
         g = W.bf16_bits_to_f32(got).astype(np.float64)
-        r = W.bf16_bits_to_f32(want).astype(np.float64)
-        assert np.isfinite(g).all()
-        assert (np.abs(g - r) <= OUT_ATOL + OUT_RTOL * np.abs(r)).all(), name
+        assert np.isfinite(g).all() and np.isfinite(q).all()
+        assert (np.abs(g - want) <= OUT_ATOL + OUT_RTOL * np.abs(want)).all(), name
         rc, flags = pa.get_device_status()
         assert rc == 0 and flags == 0
 
