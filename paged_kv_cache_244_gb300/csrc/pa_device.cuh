@@ -1,5 +1,6 @@
 // Device helpers shared by the sm_103a kernels: inline PTX for mbarriers, bulk copies into
-// shared memory, programmatic dependent launch, the bounded wait and the status flags.
+// shared memory, programmatic dependent launch, tcgen05 tensor-core and tensor-memory
+// operations, the bounded wait and the status flags.
 #pragma once
 
 #include <cstdint>
@@ -168,6 +169,78 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+
+// ---- tcgen05: 5th-generation tensor core, accumulators in tensor memory (TMEM) ----------
+// TMEM addresses: lane (row) in bits 31..16, column in bits 15..0.  A warp may access the 32
+// lanes 32 (warp % 4) .. 32 (warp % 4) + 31.
+
+// Allocate `cols` columns (a power of two >= 32) for this CTA; the base address is written to
+// shared memory at `slot`.  Warp-collective; one warp allocates and later frees.
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(cols)
+               : "memory");
+}
+// This CTA allocates no more: other CTAs on the SM may allocate without waiting for it.
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+// Order tcgen05 operations across a thread synchronisation (barrier, mbarrier, __syncthreads):
+// `before` in the thread whose tcgen05 work precedes the sync, `after` in the one that follows.
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D (TMEM) = A (shared, descriptor a) * B (shared, descriptor b) (+ D if accumulate), one
+// instruction of kind::f16 described by idesc (bf16 operands, fp32 accumulator).  Issued by one
+// thread; runs asynchronously.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+// Arrive once on the mbarrier when every tcgen05 operation this thread issued so far is done.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+#define PA_R32(v)                                                                                    \
+  "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),     \
+      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),         \
+      "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),       \
+      "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),       \
+      "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+#define PA_W32(v)                                                                                    \
+  "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),  \
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),  \
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), \
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+#define PA_OPS32                                                                                     \
+  "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, "  \
+  "%21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}"
+// 32 consecutive 32-bit columns of this thread's lane (warp-collective); complete after
+// tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 " PA_OPS32 ", [%32];" : PA_R32(v) : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+               "%10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, "
+               "%27, %28, %29, %30, %31, %32};" ::"r"(taddr), PA_W32(v)
+               : "memory");
+}
+#undef PA_R32
+#undef PA_W32
+#undef PA_OPS32
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---- bf16 ------------------------------------------------------------------------------
 // Widen a packed pair of bf16 (low half = element 0) to two floats: bf16 is the top half

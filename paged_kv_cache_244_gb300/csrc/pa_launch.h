@@ -110,9 +110,11 @@ struct PrefillArgs {
   unsigned* status;
 };
 
-// TMA tensor map of a paged cache viewed as [num_blocks * Hkv * 16][128] (bf16 boxes of 64 x 16,
-// or E4M3 boxes of 128 x 16), 128-byte swizzle; encoded once per (address, rows, type).
-bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* out);
+// TMA tensor map of a paged cache viewed as [num_blocks * Hkv * 16][128], 128-byte swizzle;
+// encoded once per (address, rows, type, box).  bf16: a 3-D view (64 columns, rows, 2 halves of
+// 64 columns) whose box is 64 x 16 x box_halves (both halves of a tile: 4 KiB as two 2 KiB
+// halves; or one half); E4M3: boxes of 128 x 16 bytes.
+bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* out, int box_halves = 2);
 
 cudaError_t launch_rope_kv_store(const RopeArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);

@@ -1009,14 +1009,18 @@ cudaError_t launch_partition(DecodeArgs& a, const CUtensorMap& tm_k, const CUten
 // 128-col row is 256 bytes, wider than the swizzle span, so the map is 3-D -- (col within a
 // 64-col half, row, half) with strides 256 bytes (row) and 128 bytes (half) -- and the box
 // (64, 16, 2) lands a tile in shared memory as its two 2 KiB halves, cols 0-63 of the 16 rows
-// followed by cols 64-127.  Encoded maps are cached by (address, rows, type).
-bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* out) {
+// followed by cols 64-127; the box (64, 16, 1) lands one half (the prefill kernel places the K
+// halves of neighbouring blocks side by side).  Encoded maps are cached by (address, rows, type,
+// box).
+bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* out, int box_halves) {
   struct Entry {
     const void* ptr;
     long long rows;
     bool fp8;
+    int halves;
     CUtensorMap map;
   };
+  if (box_halves != 1 && box_halves != 2) return false;
   // Room for the K and V caches of every layer of a large model in both element types; the
   // oldest entry is replaced when it is full.
   constexpr int kEntries = 512;
@@ -1025,7 +1029,8 @@ bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* 
   static int used = 0, next = 0;
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < used; ++i)
-    if (table[i].ptr == cache && table[i].rows == rows && table[i].fp8 == fp8) {
+    if (table[i].ptr == cache && table[i].rows == rows && table[i].fp8 == fp8 &&
+        (fp8 || table[i].halves == box_halves)) {
       *out = table[i].map;
       return true;
     }
@@ -1045,7 +1050,7 @@ bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* 
   } else {
     cuuint64_t dims[3] = {64, n, 2};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2, 128};
-    cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(kBlockSize), 2u};
+    cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(kBlockSize), static_cast<cuuint32_t>(box_halves)};
     cuuint32_t estr[3] = {1, 1, 1};
     rc = encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(cache), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1053,7 +1058,7 @@ bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* 
   }
   if (rc != CUDA_SUCCESS) return false;
   const int slot = used < kEntries ? used++ : (next++ % kEntries);
-  table[slot] = Entry{cache, rows, fp8, m};
+  table[slot] = Entry{cache, rows, fp8, box_halves, m};
   *out = m;
   return true;
 }

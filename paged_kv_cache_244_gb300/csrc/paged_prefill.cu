@@ -1,4 +1,4 @@
-// Paged (chunked) prefill attention for sm_103a.
+// Paged (chunked) prefill attention for sm_103a on the tcgen05 tensor cores.
 //
 // "Pico-vLLM：从零手写的工业级LLM推理引擎实现", §2 Kernel层 (PagedAttention prefill kernel, after
 // the FlashAttention work); "从零实现 LLM 推理引擎：深挖 vLLM 的六大核心优化", §3.1 (16-token blocks,
@@ -9,25 +9,36 @@
 // in the paged cache; context_lens[s] counts every cached token including them.  Query i sits
 // at position p_i = context_lens[s] - n_s + i and attends causally to cached tokens 0..p_i.
 //
-// CTA = (sequence, KV head g, tile of 16 query tokens), one warp per query head of the group
-// (G <= 8 warps), so every K/V tile brought in is used by all G heads.  Each warp holds its
-// 16 x 128 Q tile as MMA A fragments and walks the key blocks 0 .. p_last / 16:
-//   S (16 x 64) = Q K^T      64 mma.sync m16n8k16 (bf16 -> fp32), B = K via ldmatrix
-//   online softmax           per row, in the log2 domain, the scale folded into one FMA per
-//                            exponent; a row's shift moves only when its maximum passes it by
-//                            more than 8 (P <= 2^8, few O rescales); causal mask t > p_i only on
-//                            the stages that reach the tile's diagonal; V rows past the context
-//                            zeroed in the operand (they may hold anything), in the context's
-//                            last block only
-//   O (16 x 128) += P V      64 MMAs; P is the S accumulators rounded to bf16 (the C layout of
-//                            two n8 tiles is the A layout of one k16 step), B = V via
-//                            transposing ldmatrix
-// Keys come 64 at a time (4 blocks) through a 2-stage ring, so the softmax bookkeeping and the
-// handshakes are paid once per 128 MMAs: the warp whose release of stage j is the last of the
-// G (a shared-memory count) issues at once the TMA tensor loads of stage j + 2 (one box per K
-// tile and per V tile, landing as two 64-column halves, 128-byte swizzle), so no warp waits
-// for the others.  Measured against 3 stages of 48 keys, 2 of 64 are 1-2% faster; 4 of 32
-// were slower.  All waits are bounded.
+// CTA = (sequence, KV head g, tile of Tq = floor(128 / G) query tokens).  Its 128 matrix rows
+// are the (query, head) pairs of the GQA group, row r = i G + h for query i and head g G + h,
+// so every K/V tile brought in serves all G heads and the tensor core sees M = 128 rows.  The
+// Q tile (128 x 128 bf16) stays in shared memory; keys come 32 at a time (two blocks) through a
+// 3-stage ring filled by TMA.  Per stage j:
+//   S_j (128 x 32, fp32, TMEM)  = Q K_j^T      8 tcgen05.mma, M = 128, N = 32, K = 16 each
+//   softmax (one thread per row) reads S_j with tcgen05.ld, masks causally, keeps a lazy
+//   row shift in the log2 domain (it moves only when the row maximum passes it by more than 8,
+//   so P <= 2^8 and O is rarely rescaled), writes P_j = bf16(2^(scale_log2 s - shift)) to
+//   shared memory and adds the same rounded values to the row sum
+//   O (128 x 128, fp32, TMEM)  += P_j V_j      2 tcgen05.mma (one per key block), M = N = 128,
+//                                              K = 16, V read with its dims contiguous
+// Warps 0-3 run the softmax (warp w owns TMEM lanes 32w..32w+31), warp 4 issues the TMA loads,
+// one thread of warp 5 issues the MMAs.  The MMA thread issues S_{j+1} before it waits for
+// P_j, so the tensor core computes the next scores while the softmax works; two S buffers in
+// TMEM and two P buffers in shared memory (the two 64-byte halves of each 128-byte P row) keep
+// the stages apart.  TMEM per CTA: S 2 x 32 columns + O 128 columns (256 allocated); shared
+// memory ~97 KB, so two CTAs share an SM and the tensor core alternates between them.
+//
+// Shared-memory operands use the 128-byte swizzle (16-byte chunk c of a 128-byte row r at
+// c ^ (r % 8), 8-row atoms of 1024 bytes):
+//   Q     two 64-column halves of 128 rows, 16 KiB each (K-major A operand)
+//   stage K half 0 of both blocks (rows 0-31, 4 KiB), K half 1 (4 KiB), then V of block 0 and
+//         of block 1 (4 KiB each, as two 2 KiB halves of 16 rows): K is the K-major B operand
+//         of S (N = 32 keys), V the MN-major B operand of P V (N = 128 dims)
+//   P     128 rows of 128 bytes; stage j uses bytes 64 (j % 2) .. +63 of each row (32 keys)
+// Keys past the context in the context's last block may hold anything: their scores are
+// masked and their V rows zeroed in shared memory before P V.  A block id out of range is not
+// loaded: its keys are masked and its P V step skipped.  Every wait is bounded; a timeout
+// raises PA_FLAG_TIMEOUT and the CTA drains its copies and MMAs before it exits.
 // Tiles are scheduled latest first over the whole grid: the last tiles of a sequence see the
 // most keys.
 
@@ -37,31 +48,48 @@
 
 #include "pa_device.cuh"
 #include "pa_launch.h"
+#include "umma_desc.h"
 
 namespace pa {
 namespace {
 
-constexpr int kQTile = 16;                          // query tokens per CTA
-constexpr int kKB = 4;                              // key blocks (16 tokens each) per stage
-constexpr int kPfStages = 2;
-constexpr int kPfMaxWarps = 8;                      // G <= 8
-constexpr int kPfHalf = kBlockSize * 128;           // 16 rows x 64 bf16
-constexpr int kPfBlockBytes = 2 * kTileBytes;       // K tile + V tile of one key block
-constexpr int kPfStageBytes = kKB * kPfBlockBytes;  // 32 KiB
-constexpr int kPfQBytes = kQTile * kHeadDim * 2;    // one warp's Q tile: 4 KiB
-// header: per stage a full mbarrier, a block-present mask and a release count; then the
-// 1024-aligned stages and the Q tiles
-constexpr int kPfHeader = 1024;
-constexpr int kPfSmem = kPfHeader + kPfStages * kPfStageBytes + kPfMaxWarps * kPfQBytes + 1024;
+constexpr int kPfRows = 128;                        // MMA rows: (query, head) pairs per CTA
+constexpr int kPfKB = 2;                            // key blocks per stage
+constexpr int kPfKeys = kPfKB * kBlockSize;         // 32 keys per stage
+constexpr int kPfStages = 3;
+constexpr int kPfHalf = kBlockSize * 128;           // 16 rows x 64 bf16: 2 KiB
+constexpr int kPfKHalfBytes = kPfKB * kPfHalf;      // one K half of the stage's blocks: 4 KiB
+constexpr int kPfVOff = 2 * kPfKHalfBytes;          // V tiles after the two K halves
+constexpr int kPfStageBytes = kPfVOff + kPfKB * kTileBytes;   // 16 KiB
+constexpr int kPfQHalfBytes = kPfRows * 128;        // 16 KiB
+constexpr int kPfQBytes = 2 * kPfQHalfBytes;        // 32 KiB
+constexpr int kPfPBytes = kPfRows * 128;            // 16 KiB
+constexpr int kPfHeader = 256;                      // mbarriers, present masks, TMEM address
+constexpr int kPfSmem = kPfHeader + 1024 + kPfQBytes + kPfStages * kPfStageBytes + kPfPBytes;
+constexpr int kPfThreads = 192;                     // 4 softmax warps, TMA warp, MMA warp
+constexpr uint32_t kPfTmemCols = 256;
+constexpr uint32_t kPfSCol = 0;                     // S buffers: columns 0-31 and 32-63
+constexpr uint32_t kPfOCol = 64;                    // O: columns 64-191
 
-__global__ void __maxnreg__(168)  // two CTAs of up to 6 warps per SM; 8 warps still fit one
-prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+// header layout (byte offsets)
+constexpr int kBarKvFull = 0;                       // [3] TMA -> MMA, softmax
+constexpr int kBarKvEmpty = 24;                     // [3] MMA (P V done) -> TMA
+constexpr int kBarSFull = 48;                       // [2] MMA (S done) -> softmax
+constexpr int kBarPFull = 64;                       // [2] softmax (P written) -> MMA, 128 arrivals
+constexpr int kBarOReady = 80;                      // MMA (P V done) -> softmax
+constexpr int kBarDone = 88;                        // MMA thread: its last MMAs finished
+constexpr int kPresent = 96;                        // [3] int: bit i = block i of the stage loaded
+constexpr int kTmemSlot = 112;
+
+__global__ void __launch_bounds__(kPfThreads, 2)
+prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant__ CUtensorMap tm_v,
                const PrefillArgs a) {
   extern __shared__ unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int Hkv = a.num_kv_heads;
   const int G = a.num_q_heads / Hkv;
+  const int Tq = kPfRows / G;                       // query tokens per CTA
   // CTAs start in the order of their linear index (x fastest).  Consecutive indices take the
   // same query tile of every (sequence, KV head) pair, latest tile first, so the CTAs with the
   // most keys start first across the whole grid and the last wave holds the cheapest ones.
@@ -83,260 +111,291 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (threadIdx.x == 0 && tile == 0 && g == 0) raise_flag(a.status, PA_FLAG_CONTEXT_LEN_OOB);
     return;
   }
-  const int i0 = tile * kQTile;
+  const int i0 = tile * Tq;
   if (i0 >= n) return;
-  const int rows = min(kQTile, n - i0);
+  const int rows_q = min(Tq, n - i0);               // real queries of the tile
   const int pos0 = ctx - n + i0;                    // position of the tile's first query
-  const int nblocks = (pos0 + rows - 1) / kBlockSize + 1;
-  const int nst = (nblocks + kKB - 1) / kKB;        // stages of kKB key blocks
+  const int nblocks = (pos0 + rows_q - 1) / kBlockSize + 1;
+  const int nst = (nblocks + kPfKB - 1) / kPfKB;    // stages of kPfKB key blocks
 
   const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t full = raw;                        // kPfStages x 8 bytes
-  int* present = reinterpret_cast<int*>(smem_raw + 8 * kPfStages);   // bit i: block i loaded
-  // per stage: releases so far, G a round; the release that completes a round refills it
-  unsigned* released = reinterpret_cast<unsigned*>(smem_raw + 12 * kPfStages);
-  const uint32_t stages = (raw + kPfHeader + 1023u) & ~1023u;
-  const uint32_t qtiles = stages + kPfStages * kPfStageBytes;
+  const uint32_t qbuf = (raw + kPfHeader + 1023u) & ~1023u;
+  const uint32_t stages = qbuf + kPfQBytes;
+  const uint32_t pbuf = stages + kPfStages * kPfStageBytes;
+  volatile int* present = reinterpret_cast<volatile int*>(smem_raw + kPresent);
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPfStages; ++i) {
-      mbar_init(full + 8 * i, 1);
-      released[i] = 0u;
+      mbar_init(raw + kBarKvFull + 8 * i, 1);
+      mbar_init(raw + kBarKvEmpty + 8 * i, 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(raw + kBarSFull + 8 * i, 1);
+      mbar_init(raw + kBarPFull + 8 * i, 128);
+    }
+    mbar_init(raw + kBarOReady, 1);
+    mbar_init(raw + kBarDone, 1);
     fence_mbar_init();
-    prefetch_tensor_map(&tm_k);
+    prefetch_tensor_map(&tm_kh);
     prefetch_tensor_map(&tm_v);
   }
-  __syncthreads();
-
-  // Bring key blocks kKB j .. kKB j + kKB - 1 into stage j % kPfStages (one thread).
-  const int32_t* bt_row = a.block_tables + static_cast<size_t>(s) * a.max_blocks;
-  auto issue = [&](int j) {
-    const int st = j % kPfStages;
-    int blk[kKB];
-    int mask = 0;
-#pragma unroll
-    for (int i = 0; i < kKB; ++i) {
-      const int b = kKB * j + i;
-      blk[i] = b < nblocks ? bt_row[b] : -1;
-      if (b < nblocks && blk[i] >= 0 && blk[i] < a.num_blocks) mask |= 1 << i;
-      else if (b < nblocks) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
-    }
-    present[st] = mask;
-    const uint32_t bar = full + 8 * st;
-    const uint32_t dst = stages + st * kPfStageBytes;
-    fence_proxy_async_smem();
-    if (mask) {
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask)) * kPfBlockBytes);
-#pragma unroll
-      for (int i = 0; i < kKB; ++i) {
-        if (!(mask & (1 << i))) continue;
-        const int y = (blk[i] * Hkv + g) * kBlockSize;
-        const uint32_t d = dst + i * kPfBlockBytes;
-        tma_load_3d(d, &tm_k, 0, y, 0, bar);              // both 64-col halves of the K tile
-        tma_load_3d(d + 2 * kPfHalf, &tm_v, 0, y, 0, bar);
-      }
-    } else {
-      mbar_arrive(bar);
-    }
-  };
-  if (threadIdx.x == 0)
-    for (int j = 0; j < min(kPfStages, nst); ++j) issue(j);
-
-  // ---- this warp's Q tile (query head g * G + warp) as A fragments ------------------------
-  const int h = g * G + warp;
-  const int gq = lane >> 2, cq = lane & 3;          // fragment row group / column pair
-  const int mi = lane >> 3, r = lane & 7;           // ldmatrix: matrix / row this lane addresses
-  const uint32_t qs = qtiles + warp * kPfQBytes;
+  // Q tile into shared memory by every thread: row r = i G + h (zero past the tile's queries),
+  // 16 chunks of 16 bytes, chunk c in half c / 8 at position (c % 8) ^ (r % 8).
   {
-    // row = query i0 + row (zero past the tile), 16 chunks of 16 bytes, chunk c at c ^ (row % 8)
-    unsigned char* qgen = smem_raw + (qs - raw);
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int idx = it * 32 + lane;
-      const int row = idx >> 4, c = idx & 15;
+    unsigned char* qgen = smem_raw + (qbuf - raw);
+    for (int idx = threadIdx.x; idx < kPfRows * 16; idx += kPfThreads) {
+      const int r = idx >> 4, c = idx & 15;
+      const int i = r / G, h = r - (r / G) * G;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (row < rows)
-        v = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(q0 + i0 + row) * a.num_q_heads + h) *
-                                                     kHeadDim)[c];
-      *reinterpret_cast<uint4*>(qgen + row * 256 + ((c ^ (row & 7)) << 4)) = v;
+      if (i < rows_q)
+        v = reinterpret_cast<const uint4*>(
+            a.q + (static_cast<size_t>(q0 + i0 + i) * a.num_q_heads + g * G + h) * kHeadDim)[c];
+      *reinterpret_cast<uint4*>(qgen + (c >> 3) * kPfQHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
     }
   }
-  __syncwarp();
-  uint32_t qa[8][4];
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const int row = r + 8 * (mi & 1);
-    const int c = 2 * kk + (mi >> 1);
-    ldsm_x4(qs + row * 256 + ((c ^ r) << 4), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+  fence_proxy_async_smem();                         // the tensor core reads Q through the async proxy
+  if (warp == 0) {
+    tmem_alloc(raw + kTmemSlot, kPfTmemCols);
+    tmem_relinquish();
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem_raw + kTmemSlot);
 
-  float o[16][4];
+  if (warp == 4) {
+    // ---- TMA producer: stage j holds key blocks 2j, 2j + 1 -------------------------------
+    if (lane == 0) {
+      const int32_t* bt_row = a.block_tables + static_cast<size_t>(s) * a.max_blocks;
+      int issued = 0;
+      bool failed = false;
+      for (int j = 0; j < nst; ++j) {
+        const int st = j % kPfStages;
+        if (j >= kPfStages &&
+            !mbar_wait_bounded(raw + kBarKvEmpty + 8 * st, ((j / kPfStages) - 1) & 1)) {
+          failed = true;
+          break;
+        }
+        int blk[kPfKB];
+        int mask = 0;
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows gq, gq + 8
-  const int p0 = pos0 + gq, p1 = pos0 + gq + 8;               // their positions
-  bool failed = false;
-  int seen = 0;                                               // stages this warp waited for
-
-  for (int j = 0; j < nst; ++j) {
-    const int st = j % kPfStages;
-    if (!mbar_wait_bounded(full + 8 * st, (j / kPfStages) & 1)) {
-      failed = true;
-      break;
-    }
-    seen = j + 1;
-    const int mask = present[st];
-    const uint32_t stage = stages + st * kPfStageBytes;
-    // S = Q K^T for the stage's 16 kKB keys: n8 tile 2i (+1) = keys 0-7 (8-15) of block i.
-    // k steps outside, blocks inside: 2 kKB independent accumulator chains between two MMAs
-    // of one chain (the MMAs issue in program order).
-    float sc[2 * kKB][4];
+        for (int i = 0; i < kPfKB; ++i) {
+          const int b = kPfKB * j + i;
+          blk[i] = b < nblocks ? bt_row[b] : -1;
+          if (b < nblocks && blk[i] >= 0 && blk[i] < a.num_blocks) mask |= 1 << i;
+          else if (b < nblocks) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
+        }
+        present[st] = mask;
+        const uint32_t bar = raw + kBarKvFull + 8 * st;
+        const uint32_t dst = stages + st * kPfStageBytes;
+        if (mask) {
+          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask)) * (2 * kTileBytes));
 #pragma unroll
-    for (int nt = 0; nt < 2 * kKB; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-    const int key = r + 8 * (mi >> 1);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int chunk = (2 * kk + (mi & 1)) & 7;
-      const uint32_t ko = (kk >> 2) * kPfHalf + key * 128 + ((chunk ^ r) << 4);
-#pragma unroll
-      for (int i = 0; i < kKB; ++i) {
-        if (!(mask & (1 << i))) continue;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(stage + i * kPfBlockBytes + ko, b0, b1, b2, b3);
-        mma_bf16_16816(sc[2 * i], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-        mma_bf16_16816(sc[2 * i + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+          for (int i = 0; i < kPfKB; ++i) {
+            if (!(mask & (1 << i))) continue;
+            const int y = (blk[i] * Hkv + g) * kBlockSize;
+            tma_load_3d(dst + i * kPfHalf, &tm_kh, 0, y, 0, bar);                  // K cols 0-63
+            tma_load_3d(dst + kPfKHalfBytes + i * kPfHalf, &tm_kh, 0, y, 1, bar);  // K cols 64-127
+            tma_load_3d(dst + kPfVOff + i * kTileBytes, &tm_v, 0, y, 0, bar);      // V, both halves
+          }
+        } else {
+          mbar_arrive(bar);
+        }
+        issued = j + 1;
       }
+      if (failed) raise_flag(a.status, PA_FLAG_TIMEOUT);
+      // Copies still in flight can only be those of the last kPfStages fills: let them land
+      // (immediate in a normal run, where the MMAs consumed every stage) before the CTA exits.
+      for (int j = max(0, issued - kPfStages); j < issued; ++j)
+        mbar_wait_bounded(raw + kBarKvFull + 8 * (j % kPfStages), (j / kPfStages) & 1, 10000000ull);
     }
-    // Scores stay unscaled until the exponent (scale > 0, so the row maxima are the same).
-    // Causal mask and missing blocks -> -inf, only on a stage that reaches past the tile's first
-    // query or lacks a block; the others lie wholly before every query of the tile.
-    // sc[nt]: [0] (row gq, key 8nt+2cq), [1] (gq, +1), [2] (gq+8, 8nt+2cq), [3] (gq+8, +1)
-    if (mask != (1 << kKB) - 1 || kKB * kBlockSize * (j + 1) - 1 > pos0) {
-      const int tbase = kKB * kBlockSize * j + 2 * cq;
+  } else if (warp == 5) {
+    // ---- MMA issuer --------------------------------------------------------------------------
+    if (lane == 0) {
+      const uint32_t id_s = umma_idesc_bf16(kPfRows, kPfKeys, false, false);
+      const uint32_t id_pv = umma_idesc_bf16(kPfRows, kHeadDim, false, true);
+      bool failed = false;
+      bool o_started = false;
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % kPfStages;
+        if (!mbar_wait_bounded(raw + kBarKvFull + 8 * st, (j / kPfStages) & 1)) return false;
+        tc_fence_after();
+        const uint32_t kst = stages + st * kPfStageBytes;
 #pragma unroll
-      for (int nt = 0; nt < 2 * kKB; ++nt) {
-        const bool here = (mask >> (nt >> 1)) & 1;
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = umma_smem_desc(qbuf + (kk >> 2) * kPfQHalfBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = umma_smem_desc(kst + (kk >> 2) * kPfKHalfBytes + (kk & 3) * 32, 16, 1024);
+          umma_bf16(tmem + kPfSCol + kPfKeys * (j & 1), ad, bd, id_s, kk > 0);
+        }
+        umma_commit(raw + kBarSFull + 8 * (j & 1));
+        return true;
+      };
+      failed = !issue_s(0);
+      for (int j = 0; j < nst && !failed; ++j) {
+        if (j + 1 < nst && !issue_s(j + 1)) {
+          failed = true;
+          break;
+        }
+        if (!mbar_wait_bounded(raw + kBarPFull + 8 * (j & 1), (j >> 1) & 1)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const int st = j % kPfStages;
+        const int mask = present[st];
+        const uint32_t vst = stages + st * kPfStageBytes + kPfVOff;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int t = tbase + 8 * nt + e;
-          if (!(here && t <= p0)) sc[nt][e] = -INFINITY;
-          if (!(here && t <= p1)) sc[nt][2 + e] = -INFINITY;
+        for (int i = 0; i < kPfKB; ++i) {
+          if (!(mask & (1 << i))) continue;
+          const uint64_t ad = umma_smem_desc(pbuf + 64 * (j & 1) + 32 * i, 16, 1024);
+          const uint64_t bd = umma_smem_desc(vst + i * kTileBytes, kPfHalf, 1024);
+          umma_bf16(tmem + kPfOCol, ad, bd, id_pv, o_started);
+          o_started = true;
+        }
+        umma_commit(raw + kBarKvEmpty + 8 * st);
+        umma_commit(raw + kBarOReady);
+      }
+      if (failed) raise_flag(a.status, PA_FLAG_TIMEOUT);
+      // Every MMA issued has finished before the CTA frees TMEM and exits.
+      umma_commit(raw + kBarDone);
+      mbar_wait_bounded(raw + kBarDone, 0);
+    }
+  } else {
+    // ---- softmax: thread = row r of the tile -------------------------------------------------
+    const int r = threadIdx.x;                      // 0..127 = TMEM lane
+    const int i = r / G, h = r - (r / G) * G;
+    const int p_r = pos0 + i;                       // rows past the tile's queries are never stored
+    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float sl = a.scale_log2;
+    // the context's last block, if partial: its V rows valid_last..15 are zeroed before P V
+    const int last_blk = (ctx - 1) / kBlockSize;
+    const int valid_last = ctx - kBlockSize * last_blk;
+    float m = -INFINITY, l = 0.f;
+    bool failed = false;
+    for (int j = 0; j < nst; ++j) {
+      const int st = j % kPfStages;
+      // tcgen05.ld / st are warp-collective: a warp goes on only if all its lanes saw the phase
+      const bool ok = mbar_wait_bounded(raw + kBarSFull + 8 * (j & 1), (j >> 1) & 1) &&
+                      mbar_wait_bounded(raw + kBarKvFull + 8 * st, (j / kPfStages) & 1);
+      if (!__all_sync(kFullMask, ok)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      const int mask = present[st];
+      uint32_t sv[32];
+      tmem_ld32(trow + kPfSCol + kPfKeys * (j & 1), sv);
+      tmem_wait_ld();
+      float sc[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) sc[c] = __uint_as_float(sv[c]);
+      // Scores stay unscaled until the exponent (scale > 0, so the row maxima are the same).
+      // Causal mask and missing blocks -> -inf, only on a stage that reaches past the tile's
+      // first query or lacks a block; the others lie wholly before every query of the tile.
+      if (mask != (1 << kPfKB) - 1 || kPfKeys * (j + 1) - 1 > pos0) {
+        const int lim = p_r - kPfKeys * j;          // keys c <= lim are causal for this row
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (!((mask >> (c / kBlockSize)) & 1) || c > lim) sc[c] = -INFINITY;
+      }
+      float mx = sc[0];
+#pragma unroll
+      for (int c = 1; c < 32; ++c) mx = fmaxf(mx, sc[c]);
+      // Shift m in the log2 domain (scale * log2(e) applied): it moves to the row maximum only
+      // when that exceeds it by more than 8, so P stays at most 2^8 and O is rescaled rarely.
+      const float bs = mx * sl;
+      const float mn = bs > m + 8.f ? bs : m;
+      const float sh = mn == -INFINITY ? 0.f : mn;  // a row with no key yet keeps the shift 0
+      const float alpha = (mn == m || m == -INFINITY) ? 1.f : ex2_ftz(m - sh);
+      m = mn;
+      // P = 2^(scale_log2 s - shift), rounded to bf16 (the MMA operand); the row sum adds the
+      // same rounded values
+      uint32_t pw[16];
+      float ps = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        pw[k] = pack_bf16x2(ex2_ftz(fmaf(sc[2 * k], sl, -sh)), ex2_ftz(fmaf(sc[2 * k + 1], sl, -sh)));
+        ps += bf16lo(pw[k]) + bf16hi(pw[k]);
+      }
+      l = fmaf(l, alpha, ps);
+      // O *= alpha once P V of the previous stage has landed (warp-collective TMEM access)
+      if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
+        // P V of stage j - 1 was issued after S_j, so o_ready has completed j - 1 or j times
+        // here: its parity names the phase of stage j - 1 without ambiguity
+        if (!__all_sync(kFullMask, mbar_wait_bounded(raw + kBarOReady, (j - 1) & 1))) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t ov[32];
+          tmem_ld32(trow + kPfOCol + 32 * q4, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+          tmem_st32(trow + kPfOCol + 32 * q4, ov);
+        }
+        tmem_wait_st();
+      }
+      // Keys past the context in its last block: zero their V rows (both 64-column halves).
+      const int vb = last_blk - kPfKB * j;
+      if (valid_last < kBlockSize && vb >= 0 && vb < kPfKB && ((mask >> vb) & 1)) {
+        const int chunks = (kBlockSize - valid_last) * 16;
+        unsigned char* vt = smem_raw + (stages - raw) + st * kPfStageBytes + kPfVOff + vb * kTileBytes;
+        for (int x = r; x < chunks; x += 128) {
+          const int row = valid_last + (x >> 4), half = (x >> 3) & 1, ch = x & 7;
+          *reinterpret_cast<uint4*>(vt + half * kPfHalf + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-    }
-    float bm0 = -INFINITY, bm1 = -INFINITY;
+      // P row r: keys 0-31 of the stage = 4 chunks, chunk 4 (j % 2) + k at position ^ (r % 8)
+      {
+        unsigned char* prow = smem_raw + (pbuf - raw) + r * 128;
 #pragma unroll
-    for (int nt = 0; nt < 2 * kKB; ++nt) {
-      bm0 = fmaxf(bm0, fmaxf(sc[nt][0], sc[nt][1]));
-      bm1 = fmaxf(bm1, fmaxf(sc[nt][2], sc[nt][3]));
-    }
-#pragma unroll
-    for (int x = 1; x < 4; x <<= 1) {
-      bm0 = fmaxf(bm0, __shfl_xor_sync(kFullMask, bm0, x));
-      bm1 = fmaxf(bm1, __shfl_xor_sync(kFullMask, bm1, x));
-    }
-    // Shifts m0, m1 in the log2 domain (scale * log2(e) applied): a row's shift moves to its
-    // maximum only when that exceeds it by more than 8, so P stays at most 2^8 and O is rescaled
-    // far less often.
-    const float bs0 = bm0 * a.scale_log2, bs1 = bm1 * a.scale_log2;
-    const float mn0 = bs0 > m0 + 8.f ? bs0 : m0, mn1 = bs1 > m1 + 8.f ? bs1 : m1;
-    // a row with no key yet keeps the shift 0 (only rows past the tile can stay that way)
-    const float sh0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float sh1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = ex2_ftz(m0 - sh0), al1 = ex2_ftz(m1 - sh1);
-    m0 = mn0;
-    m1 = mn1;
-    // P = 2^(scale_log2 * s - shift), one FMA and one exp2 per score, rounded to bf16 (the MMA
-    // operand) as A fragments of one k16 step per block; the running sums add the same
-    // rounded values
-    const float sl = a.scale_log2;
-    uint32_t pa[kKB][4];
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int i = 0; i < kKB; ++i) {
-      pa[i][0] = pack_bf16x2(ex2_ftz(fmaf(sc[2 * i][0], sl, -sh0)), ex2_ftz(fmaf(sc[2 * i][1], sl, -sh0)));
-      pa[i][1] = pack_bf16x2(ex2_ftz(fmaf(sc[2 * i][2], sl, -sh1)), ex2_ftz(fmaf(sc[2 * i][3], sl, -sh1)));
-      pa[i][2] = pack_bf16x2(ex2_ftz(fmaf(sc[2 * i + 1][0], sl, -sh0)), ex2_ftz(fmaf(sc[2 * i + 1][1], sl, -sh0)));
-      pa[i][3] = pack_bf16x2(ex2_ftz(fmaf(sc[2 * i + 1][2], sl, -sh1)), ex2_ftz(fmaf(sc[2 * i + 1][3], sl, -sh1)));
-      ps0 += bf16lo(pa[i][0]) + bf16hi(pa[i][0]) + bf16lo(pa[i][2]) + bf16hi(pa[i][2]);
-      ps1 += bf16lo(pa[i][1]) + bf16hi(pa[i][1]) + bf16lo(pa[i][3]) + bf16hi(pa[i][3]);
-    }
-    l0 = fmaf(l0, al0, ps0);
-    l1 = fmaf(l1, al1, ps1);
-    if (__any_sync(kFullMask, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        o[nt][0] *= al0;
-        o[nt][1] *= al0;
-        o[nt][2] *= al1;
-        o[nt][3] *= al1;
+        for (int k = 0; k < 4; ++k) {
+          const int c = 4 * (j & 1) + k;
+          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+              make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
+        }
       }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(raw + kBarPFull + 8 * (j & 1));
     }
-    // O += P V, block by block; two n8 dim tiles per transposing ldmatrix
-    auto pv = [&](int i, uint32_t vm_lo, uint32_t vm_hi) {
-      const uint32_t vt = stage + i * kPfBlockBytes + 2 * kPfHalf;
+    if (failed) {
+      if (lane == 0) raise_flag(a.status, PA_FLAG_TIMEOUT);
+    } else if (__all_sync(kFullMask, mbar_wait_bounded(raw + kBarDone, 0))) {
+      // (the MMA thread commits kBarDone once, after its last P V)
+      // ---- out = O / l for the tile's real rows ------------------------------------------------
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool store = i < rows_q;
+      uint4* dst = reinterpret_cast<uint4*>(
+          a.out + (static_cast<size_t>(q0 + i0 + (store ? i : 0)) * a.num_q_heads + g * G + h) * kHeadDim);
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t ov[32];
+        tmem_ld32(trow + kPfOCol + 32 * q4, ov);
+        tmem_wait_ld();
+        if (store) {
 #pragma unroll
-      for (int d2 = 0; d2 < 8; ++d2) {
-        uint32_t v0, v1, v2, v3;
-        const int key = r + 8 * (mi & 1);
-        const int chunk = (2 * d2 + (mi >> 1)) & 7;
-        ldsm_x4_trans(vt + (d2 >> 2) * kPfHalf + key * 128 + ((chunk ^ r) << 4), v0, v1, v2, v3);
-        mma_bf16_16816(o[2 * d2], pa[i][0], pa[i][1], pa[i][2], pa[i][3], v0 & vm_lo, v1 & vm_hi);
-        mma_bf16_16816(o[2 * d2 + 1], pa[i][0], pa[i][1], pa[i][2], pa[i][3], v2 & vm_lo, v3 & vm_hi);
+          for (int k = 0; k < 4; ++k) {
+            const float* f = reinterpret_cast<const float*>(ov) + 8 * k;
+            dst[4 * q4 + k] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
+                                         pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
+          }
+        }
       }
-    };
-#pragma unroll
-    for (int i = 0; i < kKB; ++i) {
-      if (!(mask & (1 << i))) continue;
-      const int valid = ctx - kBlockSize * (kKB * j + i);
-      if (valid >= kBlockSize) {
-        pv(i, 0xffffffffu, 0xffffffffu);
-      } else {
-        // keys past the context may hold anything (even NaN): zero their V rows in the operand
-        pv(i, (2 * cq < valid ? 0x0000ffffu : 0u) | (2 * cq + 1 < valid ? 0xffff0000u : 0u),
-           (2 * cq + 8 < valid ? 0x0000ffffu : 0u) | (2 * cq + 9 < valid ? 0xffff0000u : 0u));
-      }
+    } else if (lane == 0) {
+      raise_flag(a.status, PA_FLAG_TIMEOUT);
     }
-    // Release the stage.  The warp whose release is the G-th of this round refills it at once,
-    // so no warp waits for the others here.
-    __syncwarp();
-    if (lane == 0) {
-      __threadfence_block();  // this warp's reads of the stage before the refill's writes
-      const unsigned before = atomicAdd(&released[st], 1u);
-      if ((before + 1u) % static_cast<unsigned>(G) == 0u && j + kPfStages < nst) {
-        __threadfence_block();
-        issue(j + kPfStages);
-      }
-    }
-    __syncwarp();
   }
-  if (failed && lane == 0) {
-    raise_flag(a.status, PA_FLAG_TIMEOUT);
-    // Only stages seen .. seen + kPfStages - 1 can have copies in flight (a stage is refilled
-    // after every warp released its previous round, and this warp released none from `seen`
-    // on): let them land (bounded; a stage never refilled gives up after 10 ms) before the
-    // CTA can exit.
-    for (int j = seen; j < min(nst, seen + kPfStages); ++j)
-      mbar_wait_bounded(full + 8 * (j % kPfStages), (j / kPfStages) & 1, 10000000ull);
-  }
-  if (failed) return;
-
-  // ---- out = O / l for the tile's real rows -----------------------------------------------
-  float L0 = l0, L1 = l1;
-#pragma unroll
-  for (int x = 1; x < 4; x <<= 1) {
-    L0 += __shfl_xor_sync(kFullMask, L0, x);
-    L1 += __shfl_xor_sync(kFullMask, L1, x);
-  }
-  const float i0f = 1.f / L0, i1f = 1.f / L1;
-  uint32_t* out0 = reinterpret_cast<uint32_t*>(
-      a.out + (static_cast<size_t>(q0 + i0 + gq) * a.num_q_heads + h) * kHeadDim);
-  uint32_t* out1 = reinterpret_cast<uint32_t*>(
-      a.out + (static_cast<size_t>(q0 + i0 + gq + 8) * a.num_q_heads + h) * kHeadDim);
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    if (gq < rows) out0[4 * nt + cq] = pack_bf16x2(o[nt][0] * i0f, o[nt][1] * i0f);
-    if (gq + 8 < rows) out1[4 * nt + cq] = pack_bf16x2(o[nt][2] * i1f, o[nt][3] * i1f);
+  // every TMEM access and MMA of the CTA is complete: free the columns
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kPfTmemCols);
   }
 }
 
@@ -344,10 +403,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   const int G = a.num_q_heads / a.num_kv_heads;
-  if (G < 1 || G > kPfMaxWarps) return cudaErrorInvalidValue;
+  if (G < 1 || G > kPfRows) return cudaErrorInvalidValue;
+  const int Tq = kPfRows / G;
   const long long rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * kBlockSize;
-  CUtensorMap tm_k, tm_v;
-  if (!cache_tensor_map(a.k_cache, rows, false, &tm_k) || !cache_tensor_map(a.v_cache, rows, false, &tm_v))
+  CUtensorMap tm_kh, tm_v;
+  if (!cache_tensor_map(a.k_cache, rows, false, &tm_kh, 1) || !cache_tensor_map(a.v_cache, rows, false, &tm_v, 2))
     return cudaErrorInvalidValue;
   {  // opt in to the shared-memory size once per device
     static std::mutex mu;
@@ -367,14 +427,14 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((a.max_query_len + kQTile - 1) / kQTile),
+  cfg.gridDim = dim3(static_cast<unsigned>((a.max_query_len + Tq - 1) / Tq),
                      static_cast<unsigned>(a.num_seqs * a.num_kv_heads));
-  cfg.blockDim = dim3(static_cast<unsigned>(G * 32));
+  cfg.blockDim = dim3(static_cast<unsigned>(kPfThreads));
   cfg.dynamicSmemBytes = kPfSmem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel, tm_k, tm_v, a);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel, tm_kh, tm_v, a);
 }
 
 }  // namespace pa
