@@ -11,30 +11,30 @@
 //
 // CTA = (sequence, KV head g, tile of Tq = floor(128 / G) query tokens).  Its 128 matrix rows
 // are the (query, head) pairs of the GQA group, row r = i G + h for query i and head g G + h,
-// so every K/V tile brought in serves all G heads and the tensor core sees M = 128 rows.  The
-// Q tile (128 x 128 bf16) stays in shared memory; keys come 32 at a time (two blocks) through a
-// 3-stage ring filled by TMA.  Per stage j:
-//   S_j (128 x 32, fp32, TMEM)  = Q K_j^T      8 tcgen05.mma, M = 128, N = 32, K = 16 each
-//   softmax (one thread per row) reads S_j with tcgen05.ld, masks causally, keeps a lazy
-//   row shift in the log2 domain (it moves only when the row maximum passes it by more than 8,
-//   so P <= 2^8 and O is rarely rescaled), writes P_j = bf16(2^(scale_log2 s - shift)) to
-//   shared memory and adds the same rounded values to the row sum
-//   O (128 x 128, fp32, TMEM)  += P_j V_j      2 tcgen05.mma (one per key block), M = N = 128,
-//                                              K = 16, V read with its dims contiguous
-// Warps 0-3 run the softmax (warp w owns TMEM lanes 32w..32w+31), warp 4 issues the TMA loads,
-// one thread of warp 5 issues the MMAs.  The MMA thread issues S_{j+1} before it waits for
-// P_j, so the tensor core computes the next scores while the softmax works; two S buffers in
-// TMEM and two P buffers in shared memory (the two 64-byte halves of each 128-byte P row) keep
-// the stages apart.  TMEM per CTA: S 2 x 32 columns + O 128 columns (256 allocated); shared
-// memory ~97 KB, so two CTAs share an SM and the tensor core alternates between them.
+// so every K/V tile brought in serves all G heads and the tensor core sees M = 128 rows.  Keys
+// come 32 at a time (two blocks) through a 6-stage ring of shared memory filled by TMA.  Per
+// stage j:
+//   S_j (128 x 32, fp32)  = Q K_j^T      8 tcgen05.mma, M = 128, N = 32, K = 16 each
+//   softmax (one thread per row) reads S_j with tcgen05.ld, masks causally, keeps a lazy row
+//   shift in the log2 domain (it moves only when the row maximum passes it by more than 8, so
+//   P <= 2^8 and O is rarely rescaled), writes P_j = bf16(2^(scale_log2 s - shift)) back over
+//   the first 16 columns of S_j with tcgen05.st and adds the same rounded values to the row sum
+//   O (128 x 128, fp32) += P_j V_j       2 tcgen05.mma (one per key block), M = N = 128, K = 16
+// Tensor memory (256 columns): Q as bf16 pairs in columns 0-63, two S buffers in 64-95 and
+// 96-127, O in 128-255.  Q and P are the A operands read from tensor memory, so shared memory
+// feeds only K (the K-major B operand of S) and V (the B operand of P V, dims contiguous):
+// with N = 32 an A operand read from shared memory at every MMA would need more bandwidth than
+// shared memory has.
+// Warps 0-3 load Q and run the softmax (warp w owns TMEM lanes 32w..32w+31), warp 4 issues the
+// TMA loads (its lanes read 32 block ids at a time, a window ahead), one thread of warp 5
+// issues the MMAs.  The MMA thread issues S_{j+1} before it waits for P_j, so the tensor core
+// computes the next scores while the softmax works; S_{j+2} reuses the buffer of P_j only
+// after P_j V_j (the MMAs of one thread run in issue order).  Shared memory is ~97 KB, so two
+// CTAs share an SM and the tensor core alternates between them.
 //
-// Shared-memory operands use the 128-byte swizzle (16-byte chunk c of a 128-byte row r at
-// c ^ (r % 8), 8-row atoms of 1024 bytes):
-//   Q     two 64-column halves of 128 rows, 16 KiB each (K-major A operand)
-//   stage K half 0 of both blocks (rows 0-31, 4 KiB), K half 1 (4 KiB), then V of block 0 and
-//         of block 1 (4 KiB each, as two 2 KiB halves of 16 rows): K is the K-major B operand
-//         of S (N = 32 keys), V the MN-major B operand of P V (N = 128 dims)
-//   P     128 rows of 128 bytes; stage j uses bytes 64 (j % 2) .. +63 of each row (32 keys)
+// K and V tiles use the 128-byte swizzle (16-byte chunk c of a 128-byte row r at c ^ (r % 8),
+// 8-row atoms of 1024 bytes).  A stage holds K half 0 of both blocks (rows 0-31, 4 KiB), K half
+// 1 (4 KiB), then V of block 0 and of block 1 (4 KiB each, as two 2 KiB halves of 16 rows).
 // Keys past the context in the context's last block may hold anything: their scores are
 // masked and their V rows zeroed in shared memory before P V.  A block id out of range is not
 // loaded: its keys are masked and its P V step skipped.  Every wait is bounded; a timeout
@@ -56,30 +56,30 @@ namespace {
 constexpr int kPfRows = 128;                        // MMA rows: (query, head) pairs per CTA
 constexpr int kPfKB = 2;                            // key blocks per stage
 constexpr int kPfKeys = kPfKB * kBlockSize;         // 32 keys per stage
-constexpr int kPfStages = 3;
+constexpr int kPfStages = 6;
 constexpr int kPfHalf = kBlockSize * 128;           // 16 rows x 64 bf16: 2 KiB
 constexpr int kPfKHalfBytes = kPfKB * kPfHalf;      // one K half of the stage's blocks: 4 KiB
 constexpr int kPfVOff = 2 * kPfKHalfBytes;          // V tiles after the two K halves
 constexpr int kPfStageBytes = kPfVOff + kPfKB * kTileBytes;   // 16 KiB
-constexpr int kPfQHalfBytes = kPfRows * 128;        // 16 KiB
-constexpr int kPfQBytes = 2 * kPfQHalfBytes;        // 32 KiB
-constexpr int kPfPBytes = kPfRows * 128;            // 16 KiB
 constexpr int kPfHeader = 256;                      // mbarriers, present masks, TMEM address
-constexpr int kPfSmem = kPfHeader + 1024 + kPfQBytes + kPfStages * kPfStageBytes + kPfPBytes;
+constexpr int kPfSmem = kPfHeader + 1024 + kPfStages * kPfStageBytes;
 constexpr int kPfThreads = 192;                     // 4 softmax warps, TMA warp, MMA warp
 constexpr uint32_t kPfTmemCols = 256;
-constexpr uint32_t kPfSCol = 0;                     // S buffers: columns 0-31 and 32-63
-constexpr uint32_t kPfOCol = 64;                    // O: columns 64-191
+constexpr uint32_t kPfQCol = 0;                     // Q: 64 columns of bf16 pairs
+constexpr uint32_t kPfSCol = 64;                    // S buffers: columns 64-95 and 96-127
+constexpr uint32_t kPfOCol = 128;                   // O: columns 128-255
 
 // header layout (byte offsets)
-constexpr int kBarKvFull = 0;                       // [3] TMA -> MMA, softmax
-constexpr int kBarKvEmpty = 24;                     // [3] MMA (P V done) -> TMA
-constexpr int kBarSFull = 48;                       // [2] MMA (S done) -> softmax
-constexpr int kBarPFull = 64;                       // [2] softmax (P written) -> MMA, 128 arrivals
-constexpr int kBarOReady = 80;                      // MMA (P V done) -> softmax
-constexpr int kBarDone = 88;                        // MMA thread: its last MMAs finished
-constexpr int kPresent = 96;                        // [3] int: bit i = block i of the stage loaded
-constexpr int kTmemSlot = 112;
+constexpr int kBarKvFull = 0;                       // [6] TMA -> MMA, softmax
+constexpr int kBarKvEmpty = 48;                     // [6] MMA (P V done) -> TMA
+constexpr int kBarSFull = 96;                       // [2] MMA (S done) -> softmax
+constexpr int kBarPFull = 112;                      // [2] softmax (P written) -> MMA, 128 arrivals
+constexpr int kBarOReady = 128;                     // MMA (P V done) -> softmax
+constexpr int kBarDone = 136;                       // MMA thread: its last MMAs finished
+constexpr int kBarQReady = 144;                     // softmax (Q in TMEM) -> MMA, 128 arrivals
+constexpr int kPresent = 152;                       // [6] int: bit i = block i of the stage loaded
+constexpr int kTmemSlot = 176;
+static_assert(kTmemSlot + 4 <= kPfHeader, "header");
 
 __global__ void __launch_bounds__(kPfThreads, 2)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant__ CUtensorMap tm_v,
@@ -119,9 +119,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
   const int nst = (nblocks + kPfKB - 1) / kPfKB;    // stages of kPfKB key blocks
 
   const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t qbuf = (raw + kPfHeader + 1023u) & ~1023u;
-  const uint32_t stages = qbuf + kPfQBytes;
-  const uint32_t pbuf = stages + kPfStages * kPfStageBytes;
+  const uint32_t stages = (raw + kPfHeader + 1023u) & ~1023u;
   volatile int* present = reinterpret_cast<volatile int*>(smem_raw + kPresent);
 
   if (threadIdx.x == 0) {
@@ -135,25 +133,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
     }
     mbar_init(raw + kBarOReady, 1);
     mbar_init(raw + kBarDone, 1);
+    mbar_init(raw + kBarQReady, 128);
     fence_mbar_init();
-    prefetch_tensor_map(&tm_kh);
-    prefetch_tensor_map(&tm_v);
   }
-  // Q tile into shared memory by every thread: row r = i G + h (zero past the tile's queries),
-  // 16 chunks of 16 bytes, chunk c in half c / 8 at position (c % 8) ^ (r % 8).
-  {
-    unsigned char* qgen = smem_raw + (qbuf - raw);
-    for (int idx = threadIdx.x; idx < kPfRows * 16; idx += kPfThreads) {
-      const int r = idx >> 4, c = idx & 15;
-      const int i = r / G, h = r - (r / G) * G;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (i < rows_q)
-        v = reinterpret_cast<const uint4*>(
-            a.q + (static_cast<size_t>(q0 + i0 + i) * a.num_q_heads + g * G + h) * kHeadDim)[c];
-      *reinterpret_cast<uint4*>(qgen + (c >> 3) * kPfQHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
-    }
-  }
-  fence_proxy_async_smem();                         // the tensor core reads Q through the async proxy
   if (warp == 0) {
     tmem_alloc(raw + kTmemSlot, kPfTmemCols);
     tmem_relinquish();
@@ -165,23 +147,40 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
 
   if (warp == 4) {
     // ---- TMA producer: stage j holds key blocks 2j, 2j + 1 -------------------------------
+    // Lane k holds the id of block 32 w + k of the current window w (-1 past the tile's
+    // blocks); the next window's ids are loaded when the current one starts.
     if (lane == 0) {
-      const int32_t* bt_row = a.block_tables + static_cast<size_t>(s) * a.max_blocks;
-      int issued = 0;
-      bool failed = false;
-      for (int j = 0; j < nst; ++j) {
-        const int st = j % kPfStages;
-        if (j >= kPfStages &&
-            !mbar_wait_bounded(raw + kBarKvEmpty + 8 * st, ((j / kPfStages) - 1) & 1)) {
-          failed = true;
-          break;
-        }
-        int blk[kPfKB];
+      prefetch_tensor_map(&tm_kh);
+      prefetch_tensor_map(&tm_v);
+    }
+    const int32_t* bt_row = a.block_tables + static_cast<size_t>(s) * a.max_blocks;
+    auto load_ids = [&](int w) { const int b = 32 * w + lane; return b < nblocks ? bt_row[b] : -1; };
+    int ids = load_ids(0);
+    int ids_next = load_ids(1);
+    int issued = 0;
+    bool failed = false;
+    for (int j = 0; j < nst; ++j) {
+      const int st = j % kPfStages;
+      const int k = (kPfKB * j) & 31;               // lane holding block 2j
+      if (j > 0 && k == 0) {
+        ids = ids_next;
+        ids_next = load_ids((kPfKB * j) / 32 + 1);
+      }
+      bool ok = true;
+      if (lane == 0 && j >= kPfStages)
+        ok = mbar_wait_bounded(raw + kBarKvEmpty + 8 * st, ((j / kPfStages) - 1) & 1);
+      if (!__shfl_sync(kFullMask, ok, 0)) {
+        failed = true;
+        break;
+      }
+      int blk[kPfKB];
+#pragma unroll
+      for (int i = 0; i < kPfKB; ++i) blk[i] = __shfl_sync(kFullMask, ids, k + i);
+      if (lane == 0) {
         int mask = 0;
 #pragma unroll
         for (int i = 0; i < kPfKB; ++i) {
           const int b = kPfKB * j + i;
-          blk[i] = b < nblocks ? bt_row[b] : -1;
           if (b < nblocks && blk[i] >= 0 && blk[i] < a.num_blocks) mask |= 1 << i;
           else if (b < nblocks) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
         }
@@ -201,8 +200,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
         } else {
           mbar_arrive(bar);
         }
-        issued = j + 1;
       }
+      issued = j + 1;
+    }
+    if (lane == 0) {
       if (failed) raise_flag(a.status, PA_FLAG_TIMEOUT);
       // Copies still in flight can only be those of the last kPfStages fills: let them land
       // (immediate in a normal run, where the MMAs consumed every stage) before the CTA exits.
@@ -214,7 +215,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
     if (lane == 0) {
       const uint32_t id_s = umma_idesc_bf16(kPfRows, kPfKeys, false, false);
       const uint32_t id_pv = umma_idesc_bf16(kPfRows, kHeadDim, false, true);
-      bool failed = false;
       bool o_started = false;
       auto issue_s = [&](int j) -> bool {
         const int st = j % kPfStages;
@@ -223,14 +223,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
         const uint32_t kst = stages + st * kPfStageBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = umma_smem_desc(qbuf + (kk >> 2) * kPfQHalfBytes + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = umma_smem_desc(kst + (kk >> 2) * kPfKHalfBytes + (kk & 3) * 32, 16, 1024);
-          umma_bf16(tmem + kPfSCol + kPfKeys * (j & 1), ad, bd, id_s, kk > 0);
+          umma_bf16_tmem_a(tmem + kPfSCol + kPfKeys * (j & 1), tmem + kPfQCol + 8 * kk, bd, id_s, kk > 0);
         }
         umma_commit(raw + kBarSFull + 8 * (j & 1));
         return true;
       };
-      failed = !issue_s(0);
+      bool failed = !mbar_wait_bounded(raw + kBarQReady, 0);
+      if (!failed) {
+        tc_fence_after();
+        failed = !issue_s(0);
+      }
       for (int j = 0; j < nst && !failed; ++j) {
         if (j + 1 < nst && !issue_s(j + 1)) {
           failed = true;
@@ -247,9 +250,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
 #pragma unroll
         for (int i = 0; i < kPfKB; ++i) {
           if (!(mask & (1 << i))) continue;
-          const uint64_t ad = umma_smem_desc(pbuf + 64 * (j & 1) + 32 * i, 16, 1024);
           const uint64_t bd = umma_smem_desc(vst + i * kTileBytes, kPfHalf, 1024);
-          umma_bf16(tmem + kPfOCol, ad, bd, id_pv, o_started);
+          umma_bf16_tmem_a(tmem + kPfOCol, tmem + kPfSCol + kPfKeys * (j & 1) + 8 * i, bd, id_pv, o_started);
           o_started = true;
         }
         umma_commit(raw + kBarKvEmpty + 8 * st);
@@ -261,11 +263,32 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       mbar_wait_bounded(raw + kBarDone, 0);
     }
   } else {
-    // ---- softmax: thread = row r of the tile -------------------------------------------------
+    // ---- Q into TMEM, then the softmax: thread = row r of the tile ------------------------------
     const int r = threadIdx.x;                      // 0..127 = TMEM lane
     const int i = r / G, h = r - (r / G) * G;
     const int p_r = pos0 + i;                       // rows past the tile's queries are never stored
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    {
+      // row r = query i, head g G + h: 128 bf16 = 64 columns of pairs (zero past the queries)
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + (static_cast<size_t>(q0 + i0 + (i < rows_q ? i : 0)) * a.num_q_heads + g * G + h) * kHeadDim);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t qv[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = i < rows_q ? src[8 * half + c] : make_uint4(0u, 0u, 0u, 0u);
+          qv[4 * c] = v.x;
+          qv[4 * c + 1] = v.y;
+          qv[4 * c + 2] = v.z;
+          qv[4 * c + 3] = v.w;
+        }
+        tmem_st32(trow + kPfQCol + 32 * half, qv);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(raw + kBarQReady);
+    }
     const float sl = a.scale_log2;
     // the context's last block, if partial: its V rows valid_last..15 are zeroed before P V
     const int last_blk = (ctx - 1) / kBlockSize;
@@ -274,6 +297,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
     bool failed = false;
     for (int j = 0; j < nst; ++j) {
       const int st = j % kPfStages;
+      const uint32_t sbuf = trow + kPfSCol + kPfKeys * (j & 1);
       // tcgen05.ld / st are warp-collective: a warp goes on only if all its lanes saw the phase
       const bool ok = mbar_wait_bounded(raw + kBarSFull + 8 * (j & 1), (j >> 1) & 1) &&
                       mbar_wait_bounded(raw + kBarKvFull + 8 * st, (j / kPfStages) & 1);
@@ -284,7 +308,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       tc_fence_after();
       const int mask = present[st];
       uint32_t sv[32];
-      tmem_ld32(trow + kPfSCol + kPfKeys * (j & 1), sv);
+      tmem_ld32(sbuf, sv);
       tmem_wait_ld();
       float sc[32];
 #pragma unroll
@@ -298,12 +322,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
         for (int c = 0; c < 32; ++c)
           if (!((mask >> (c / kBlockSize)) & 1) || c > lim) sc[c] = -INFINITY;
       }
-      float mx = sc[0];
+      float mt[16];
 #pragma unroll
-      for (int c = 1; c < 32; ++c) mx = fmaxf(mx, sc[c]);
+      for (int c = 0; c < 16; ++c) mt[c] = fmaxf(sc[c], sc[c + 16]);
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) mt[c] = fmaxf(mt[c], mt[c + w]);
       // Shift m in the log2 domain (scale * log2(e) applied): it moves to the row maximum only
       // when that exceeds it by more than 8, so P stays at most 2^8 and O is rescaled rarely.
-      const float bs = mx * sl;
+      const float bs = mt[0] * sl;
       const float mn = bs > m + 8.f ? bs : m;
       const float sh = mn == -INFINITY ? 0.f : mn;  // a row with no key yet keeps the shift 0
       const float alpha = (mn == m || m == -INFINITY) ? 1.f : ex2_ftz(m - sh);
@@ -311,13 +339,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       // P = 2^(scale_log2 s - shift), rounded to bf16 (the MMA operand); the row sum adds the
       // same rounded values
       uint32_t pw[16];
-      float ps = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         pw[k] = pack_bf16x2(ex2_ftz(fmaf(sc[2 * k], sl, -sh)), ex2_ftz(fmaf(sc[2 * k + 1], sl, -sh)));
-        ps += bf16lo(pw[k]) + bf16hi(pw[k]);
+        ps[k & 3] += bf16lo(pw[k]) + bf16hi(pw[k]);
       }
-      l = fmaf(l, alpha, ps);
+      l = fmaf(l, alpha, (ps[0] + ps[1]) + (ps[2] + ps[3]));
+      tmem_st16(sbuf, pw);                          // P_j over the first 16 columns of S_j
       // O *= alpha once P V of the previous stage has landed (warp-collective TMEM access)
       if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
         // P V of stage j - 1 was issued after S_j, so o_ready has completed j - 1 or j times
@@ -336,7 +365,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
           for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
           tmem_st32(trow + kPfOCol + 32 * q4, ov);
         }
-        tmem_wait_st();
       }
       // Keys past the context in its last block: zero their V rows (both 64-column halves).
       const int vb = last_blk - kPfKB * j;
@@ -347,28 +375,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
           const int row = valid_last + (x >> 4), half = (x >> 3) & 1, ch = x & 7;
           *reinterpret_cast<uint4*>(vt + half * kPfHalf + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_proxy_async_smem();                   // before the tensor core reads the tile
       }
-      // P row r: keys 0-31 of the stage = 4 chunks, chunk 4 (j % 2) + k at position ^ (r % 8)
-      {
-        unsigned char* prow = smem_raw + (pbuf - raw) + r * 128;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int c = 4 * (j & 1) + k;
-          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
-              make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
-        }
-      }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(raw + kBarPFull + 8 * (j & 1));
     }
     if (failed) {
       if (lane == 0) raise_flag(a.status, PA_FLAG_TIMEOUT);
     } else if (__all_sync(kFullMask, mbar_wait_bounded(raw + kBarDone, 0))) {
-      // (the MMA thread commits kBarDone once, after its last P V)
-      // ---- out = O / l for the tile's real rows ------------------------------------------------
+      // ---- out = O / l for the tile's real rows (kBarDone: the MMA thread's last P V) --------
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      // a row whose every key was skipped (all its blocks out of range) has l = 0 and an O
+      // never written: it stores zeros
+      const bool any = l > 0.f;
+      const float inv = any ? 1.f / l : 0.f;
       const bool store = i < rows_q;
       uint4* dst = reinterpret_cast<uint4*>(
           a.out + (static_cast<size_t>(q0 + i0 + (store ? i : 0)) * a.num_q_heads + g * G + h) * kHeadDim);
@@ -380,7 +401,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
         if (store) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float* f = reinterpret_cast<const float*>(ov) + 8 * k;
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = any ? __uint_as_float(ov[8 * k + e]) : 0.f;
             dst[4 * q4 + k] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
                                          pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
           }
