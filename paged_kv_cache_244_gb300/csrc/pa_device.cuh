@@ -43,6 +43,12 @@ __device__ __forceinline__ void pdl_allow_next_grid() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Barrier kId (1..15; 0 is __syncthreads) among `count` threads (a multiple of 32).
+template <int kId>
+__device__ __forceinline__ void named_bar_sync(int count) {
+  asm volatile("bar.sync %0, %1;" ::"n"(kId), "r"(count) : "memory");
+}
+
 // ---- mbarrier ------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -215,6 +221,15 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
       ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u)
       : "memory");
+}
+// True in exactly one lane of the (converged) warp.  Work issued under it keeps the warp's
+// values uniform, so descriptors stay in uniform registers.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 // Arrive once on the mbarrier when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {

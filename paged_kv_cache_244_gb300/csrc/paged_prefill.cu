@@ -12,35 +12,36 @@
 // CTA = (sequence, KV head g, tile of Tq = floor(128 / G) query tokens).  Its 128 matrix rows
 // are the (query, head) pairs of the GQA group, row r = i G + h for query i and head g G + h,
 // so every K/V tile brought in serves all G heads and the tensor core sees M = 128 rows.  Keys
-// come 32 at a time (two blocks) through a 6-stage ring of shared memory filled by TMA.  Per
+// come 64 at a time (four blocks) through a 3-stage ring of shared memory filled by TMA.  Per
 // stage j:
-//   S_j (128 x 32, fp32)  = Q K_j^T      8 tcgen05.mma, M = 128, N = 32, K = 16 each
-//   softmax (one thread per row) reads S_j with tcgen05.ld, masks causally, keeps a lazy row
-//   shift in the log2 domain (it moves only when the row maximum passes it by more than 8, so
-//   P <= 2^8 and O is rarely rescaled), writes P_j = bf16(2^(scale_log2 s - shift)) back over
-//   the first 16 columns of S_j with tcgen05.st and adds the same rounded values to the row sum
-//   O (128 x 128, fp32) += P_j V_j       2 tcgen05.mma (one per key block), M = N = 128, K = 16
-// Tensor memory (256 columns): Q as bf16 pairs in columns 0-63, two S buffers in 64-95 and
-// 96-127, O in 128-255.  Q and P are the A operands read from tensor memory, so shared memory
-// feeds only K (the K-major B operand of S) and V (the B operand of P V, dims contiguous):
-// with N = 32 an A operand read from shared memory at every MMA would need more bandwidth than
-// shared memory has.
-// Warps 0-3 load Q and run the softmax (warp w owns TMEM lanes 32w..32w+31), warp 4 issues the
-// TMA loads (its lanes read 32 block ids at a time, a window ahead), one thread of warp 5
-// issues the MMAs.  The MMA thread issues S_{j+1} before it waits for P_j, so the tensor core
-// computes the next scores while the softmax works; S_{j+2} reuses the buffer of P_j only
-// after P_j V_j (the MMAs of one thread run in issue order).  Shared memory is ~97 KB, so two
-// CTAs share an SM and the tensor core alternates between them.
+//   S_j (128 x 64, fp32, TMEM) = Q K_j^T   8 tcgen05.mma, M = 128, N = 64, K = 16 each
+//   softmax (one thread per row): S_j read with tcgen05.ld, causal mask, a lazy row shift in
+//   the log2 domain (it moves only when the row maximum passes it by more than 8, so P <= 2^8
+//   and O is rarely rescaled), P_j = bf16(2^(scale_log2 s - shift)) written to shared memory
+//   over K_j (dead once S_j is done; 128 rows x 64 keys is exactly its size), the same rounded
+//   values added to the row sum
+//   O (128 x 128, fp32, TMEM) += P_j V_j   4 tcgen05.mma (one per key block), M = N = 128, K = 16
+// Tensor memory (256 columns): Q as bf16 pairs in columns 0-63 (the A operand of S, read from
+// tensor memory: with N = 64 an A read from shared memory at every MMA would crowd shared
+// memory), S in 64-127, O in 128-255.  An MMA takes a fixed minimum time whatever its N up to
+// 64, so S runs 64 keys wide.
 //
-// K and V tiles use the 128-byte swizzle (16-byte chunk c of a 128-byte row r at c ^ (r % 8),
-// 8-row atoms of 1024 bytes).  A stage holds K half 0 of both blocks (rows 0-31, 4 KiB), K half
-// 1 (4 KiB), then V of block 0 and of block 1 (4 KiB each, as two 2 KiB halves of 16 rows).
-// Keys past the context in the context's last block may hold anything: their scores are
-// masked and their V rows zeroed in shared memory before P V.  A block id out of range is not
-// loaded: its keys are masked and its P V step skipped.  Every wait is bounded; a timeout
-// raises PA_FLAG_TIMEOUT and the CTA drains its copies and MMAs before it exits.
-// Tiles are scheduled latest first over the whole grid: the last tiles of a sequence see the
-// most keys.
+// Warps 0-3 load Q and run the softmax (warp w owns TMEM lanes 32w..32w+31); warp 4 issues the
+// TMA loads (its lanes read 32 block ids at a time, a window ahead); warp 5 runs the MMA loop,
+// one elected lane issuing.  The softmax frees the S columns as soon as it has loaded S_j, and
+// the MMA warp then issues S_{j+1} at once, so the tensor core computes the next scores (and
+// P_{j-1} V_{j-1}) while the softmax works on stage j.  Shared memory is ~97 KB, so two CTAs
+// share an SM.
+//
+// K, V and P use the 128-byte swizzle (16-byte chunk c of a 128-byte row r at c ^ (r % 8),
+// 8-row atoms of 1024 bytes).  A stage holds K half 0 of the four blocks (rows 0-63, 8 KiB), K
+// half 1 (8 KiB) -- later P, 128 rows of 64 keys -- then V of blocks 0-3 (4 KiB each, as two
+// 2 KiB halves of 16 rows).  Keys past the context in the context's last block may hold
+// anything: their scores are masked and their V rows zeroed in shared memory before P V.  A
+// block id out of range is not loaded: its keys are masked and its P V step skipped.  Every
+// wait is bounded; a timeout raises PA_FLAG_TIMEOUT and the CTA drains its copies and MMAs
+// before it exits.  Tiles are scheduled latest first over the whole grid: the last tiles of a
+// sequence see the most keys.
 
 #include <mutex>
 
@@ -54,31 +55,32 @@ namespace pa {
 namespace {
 
 constexpr int kPfRows = 128;                        // MMA rows: (query, head) pairs per CTA
-constexpr int kPfKB = 2;                            // key blocks per stage
-constexpr int kPfKeys = kPfKB * kBlockSize;         // 32 keys per stage
-constexpr int kPfStages = 6;
+constexpr int kPfKB = 4;                            // key blocks per stage
+constexpr int kPfKeys = kPfKB * kBlockSize;         // 64 keys per stage
+constexpr int kPfStages = 3;
 constexpr int kPfHalf = kBlockSize * 128;           // 16 rows x 64 bf16: 2 KiB
-constexpr int kPfKHalfBytes = kPfKB * kPfHalf;      // one K half of the stage's blocks: 4 KiB
+constexpr int kPfKHalfBytes = kPfKB * kPfHalf;      // one K half of the stage's blocks: 8 KiB
 constexpr int kPfVOff = 2 * kPfKHalfBytes;          // V tiles after the two K halves
-constexpr int kPfStageBytes = kPfVOff + kPfKB * kTileBytes;   // 16 KiB
+constexpr int kPfStageBytes = kPfVOff + kPfKB * kTileBytes;   // 32 KiB
+static_assert(kPfRows * kPfKeys * 2 == kPfVOff, "P of a stage fills its K region");
 constexpr int kPfHeader = 256;                      // mbarriers, present masks, TMEM address
 constexpr int kPfSmem = kPfHeader + 1024 + kPfStages * kPfStageBytes;
 constexpr int kPfThreads = 192;                     // 4 softmax warps, TMA warp, MMA warp
 constexpr uint32_t kPfTmemCols = 256;
 constexpr uint32_t kPfQCol = 0;                     // Q: 64 columns of bf16 pairs
-constexpr uint32_t kPfSCol = 64;                    // S buffers: columns 64-95 and 96-127
+constexpr uint32_t kPfSCol = 64;                    // S: columns 64-127
 constexpr uint32_t kPfOCol = 128;                   // O: columns 128-255
 
 // header layout (byte offsets)
-constexpr int kBarKvFull = 0;                       // [6] TMA -> MMA, softmax
-constexpr int kBarKvEmpty = 48;                     // [6] MMA (P V done) -> TMA
-constexpr int kBarSFull = 96;                       // [2] MMA (S done) -> softmax
-constexpr int kBarPFull = 112;                      // [2] softmax (P written) -> MMA, 128 arrivals
-constexpr int kBarOReady = 128;                     // MMA (P V done) -> softmax
-constexpr int kBarDone = 136;                       // MMA thread: its last MMAs finished
-constexpr int kBarQReady = 144;                     // softmax (Q in TMEM) -> MMA, 128 arrivals
-constexpr int kPresent = 152;                       // [6] int: bit i = block i of the stage loaded
-constexpr int kTmemSlot = 176;
+constexpr int kBarKvFull = 0;                       // [3] TMA -> MMA, softmax
+constexpr int kBarKvEmpty = 24;                     // [3] MMA (P V done) -> TMA, softmax (O rescale)
+constexpr int kBarSFull = 48;                       // MMA (S done) -> softmax
+constexpr int kBarSFree = 56;                       // softmax (S loaded) -> MMA, 128 arrivals
+constexpr int kBarPFull = 64;                       // [2] softmax (P written) -> MMA, 128 arrivals
+constexpr int kBarDone = 80;                        // MMA thread: its last MMAs finished
+constexpr int kBarQReady = 88;                      // softmax (Q in TMEM) -> MMA, 128 arrivals
+constexpr int kPresent = 96;                        // [3] int: bit i = block i of the stage loaded
+constexpr int kTmemSlot = 112;
 static_assert(kTmemSlot + 4 <= kPfHeader, "header");
 
 __global__ void __launch_bounds__(kPfThreads, 2)
@@ -127,11 +129,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       mbar_init(raw + kBarKvFull + 8 * i, 1);
       mbar_init(raw + kBarKvEmpty + 8 * i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(raw + kBarSFull + 8 * i, 1);
-      mbar_init(raw + kBarPFull + 8 * i, 128);
-    }
-    mbar_init(raw + kBarOReady, 1);
+    mbar_init(raw + kBarSFull, 1);
+    mbar_init(raw + kBarSFree, 128);
+    mbar_init(raw + kBarPFull, 128);
+    mbar_init(raw + kBarPFull + 8, 128);
     mbar_init(raw + kBarDone, 1);
     mbar_init(raw + kBarQReady, 128);
     fence_mbar_init();
@@ -146,7 +147,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem_raw + kTmemSlot);
 
   if (warp == 4) {
-    // ---- TMA producer: stage j holds key blocks 2j, 2j + 1 -------------------------------
+    // ---- TMA producer: stage j holds key blocks 4j .. 4j + 3 --------------------------------
     // Lane k holds the id of block 32 w + k of the current window w (-1 past the tile's
     // blocks); the next window's ids are loaded when the current one starts.
     if (lane == 0) {
@@ -161,7 +162,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
     bool failed = false;
     for (int j = 0; j < nst; ++j) {
       const int st = j % kPfStages;
-      const int k = (kPfKB * j) & 31;               // lane holding block 2j
+      const int k = (kPfKB * j) & 31;               // lane holding block 4j
       if (j > 0 && k == 0) {
         ids = ids_next;
         ids_next = load_ids((kPfKB * j) / 32 + 1);
@@ -211,57 +212,79 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
         mbar_wait_bounded(raw + kBarKvFull + 8 * (j % kPfStages), (j / kPfStages) & 1, 10000000ull);
     }
   } else if (warp == 5) {
-    // ---- MMA issuer --------------------------------------------------------------------------
-    if (lane == 0) {
-      const uint32_t id_s = umma_idesc_bf16(kPfRows, kPfKeys, false, false);
-      const uint32_t id_pv = umma_idesc_bf16(kPfRows, kHeadDim, false, true);
-      bool o_started = false;
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kPfStages;
-        if (!mbar_wait_bounded(raw + kBarKvFull + 8 * st, (j / kPfStages) & 1)) return false;
-        tc_fence_after();
-        const uint32_t kst = stages + st * kPfStageBytes;
+    // ---- MMA issuer: the whole warp runs the loop, one elected lane issues ----------------------
+    const uint32_t id_s = umma_idesc_bf16(kPfRows, kPfKeys, false, false);
+    const uint32_t id_pv = umma_idesc_bf16(kPfRows, kHeadDim, false, true);
+    // descriptors of stage 0; a stage, a k step or a block moves the start address field by
+    // (byte offset) / 16, which never carries out of its 14 bits (shared memory < 256 KiB)
+    const uint64_t k_desc0 = umma_smem_desc(stages, 16, 1024);
+    const uint64_t p_desc0 = umma_smem_desc(stages, 16, 1024);   // P over K: 128-byte rows
+    const uint64_t v_desc0 = umma_smem_desc(stages + kPfVOff, kPfHalf, 1024);
+    bool o_started = false;
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(kFullMask, mbar_wait_bounded(bar, parity));
+    };
+    // S_j = Q K_j^T into the S columns, once the softmax has loaded S_{j-1}
+    auto issue_s = [&](int j) -> bool {
+      const int st = j % kPfStages;
+      if (!wait_all(raw + kBarKvFull + 8 * st, (j / kPfStages) & 1)) return false;
+      if (j > 0 && !wait_all(raw + kBarSFree, (j - 1) & 1)) return false;
+      tc_fence_after();
+      const uint64_t kd = k_desc0 + static_cast<uint64_t>((st * kPfStageBytes) >> 4);
+      if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = umma_smem_desc(kst + (kk >> 2) * kPfKHalfBytes + (kk & 3) * 32, 16, 1024);
-          umma_bf16_tmem_a(tmem + kPfSCol + kPfKeys * (j & 1), tmem + kPfQCol + 8 * kk, bd, id_s, kk > 0);
-        }
-        umma_commit(raw + kBarSFull + 8 * (j & 1));
-        return true;
-      };
-      bool failed = !mbar_wait_bounded(raw + kBarQReady, 0);
-      if (!failed) {
-        tc_fence_after();
-        failed = !issue_s(0);
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_tmem_a(tmem + kPfSCol, tmem + kPfQCol + 8 * kk,
+                           kd + static_cast<uint64_t>(((kk >> 2) * kPfKHalfBytes + (kk & 3) * 32) >> 4), id_s,
+                           kk > 0);
+        umma_commit(raw + kBarSFull);
       }
-      for (int j = 0; j < nst && !failed; ++j) {
-        if (j + 1 < nst && !issue_s(j + 1)) {
-          failed = true;
-          break;
-        }
-        if (!mbar_wait_bounded(raw + kBarPFull + 8 * (j & 1), (j >> 1) & 1)) {
-          failed = true;
-          break;
-        }
-        tc_fence_after();
-        const int st = j % kPfStages;
-        const int mask = present[st];
-        const uint32_t vst = stages + st * kPfStageBytes + kPfVOff;
+      __syncwarp();
+      return true;
+    };
+    bool failed = !wait_all(raw + kBarQReady, 0);
+    if (!failed) {
+      tc_fence_after();
+      failed = !issue_s(0);
+    }
+    for (int j = 0; j < nst && !failed; ++j) {
+      if (j + 1 < nst && !issue_s(j + 1)) {
+        failed = true;
+        break;
+      }
+      // P_j: two barriers alternate, so the softmax of stage j + 1 (which may run while this
+      // warp still waits here) arrives on the other one
+      if (!wait_all(raw + kBarPFull + 8 * (j & 1), (j >> 1) & 1)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      const int st = j % kPfStages;
+      const int mask = present[st];
+      const uint64_t pd = p_desc0 + static_cast<uint64_t>((st * kPfStageBytes) >> 4);
+      const uint64_t vd = v_desc0 + static_cast<uint64_t>((st * kPfStageBytes) >> 4);
+      if (elect_one()) {
+        bool acc = o_started;                       // the first P V of the tile overwrites O
 #pragma unroll
         for (int i = 0; i < kPfKB; ++i) {
           if (!(mask & (1 << i))) continue;
-          const uint64_t bd = umma_smem_desc(vst + i * kTileBytes, kPfHalf, 1024);
-          umma_bf16_tmem_a(tmem + kPfOCol, tmem + kPfSCol + kPfKeys * (j & 1) + 8 * i, bd, id_pv, o_started);
-          o_started = true;
+          umma_bf16(tmem + kPfOCol, pd + static_cast<uint64_t>((32 * i) >> 4),
+                    vd + static_cast<uint64_t>((i * kTileBytes) >> 4), id_pv, acc);
+          acc = true;
         }
+        // P V of stage j done: the TMA warp may refill the stage, the softmax may rescale O
         umma_commit(raw + kBarKvEmpty + 8 * st);
-        umma_commit(raw + kBarOReady);
       }
+      __syncwarp();
+      o_started = o_started || mask != 0;
+    }
+    if (lane == 0) {
       if (failed) raise_flag(a.status, PA_FLAG_TIMEOUT);
       // Every MMA issued has finished before the CTA frees TMEM and exits.
       umma_commit(raw + kBarDone);
       mbar_wait_bounded(raw + kBarDone, 0);
     }
+    __syncwarp();
   } else {
     // ---- Q into TMEM, then the softmax: thread = row r of the tile ------------------------------
     const int r = threadIdx.x;                      // 0..127 = TMEM lane
@@ -295,11 +318,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
     const int valid_last = ctx - kBlockSize * last_blk;
     float m = -INFINITY, l = 0.f;
     bool failed = false;
+    const uint32_t sbuf = trow + kPfSCol;
     for (int j = 0; j < nst; ++j) {
       const int st = j % kPfStages;
-      const uint32_t sbuf = trow + kPfSCol + kPfKeys * (j & 1);
       // tcgen05.ld / st are warp-collective: a warp goes on only if all its lanes saw the phase
-      const bool ok = mbar_wait_bounded(raw + kBarSFull + 8 * (j & 1), (j >> 1) & 1) &&
+      const bool ok = mbar_wait_bounded(raw + kBarSFull, j & 1) &&
                       mbar_wait_bounded(raw + kBarKvFull + 8 * st, (j / kPfStages) & 1);
       if (!__all_sync(kFullMask, ok)) {
         failed = true;
@@ -307,26 +330,35 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       }
       tc_fence_after();
       const int mask = present[st];
-      uint32_t sv[32];
-      tmem_ld32(sbuf, sv);
-      tmem_wait_ld();
-      float sc[32];
+      float sc[kPfKeys];
+      {
+        uint32_t sv[32];
+        tmem_ld32(sbuf, sv);
+        tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 32; ++c) sc[c] = __uint_as_float(sv[c]);
+        for (int c = 0; c < 32; ++c) sc[c] = __uint_as_float(sv[c]);
+        tmem_ld32(sbuf + 32, sv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sc[32 + c] = __uint_as_float(sv[c]);
+      }
+      // S_j is in registers: the MMA warp may compute S_{j+1} over it
+      tc_fence_before();
+      mbar_arrive(raw + kBarSFree);
       // Scores stay unscaled until the exponent (scale > 0, so the row maxima are the same).
       // Causal mask and missing blocks -> -inf, only on a stage that reaches past the tile's
       // first query or lacks a block; the others lie wholly before every query of the tile.
       if (mask != (1 << kPfKB) - 1 || kPfKeys * (j + 1) - 1 > pos0) {
         const int lim = p_r - kPfKeys * j;          // keys c <= lim are causal for this row
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
+        for (int c = 0; c < kPfKeys; ++c)
           if (!((mask >> (c / kBlockSize)) & 1) || c > lim) sc[c] = -INFINITY;
       }
-      float mt[16];
+      float mt[32];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) mt[c] = fmaxf(sc[c], sc[c + 16]);
+      for (int c = 0; c < 32; ++c) mt[c] = fmaxf(sc[c], sc[c + 32]);
 #pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
+      for (int w = 16; w >= 1; w >>= 1)
 #pragma unroll
         for (int c = 0; c < w; ++c) mt[c] = fmaxf(mt[c], mt[c + w]);
       // Shift m in the log2 domain (scale * log2(e) applied): it moves to the row maximum only
@@ -338,20 +370,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       m = mn;
       // P = 2^(scale_log2 s - shift), rounded to bf16 (the MMA operand); the row sum adds the
       // same rounded values
-      uint32_t pw[16];
+      uint32_t pw[kPfKeys / 2];
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
+      for (int k = 0; k < kPfKeys / 2; ++k) {
         pw[k] = pack_bf16x2(ex2_ftz(fmaf(sc[2 * k], sl, -sh)), ex2_ftz(fmaf(sc[2 * k + 1], sl, -sh)));
         ps[k & 3] += bf16lo(pw[k]) + bf16hi(pw[k]);
       }
       l = fmaf(l, alpha, (ps[0] + ps[1]) + (ps[2] + ps[3]));
-      tmem_st16(sbuf, pw);                          // P_j over the first 16 columns of S_j
-      // O *= alpha once P V of the previous stage has landed (warp-collective TMEM access)
+      // O *= alpha once P V of stage j - 1 has landed (warp-collective TMEM access).  It completes
+      // use (j - 1) / kPfStages of its stage's kv_empty barrier; the use before is complete (it
+      // preceded S_j) and the next one needs this stage's P, so the parity is unambiguous.
       if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
-        // P V of stage j - 1 was issued after S_j, so o_ready has completed j - 1 or j times
-        // here: its parity names the phase of stage j - 1 without ambiguity
-        if (!__all_sync(kFullMask, mbar_wait_bounded(raw + kBarOReady, (j - 1) & 1))) {
+        const int pj = j - 1;
+        if (!__all_sync(kFullMask, mbar_wait_bounded(raw + kBarKvEmpty + 8 * (pj % kPfStages),
+                                                     (pj / kPfStages) & 1))) {
           failed = true;
           break;
         }
@@ -365,26 +398,36 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
           for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
           tmem_st32(trow + kPfOCol + 32 * q4, ov);
         }
+        tmem_wait_st();
+      }
+      unsigned char* stage_gen = smem_raw + (stages - raw) + st * kPfStageBytes;
+      // P row r over K_j (S_j is complete, so the tensor core no longer reads K_j): 64 keys =
+      // 8 chunks of 16 bytes, chunk c at c ^ (r % 8)
+      {
+        unsigned char* prow = stage_gen + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+              make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
       }
       // Keys past the context in its last block: zero their V rows (both 64-column halves).
       const int vb = last_blk - kPfKB * j;
       if (valid_last < kBlockSize && vb >= 0 && vb < kPfKB && ((mask >> vb) & 1)) {
         const int chunks = (kBlockSize - valid_last) * 16;
-        unsigned char* vt = smem_raw + (stages - raw) + st * kPfStageBytes + kPfVOff + vb * kTileBytes;
+        unsigned char* vt = stage_gen + kPfVOff + vb * kTileBytes;
         for (int x = r; x < chunks; x += 128) {
           const int row = valid_last + (x >> 4), half = (x >> 3) & 1, ch = x & 7;
           *reinterpret_cast<uint4*>(vt + half * kPfHalf + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
-        fence_proxy_async_smem();                   // before the tensor core reads the tile
       }
-      tmem_wait_st();
+      fence_proxy_async_smem();                     // P and zeroed V rows before the tensor core reads them
       tc_fence_before();
       mbar_arrive(raw + kBarPFull + 8 * (j & 1));
     }
     if (failed) {
       if (lane == 0) raise_flag(a.status, PA_FLAG_TIMEOUT);
     } else if (__all_sync(kFullMask, mbar_wait_bounded(raw + kBarDone, 0))) {
-      // ---- out = O / l for the tile's real rows (kBarDone: the MMA thread's last P V) --------
+      // ---- out = O / l for the tile's real rows (kBarDone: the MMA thread's last P V) ---------
       tc_fence_after();
       // a row whose every key was skipped (all its blocks out of range) has l = 0 and an O
       // never written: it stores zeros
