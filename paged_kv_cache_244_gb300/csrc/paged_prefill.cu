@@ -174,33 +174,29 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
         failed = true;
         break;
       }
-      int blk[kPfKB];
-#pragma unroll
-      for (int i = 0; i < kPfKB; ++i) blk[i] = __shfl_sync(kFullMask, ids, k + i);
+      // Lane l checks block 4j + l % 4 and, for l < 12, issues one of its three boxes (K cols
+      // 0-63, K cols 64-127, V): one thread issuing every box of a stage takes longer.  Lane 0
+      // announces the stage's bytes before any box is issued.
+      const int bi = lane & (kPfKB - 1), kind = lane / kPfKB;
+      const int blk = __shfl_sync(kFullMask, ids, k + bi);
+      const int b = kPfKB * j + bi;
+      const bool here = b < nblocks && blk >= 0 && blk < a.num_blocks;
+      const int mask = static_cast<int>(__ballot_sync(kFullMask, here) & ((1u << kPfKB) - 1));
+      if (lane < kPfKB && b < nblocks && !here) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
+      const uint32_t bar = raw + kBarKvFull + 8 * st;
       if (lane == 0) {
-        int mask = 0;
-#pragma unroll
-        for (int i = 0; i < kPfKB; ++i) {
-          const int b = kPfKB * j + i;
-          if (b < nblocks && blk[i] >= 0 && blk[i] < a.num_blocks) mask |= 1 << i;
-          else if (b < nblocks) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
-        }
         present[st] = mask;
-        const uint32_t bar = raw + kBarKvFull + 8 * st;
+        if (mask) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask)) * (2 * kTileBytes));
+        else mbar_arrive(bar);
+      }
+      __syncwarp();
+      if (kind < 3 && here) {
+        const int y = (blk * Hkv + g) * kBlockSize;
         const uint32_t dst = stages + st * kPfStageBytes;
-        if (mask) {
-          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask)) * (2 * kTileBytes));
-#pragma unroll
-          for (int i = 0; i < kPfKB; ++i) {
-            if (!(mask & (1 << i))) continue;
-            const int y = (blk[i] * Hkv + g) * kBlockSize;
-            tma_load_3d(dst + i * kPfHalf, &tm_kh, 0, y, 0, bar);                  // K cols 0-63
-            tma_load_3d(dst + kPfKHalfBytes + i * kPfHalf, &tm_kh, 0, y, 1, bar);  // K cols 64-127
-            tma_load_3d(dst + kPfVOff + i * kTileBytes, &tm_v, 0, y, 0, bar);      // V, both halves
-          }
-        } else {
-          mbar_arrive(bar);
-        }
+        if (kind < 2)
+          tma_load_3d(dst + kind * kPfKHalfBytes + bi * kPfHalf, &tm_kh, 0, y, kind, bar);   // K cols 64 kind + 0..63
+        else
+          tma_load_3d(dst + kPfVOff + bi * kTileBytes, &tm_v, 0, y, 0, bar);                  // V, both halves
       }
       issued = j + 1;
     }
@@ -368,16 +364,30 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       const float sh = mn == -INFINITY ? 0.f : mn;  // a row with no key yet keeps the shift 0
       const float alpha = (mn == m || m == -INFINITY) ? 1.f : ex2_ftz(m - sh);
       m = mn;
-      // P = 2^(scale_log2 s - shift), rounded to bf16 (the MMA operand); the row sum adds the
-      // same rounded values
+      // P = 2^(scale_log2 s - shift) with the exponent argument formed two at a time (packed
+      // fp32 FMA), rounded to bf16 (the MMA operand).  The row sum adds the fp32 values, two at
+      // a time; it differs from the sum of the rounded values by the rounding errors of P, about
+      // 2^-9 of each term and of random sign.
       uint32_t pw[kPfKeys / 2];
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint64_t psum[4] = {0ull, 0ull, 0ull, 0ull};
+      const uint64_t sl2 = pack_f32x2(sl, sl), nsh2 = pack_f32x2(-sh, -sh);
 #pragma unroll
       for (int k = 0; k < kPfKeys / 2; ++k) {
-        pw[k] = pack_bf16x2(ex2_ftz(fmaf(sc[2 * k], sl, -sh)), ex2_ftz(fmaf(sc[2 * k + 1], sl, -sh)));
-        ps[k & 3] += bf16lo(pw[k]) + bf16hi(pw[k]);
+        const uint64_t x = fma_f32x2(pack_f32x2(sc[2 * k], sc[2 * k + 1]), sl2, nsh2);
+        float x0, x1;
+        unpack_f32x2(x, x0, x1);
+        const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+        pw[k] = pack_bf16x2(p0, p1);
+        psum[k & 3] = add_f32x2(psum[k & 3], pack_f32x2(p0, p1));
       }
-      l = fmaf(l, alpha, (ps[0] + ps[1]) + (ps[2] + ps[3]));
+      float ps;
+      {
+        const uint64_t t = add_f32x2(add_f32x2(psum[0], psum[1]), add_f32x2(psum[2], psum[3]));
+        float t0, t1;
+        unpack_f32x2(t, t0, t1);
+        ps = t0 + t1;
+      }
+      l = fmaf(l, alpha, ps);
       // O *= alpha once P V of stage j - 1 has landed (warp-collective TMEM access).  It completes
       // use (j - 1) / kPfStages of its stage's kv_empty barrier; the use before is complete (it
       // preceded S_j) and the next one needs this stage's P, so the parity is unambiguous.
