@@ -288,6 +288,13 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (a NaN operand is ignored, as by fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // ---- packed fp32 pairs (Blackwell f32x2 arithmetic: two lanes' worth per instruction) ------
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
   uint64_t r;

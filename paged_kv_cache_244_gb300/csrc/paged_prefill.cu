@@ -350,16 +350,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
         for (int c = 0; c < kPfKeys; ++c)
           if (!((mask >> (c / kBlockSize)) & 1) || c > lim) sc[c] = -INFINITY;
       }
-      float mt[32];
+      // row maximum by three-input max: 64 -> 22 -> 8 -> 3 -> 1
+      float m1[22], m2[8];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) mt[c] = fmaxf(sc[c], sc[c + 32]);
+      for (int c = 0; c < 21; ++c) m1[c] = fmax3(sc[3 * c], sc[3 * c + 1], sc[3 * c + 2]);
+      m1[21] = sc[63];
 #pragma unroll
-      for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-        for (int c = 0; c < w; ++c) mt[c] = fmaxf(mt[c], mt[c + w]);
+      for (int c = 0; c < 7; ++c) m2[c] = fmax3(m1[3 * c], m1[3 * c + 1], m1[3 * c + 2]);
+      m2[7] = m1[21];
+      const float mrow = fmax3(fmax3(m2[0], m2[1], m2[2]), fmax3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
       // Shift m in the log2 domain (scale * log2(e) applied): it moves to the row maximum only
       // when that exceeds it by more than 8, so P stays at most 2^8 and O is rescaled rarely.
-      const float bs = mt[0] * sl;
+      const float bs = mrow * sl;
       const float mn = bs > m + 8.f ? bs : m;
       const float sh = mn == -INFINITY ? 0.f : mn;  // a row with no key yet keeps the shift 0
       const float alpha = (mn == m || m == -INFINITY) ? 1.f : ex2_ftz(m - sh);
