@@ -30,7 +30,8 @@ The printed JSON line carries:
                        HBM peak, decode tokens/s (--no-configs skips it);
   cpu_baseline         the fp64 oracle on the host cores over a bounded sample;
   fp8_kv               the step's decode on E4M3 caches (pa_decode_fp8, pa_decode_step_fp8),
-                       bandwidth counted on the E4M3 bytes (--no-fp8 skips it);
+                       bandwidth counted on the E4M3 bytes, and beside it gather_floor_*:
+                       pa_gather_checksum_fp8, the same tile gather alone (--no-fp8 skips it);
   prefill              pa_prefill on two prefill workloads, TFLOP/s against the measured bf16
                        dense peak, and pa_rope_kv_store of their new tokens against the HBM
                        copy bandwidth (--no-prefill skips it);
@@ -510,9 +511,10 @@ def block_ops(torch, binding, flush_l2, timed_loop, w, layers=28, pool_blocks=10
 
 def fp8_kv(torch, binding, timed_loop, st, steps):
     """The step's decode on E4M3 caches (one byte per element, one scale per KV head), layer 0
-    of the workload: pa_decode_fp8 and pa_decode_step_fp8, L2 flushed before each call.  The
-    codes are made once on the GPU with torch's float8 cast from the bf16 caches (set-up, not
-    timed); achieved bandwidth counts the E4M3 bytes, half the bf16 bytes."""
+    of the workload: pa_decode_fp8 and pa_decode_step_fp8, L2 flushed before each call, and
+    pa_gather_checksum_fp8 (the same tile gather without attention or merge) as their floor.
+    The codes are made once on the GPU with torch's float8 cast from the bf16 caches (set-up,
+    not timed); achieved bandwidth counts the E4M3 bytes, half the bf16 bytes."""
     w = st.w
 
     def codes(cache):
@@ -531,10 +533,16 @@ def fp8_kv(torch, binding, timed_loop, st, steps):
                                           st.block_tables, st.context_lens, w.max_context_len,
                                           w.scale, partition_tokens=st.P, workspace=st.workspace,
                                           out=out)
+    # the floor of the E4M3 decode's access pattern: its tile gather alone, same kernel shape
+    gx = torch.zeros((w.num_seqs, w.num_kv_heads), dtype=torch.int32, device=k8.device)
+    gat = lambda: binding.gather_checksum(k8, v8, st.block_tables, st.context_lens, w.max_context_len,
+                                          w.num_q_heads, out_xor=gx)
     dec()
     stp()
+    gat()
     dec_ms = float(np.mean(timed_loop(dec, steps)))
     stp_ms = float(np.mean(timed_loop(stp, steps)))
+    gat_ms = float(np.mean(timed_loop(gat, steps)))
     rc, flags = binding.get_device_status()
     if rc != 0:
         raise RuntimeError(f"device status after the E4M3 decode: {rc} flags {flags:#x}")
@@ -545,6 +553,9 @@ def fp8_kv(torch, binding, timed_loop, st, steps):
             "pa_decode_fp8_us": round(dec_ms * 1e3, 3), "GB/s": round(gbs, 1),
             "frac_of_hbm_copy_peak": round(gbs / peak, 4),
             "pa_decode_step_fp8_us": round(stp_ms * 1e3, 3),
+            "gather_floor_us": round(gat_ms * 1e3, 3),
+            "gather_floor_frac": round(nbytes / (gat_ms * 1e-3) / 1e9 / peak, 4),
+            "decode_over_floor": round(dec_ms / gat_ms, 4),
             "context_tokens_per_s": round(int(w.context_lens.astype(np.int64).sum()) / (dec_ms * 1e-3), 1)}
 
 

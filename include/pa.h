@@ -423,6 +423,17 @@ int pa_gather_checksum(const pa_dims* dims, int num_seqs, const void* k_cache, c
                        const int32_t* context_lens, int max_context_len, uint32_t* out_xor,
                        void* stream);
 
+/*
+ * pa_gather_checksum_fp8 -- pa_gather_checksum over E4M3 caches ([num_blocks][Hkv][16][128]
+ * one-byte codes, the layout of pa_decode_fp8): the gather half of pa_decode_fp8 alone, by the
+ * same kernel shape.  Each row is 128 bytes = 32 32-bit words of codes as stored; otherwise as
+ * pa_gather_checksum (no scales are read).
+ */
+int pa_gather_checksum_fp8(const pa_dims* dims, int num_seqs, const void* k_cache,
+                           const void* v_cache, int num_blocks, const int32_t* block_tables,
+                           int max_blocks, const int32_t* context_lens, int max_context_len,
+                           uint32_t* out_xor, void* stream);
+
 /* Human-readable name of a PA_* return code (static storage, never NULL). */
 const char* pa_status_string(int status);
 

@@ -80,6 +80,8 @@ def lib():
         L.pa_decode_step_fp8.restype = i
         L.pa_gather_checksum.argtypes = [pd, i, p, p, i, p, i, p, i, p, p]
         L.pa_gather_checksum.restype = i
+        L.pa_gather_checksum_fp8.argtypes = [pd, i, p, p, i, p, i, p, i, p, p]
+        L.pa_gather_checksum_fp8.restype = i
         L.pa_prefill.argtypes = [pd, i, i, p, p, i, p, p, i, p, i, p, i, f, p, p]
         L.pa_prefill.restype = i
         L.pa_copy_blocks.argtypes = [pd, i, p, ctypes.c_int64, p, ctypes.c_int64, p, i, p]
@@ -312,23 +314,25 @@ def rope_kv_store_fp8(q, k, v, positions, cos_sin, slot_mapping, k_cache, v_cach
 
 def gather_checksum(k_cache, v_cache, block_tables, context_lens, max_context_len, num_q_heads,
                     out_xor=None, stream=None):
-    """pa_gather_checksum: XOR of the tile words of every (sequence, KV head)'s context, read
-    through the block tables the way pa_decode reads them.  out_xor [S, Hkv] int32 (zero-filled
-    here when None) is XORed into and returned."""
+    """pa_gather_checksum (bf16 caches) or pa_gather_checksum_fp8 (uint8 E4M3 caches): XOR of the
+    tile words of every (sequence, KV head)'s context, read through the block tables the way
+    the decode reads them.  out_xor [S, Hkv] int32 (zero-filled here when None) is XORed into
+    and returned."""
     nb, Hkv, B, D = k_cache.shape
     S = context_lens.shape[0]
     if tuple(v_cache.shape) != tuple(k_cache.shape) or block_tables.shape[0] != S:
         raise ValueError("shape mismatch between the caches, block_tables and context_lens")
+    fp8 = k_cache.dtype == torch.uint8
+    dt = torch.uint8 if fp8 else torch.bfloat16
     if out_xor is None:
         out_xor = torch.zeros((S, Hkv), dtype=torch.int32, device=k_cache.device)
     dims = make_dims(num_q_heads, Hkv, D, B)
-    rc = lib().pa_gather_checksum(
-        ctypes.byref(dims), S, _dev_ptr(k_cache, "k_cache", torch.bfloat16),
-        _dev_ptr(v_cache, "v_cache", torch.bfloat16), nb,
-        _dev_ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
-        _dev_ptr(context_lens, "context_lens", torch.int32), int(max_context_len),
-        _dev_ptr(out_xor, "out_xor", torch.int32), _stream(stream))
-    _check(rc, "pa_gather_checksum")
+    fn = lib().pa_gather_checksum_fp8 if fp8 else lib().pa_gather_checksum
+    rc = fn(ctypes.byref(dims), S, _dev_ptr(k_cache, "k_cache", dt), _dev_ptr(v_cache, "v_cache", dt), nb,
+            _dev_ptr(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+            _dev_ptr(context_lens, "context_lens", torch.int32), int(max_context_len),
+            _dev_ptr(out_xor, "out_xor", torch.int32), _stream(stream))
+    _check(rc, "pa_gather_checksum_fp8" if fp8 else "pa_gather_checksum")
     return out_xor
 
 

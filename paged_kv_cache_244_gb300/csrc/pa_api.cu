@@ -296,10 +296,12 @@ int pa_decode(const pa_dims* dims, int num_seqs, const void* q, const void* k_ca
                                                                                  : PA_ERR_CUDA;
 }
 
-int pa_gather_checksum(const pa_dims* dims, int num_seqs, const void* k_cache, const void* v_cache,
-                       int num_blocks, const int32_t* block_tables, int max_blocks,
-                       const int32_t* context_lens, int max_context_len, uint32_t* out_xor,
-                       void* stream) {
+namespace {
+
+int gather_checksum(const pa_dims* dims, int num_seqs, const void* k_cache, const void* v_cache,
+                    int num_blocks, const int32_t* block_tables, int max_blocks,
+                    const int32_t* context_lens, int max_context_len, uint32_t* out_xor, bool fp8,
+                    void* stream) {
   if (const int rc = check_dims(dims)) return rc;
   if (num_seqs < 0 || num_seqs > pa::kMaxDecodeSeqs) return PA_ERR_RANGE;
   if (num_seqs == 0) return PA_OK;
@@ -333,7 +335,25 @@ int pa_gather_checksum(const pa_dims* dims, int num_seqs, const void* k_cache, c
   a.max_parts = 1;
   a.status = status;
   a.gather_xor = out_xor;
-  return pa::launch_gather(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return pa::launch_gather(a, fp8, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+int pa_gather_checksum(const pa_dims* dims, int num_seqs, const void* k_cache, const void* v_cache,
+                       int num_blocks, const int32_t* block_tables, int max_blocks,
+                       const int32_t* context_lens, int max_context_len, uint32_t* out_xor,
+                       void* stream) {
+  return gather_checksum(dims, num_seqs, k_cache, v_cache, num_blocks, block_tables, max_blocks,
+                         context_lens, max_context_len, out_xor, false, stream);
+}
+
+int pa_gather_checksum_fp8(const pa_dims* dims, int num_seqs, const void* k_cache,
+                           const void* v_cache, int num_blocks, const int32_t* block_tables,
+                           int max_blocks, const int32_t* context_lens, int max_context_len,
+                           uint32_t* out_xor, void* stream) {
+  return gather_checksum(dims, num_seqs, k_cache, v_cache, num_blocks, block_tables, max_blocks,
+                         context_lens, max_context_len, out_xor, true, stream);
 }
 
 int pa_decode_step(const pa_dims* dims, int num_seqs, const void* q, const void* k, const void* v,

@@ -121,7 +121,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const BlockCopyArgs& a, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
-// The decode kernel's gather of K/V tiles alone (no attention, no merge): pa_gather_checksum.
-cudaError_t launch_gather(const DecodeArgs& a, cudaStream_t stream);
+// The decode kernel's gather of K/V tiles alone (no attention, no merge): pa_gather_checksum,
+// over bf16 or E4M3 (fp8) caches.
+cudaError_t launch_gather(const DecodeArgs& a, bool fp8, cudaStream_t stream);
 
 }  // namespace pa

@@ -398,14 +398,16 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
     const uint32_t vt = kt + (kFp8 ? L::kTile : 2 * kHalfBytes);
     unsigned char* const stage = smem_raw + (kt - raw);  // generic address of the stage
     if constexpr (kGather) {
-      // The stage's 8 KiB are [K cols 0-63 | K cols 64-127 | V cols 0-63 | V cols 64-127], each
-      // 16 rows of 128 bytes whose 16-byte chunks the swizzle permutes within the row: chunk c
-      // (16 bytes at 16 c) lies in row (c / 8) % 16.  XOR the words of the valid rows.
+      // bf16: the stage's 8 KiB are [K cols 0-63 | K cols 64-127 | V cols 0-63 | V cols 64-127];
+      // E4M3: 4 KiB, [K | V].  Either way 16-row pieces of 128-byte rows whose 16-byte chunks the
+      // swizzle permutes within the row: chunk c (16 bytes at 16 c) lies in row (c / 8) % 16.
+      // XOR the words of the valid rows.
+      constexpr int kPasses = kFp8 ? 8 : 16;        // 32 lanes x 16 bytes per pass
       if (fl & kFirst) gx = 0;
       if (fl & kHasData) {
         const int valid = static_cast<int>((fl >> 8) & 0xffu);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < kPasses; ++i) {
           const int c = lane + 32 * i;
           if (((c >> 3) & 15) < valid) {
             const uint4 wv = *reinterpret_cast<const uint4*>(stage + 16 * c);
@@ -962,8 +964,8 @@ cudaError_t persistent_ctas(int* ctas) {
     auto kernel = decode_partition_kernel<kStep, kFp8>;
     err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    if (!kStep && !kFp8) {  // the gather runs the same kernel shape
-      err = cudaFuncSetAttribute(decode_partition_kernel<false, false, true>,
+    if (!kStep) {  // the gather runs the same kernel shape
+      err = cudaFuncSetAttribute(decode_partition_kernel<false, kFp8, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (err != cudaSuccess) return err;
     }
@@ -1063,17 +1065,18 @@ bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* 
   return true;
 }
 
-cudaError_t launch_gather(const DecodeArgs& args, cudaStream_t stream) {
+cudaError_t launch_gather(const DecodeArgs& args, bool fp8, cudaStream_t stream) {
   DecodeArgs a = args;
   if (a.num_seqs > kMaxDecodeSeqs) return cudaErrorInvalidValue;
   const long long rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * kBlockSize;
   CUtensorMap tm_k, tm_v;
-  if (!cache_tensor_map(a.k_cache, rows, false, &tm_k) || !cache_tensor_map(a.v_cache, rows, false, &tm_v))
+  if (!cache_tensor_map(a.k_cache, rows, fp8, &tm_k) || !cache_tensor_map(a.v_cache, rows, fp8, &tm_v))
     return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  return launch_partition<false, false, true>(a, tm_k, tm_v, attr, stream);
+  return fp8 ? launch_partition<false, true, true>(a, tm_k, tm_v, attr, stream)
+             : launch_partition<false, false, true>(a, tm_k, tm_v, attr, stream);
 }
 
 cudaError_t launch_decode(const DecodeArgs& args, cudaStream_t stream) {

@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
                  "pa_decode_partition_tokens", "pa_get_device_status", "pa_status_string",
                  "pa_selftest_wait_timeout", "pa_decode_static_workspace", "pa_decode_step",
                  "pa_copy_blocks", "pa_rope_kv_store_fp8", "pa_decode_fp8", "pa_decode_step_fp8",
-                 "pa_prefill", "pa_gather_checksum"):
+                 "pa_prefill", "pa_gather_checksum", "pa_gather_checksum_fp8"):
         assert must in names
 
 

@@ -1,9 +1,9 @@
-"""pa_gather_checksum: the decode kernel's gather of K/V tiles without the attention.
+"""pa_gather_checksum(_fp8): the decode kernels' gather of K/V tiles without the attention.
 
 The expected value is the checksum's plain definition, computed here with numpy from the
 host caches: for every (sequence, KV head), the XOR of all 32-bit words of its K and V rows
-t < context length, reached through the block table.  XOR does not depend on the order of
-the work, so the result is compared bit for bit.
+t < context length, reached through the block table (a bf16 row is 64 words, an E4M3 row
+32).  XOR does not depend on the order of the work, so the result is compared bit for bit.
 """
 
 from __future__ import annotations
@@ -46,9 +46,17 @@ def expected_xor(k_cache, v_cache, block_tables, context_lens, max_context_len):
 
 
 def run(pa, w, kc, vc, bt, ctx, maxctx):
-    got = pa.gather_checksum(dev_bf16(kc), dev_bf16(vc), dev(bt), dev(ctx), maxctx, w.num_q_heads)
+    put = dev if kc.dtype == np.uint8 else dev_bf16
+    got = pa.gather_checksum(put(kc), put(vc), dev(bt), dev(ctx), maxctx, w.num_q_heads)
     torch.cuda.synchronize()
     return got.cpu().numpy().view(np.uint32)
+
+
+def e4m3_caches(w, seed):
+    """Seeded random code bytes in the E4M3 cache layout (the checksum reads them as stored)."""
+    rng = np.random.default_rng(seed)
+    shape = (w.num_blocks, w.num_kv_heads, 16, 128)
+    return rng.integers(0, 256, size=shape, dtype=np.uint8), rng.integers(0, 256, size=shape, dtype=np.uint8)
 
 
 @pytest.mark.parametrize("name", W.WORKLOADS)
@@ -56,6 +64,17 @@ def test_gather_checksum_matches_definition(pa, name):
     w = W.make(name)
     want = expected_xor(w.k_cache[0], w.v_cache[0], w.block_tables, w.context_lens, w.max_context_len)
     got = run(pa, w, w.k_cache[0], w.v_cache[0], w.block_tables, w.context_lens, w.max_context_len)
+    assert np.array_equal(got, want)
+    rc, flags = pa.get_device_status()
+    assert rc == 0 and flags == 0, (rc, hex(flags))
+
+
+@pytest.mark.parametrize("name", W.WORKLOADS)
+def test_gather_checksum_fp8_matches_definition(pa, name):
+    w = W.make(name)
+    k8, v8 = e4m3_caches(w, 3100 + W.WORKLOADS.index(name))
+    want = expected_xor(k8, v8, w.block_tables, w.context_lens, w.max_context_len)
+    got = run(pa, w, k8, v8, w.block_tables, w.context_lens, w.max_context_len)
     assert np.array_equal(got, want)
     rc, flags = pa.get_device_status()
     assert rc == 0 and flags == 0, (rc, hex(flags))
