@@ -141,3 +141,27 @@ def test_prefill_out_of_range_block_is_flagged(pa, orc):
     rows = slice(0, int(w.q_start[1]))                          # sequence 0 is untouched by it
     assert_out_close(host_bits(got)[rows], ref[rows])
     check_status_clean(pa)
+
+
+def test_prefill_first_block_out_of_range(pa, orc):
+    """Sequence 1's first block id is out of range: that block is skipped.  Its queries 0-15 see
+    keys of block 0 only, so every key of theirs is skipped and they store zeros (the tile's
+    first P V never runs for them).  Query i >= 16 attends over keys 16..i alone, which is the
+    oracle's decode of that query over the block table shifted by one block (attention depends
+    on the set of keys, and RoPE is already in K)."""
+    w = W.build_prefill("pf_blk0", [40, 50], [40, 50], 16, 106)
+    bt = w.block_tables.copy()
+    bt[1, 0] = -1
+    got = host_bits(pa.prefill(dev_bf16(w.q), dev(w.q_start), dev_bf16(w.k_cache), dev_bf16(w.v_cache),
+                               dev(bt), dev(w.context_lens), w.max_query_len, w.max_context_len, w.scale))
+    rc, flags = pa.get_device_status()
+    assert flags == pa.PA_FLAG_BLOCK_ID_OOB
+    q1 = int(w.q_start[1])
+    assert (W.bf16_bits_to_f32(got[q1:q1 + 16]) == 0.0).all()
+    rows = np.arange(16, int(w.context_lens[1]))
+    shifted = np.tile(w.block_tables[1, 1:], (len(rows), 1))
+    ref, _ = orc.decode(w.q[q1 + rows], w.k_cache, w.v_cache, shifted, (rows - 15).astype(np.int32), w.scale)
+    assert_out_close(got[q1 + rows], ref, "shifted")
+    ref_all, _ = orc.prefill(w.q, w.q_start, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale)
+    assert_out_close(got[:q1], ref_all[:q1], "untouched sequence")
+    check_status_clean(pa)
