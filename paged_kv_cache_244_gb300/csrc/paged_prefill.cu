@@ -124,6 +124,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
   const uint32_t stages = (raw + kPfHeader + 1023u) & ~1023u;
   volatile int* present = reinterpret_cast<volatile int*>(smem_raw + kPresent);
 
+  // The first global reads of each role go out before the set-up below, so their latency
+  // overlaps it: the softmax threads' Q rows, the TMA warp's first two windows of block ids.
+  const int32_t* bt_row = a.block_tables + static_cast<size_t>(s) * a.max_blocks;
+  auto load_ids = [&](int w) { const int b = 32 * w + lane; return b < nblocks ? bt_row[b] : -1; };
+  int ids = -1, ids_next = -1;
+  uint4 qpre[16];
+  if (warp == 4) {
+    ids = load_ids(0);
+    ids_next = load_ids(1);
+  } else if (warp < 4) {
+    // row r = query i, head g G + h: 128 bf16 (zero past the queries)
+    const int r = threadIdx.x, i = r / G, h = r - (r / G) * G;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        a.q + (static_cast<size_t>(q0 + i0 + (i < rows_q ? i : 0)) * a.num_q_heads + g * G + h) * kHeadDim);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) qpre[c] = i < rows_q ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPfStages; ++i) {
       mbar_init(raw + kBarKvFull + 8 * i, 1);
@@ -154,10 +171,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       prefetch_tensor_map(&tm_kh);
       prefetch_tensor_map(&tm_v);
     }
-    const int32_t* bt_row = a.block_tables + static_cast<size_t>(s) * a.max_blocks;
-    auto load_ids = [&](int w) { const int b = 32 * w + lane; return b < nblocks ? bt_row[b] : -1; };
-    int ids = load_ids(0);
-    int ids_next = load_ids(1);
     int issued = 0;
     bool failed = false;
     for (int j = 0; j < nst; ++j) {
@@ -288,15 +301,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
     const int p_r = pos0 + i;                       // rows past the tile's queries are never stored
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     {
-      // row r = query i, head g G + h: 128 bf16 = 64 columns of pairs (zero past the queries)
-      const uint4* src = reinterpret_cast<const uint4*>(
-          a.q + (static_cast<size_t>(q0 + i0 + (i < rows_q ? i : 0)) * a.num_q_heads + g * G + h) * kHeadDim);
+      // Q row r (loaded before the set-up) = 64 columns of bf16 pairs
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t qv[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 v = i < rows_q ? src[8 * half + c] : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 v = qpre[8 * half + c];
           qv[4 * c] = v.x;
           qv[4 * c + 1] = v.y;
           qv[4 * c + 2] = v.z;
