@@ -553,10 +553,11 @@ decode_partition_kernel(const __grid_constant__ CUtensorMap tm_k,
           mma_f16_16816(sc, lo0, lo1, hi0, hi1, qb[2 * c2][0], qb[2 * c2][1]);
           e4m3x4_to_f16x2x2(w2, lo0, hi0);
           e4m3x4_to_f16x2x2(w3, lo1, hi1);
-          mma_f16_16816(sc, lo0, lo1, hi0, hi1, qb[2 * c2 + 1][0], qb[2 * c2 + 1][1]);
+          // two accumulator chains, as for bf16: the MMAs issue in program order
+          mma_f16_16816(sc2, lo0, lo1, hi0, hi1, qb[2 * c2 + 1][0], qb[2 * c2 + 1][1]);
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) sc[i] *= k_fold;
+        for (int i = 0; i < 4; ++i) sc[i] = (sc[i] + sc2[i]) * k_fold;
       } else {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
