@@ -69,9 +69,9 @@ METRIC = "paged GQA decode: KV-cache HBM GB/s (% of GB300 peak) and attention to
 # the step form and a hash of the CUDA sources it was taken on: once a kernel changes, the
 # hash no longer matches and roofline.traffic is reported as null until it is captured again.
 MEASURED_TRAFFIC = {
-    ("mix64", "fused", "c63a37d6dd34bdf3"): 122114816 + 3408384 + 4185600,
-    ("prefix32", "fused", "c63a37d6dd34bdf3"): 4348928 + 0 + 3823104,
-    ("long4", "fused", "c63a37d6dd34bdf3"): 83981568 + 2109952 + 4823296,
+    ("mix64", "fused", "579864ccac2b18c4"): 122111744 + 3003136 + 4185856,
+    ("prefix32", "fused", "579864ccac2b18c4"): 4348928 + 0 + 3823104,
+    ("long4", "fused", "579864ccac2b18c4"): 83982080 + 2082304 + 4823040,
 }
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
