@@ -165,3 +165,14 @@ def test_prefill_first_block_out_of_range(pa, orc):
     ref_all, _ = orc.prefill(w.q, w.q_start, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale)
     assert_out_close(got[:q1], ref_all[:q1], "untouched sequence")
     check_status_clean(pa)
+
+
+@pytest.mark.parametrize("hq,hkv,ctx,ql", [(2, 2, [4100, 1200], [300, 130]), (12, 2, [9000, 777], [150, 40])])
+def test_prefill_long_contexts_every_row(pa, orc, hq, hkv, ctx, ql):
+    """Chunks late in long contexts (many 64-key stages, block ids read window after window) and
+    G = 1 (128 queries per tile, every row its own query): every row against the oracle."""
+    nb = sum((c + 15) // 16 for c in ctx) + 9
+    w = W.build_prefill("pf_long", ctx, ql, nb, 107, num_q_heads=hq, num_kv_heads=hkv)
+    ref, _ = orc.prefill(w.q, w.q_start, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale)
+    assert_out_close(run_prefill(pa, w), ref, f"{hq}/{hkv}")
+    check_status_clean(pa)
