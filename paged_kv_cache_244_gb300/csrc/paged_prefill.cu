@@ -18,8 +18,8 @@
 //   softmax (one thread per row): S_j read with tcgen05.ld, causal mask, a lazy row shift in
 //   the log2 domain (it moves only when the row maximum passes it by more than 8, so P <= 2^8
 //   and O is rarely rescaled), P_j = bf16(2^(scale_log2 s - shift)) written to shared memory
-//   over K_j (dead once S_j is done; 128 rows x 64 keys is exactly its size), the same rounded
-//   values added to the row sum
+//   over K_j (dead once S_j is done; 128 rows x 64 keys is exactly its size), the fp32 values
+//   added to the row sum (exponent arguments and sums two at a time, packed f32x2)
 //   O (128 x 128, fp32, TMEM) += P_j V_j   4 tcgen05.mma (one per key block), M = N = 128, K = 16
 // Tensor memory (256 columns): Q as bf16 pairs in columns 0-63 (the A operand of S, read from
 // tensor memory: with N = 64 an A read from shared memory at every MMA would crowd shared
@@ -27,7 +27,8 @@
 // 64, so S runs 64 keys wide.
 //
 // Warps 0-3 load Q and run the softmax (warp w owns TMEM lanes 32w..32w+31); warp 4 issues the
-// TMA loads (its lanes read 32 block ids at a time, a window ahead); warp 5 runs the MMA loop,
+// TMA loads (lanes 0-11 one box each; its lanes read 32 block ids at a time, a window ahead);
+// warp 5 runs the MMA loop,
 // one elected lane issuing.  The softmax frees the S columns as soon as it has loaded S_j, and
 // the MMA warp then issues S_{j+1} at once, so the tensor core computes the next scores (and
 // P_{j-1} V_{j-1}) while the softmax works on stage j.  Shared memory is ~97 KB, so two CTAs
