@@ -29,10 +29,9 @@
 // Warps 0-3 load Q and run the softmax (warp w owns TMEM lanes 32w..32w+31); warp 4 issues the
 // TMA loads (lanes 0-11 one box each; its lanes read 32 block ids at a time, a window ahead);
 // warp 5 runs the MMA loop, one elected lane issuing.  The softmax frees the S columns as soon
-// as it has loaded S_j, and
-// the MMA warp then issues S_{j+1} at once, so the tensor core computes the next scores (and
-// P_{j-1} V_{j-1}) while the softmax works on stage j.  Shared memory is ~97 KB, so two CTAs
-// share an SM.
+// as it has loaded S_j, and the MMA warp then issues S_{j+1} at once, so the tensor core
+// computes the next scores (and P_{j-1} V_{j-1}) while the softmax works on stage j.  Shared
+// memory is ~97 KB, so two CTAs share an SM.
 //
 // K, V and P use the 128-byte swizzle (16-byte chunk c of a 128-byte row r at c ^ (r % 8),
 // 8-row atoms of 1024 bytes).  A stage holds K half 0 of the four blocks (rows 0-63, 8 KiB), K
