@@ -65,7 +65,7 @@ constexpr int kPfStageBytes = kPfVOff + kPfKB * kTileBytes;   // 32 KiB
 static_assert(kPfRows * kPfKeys * 2 == kPfVOff, "P of a stage fills its K region");
 constexpr int kPfHeader = 256;                      // mbarriers, present masks, TMEM address
 constexpr int kPfSmem = kPfHeader + 1024 + kPfStages * kPfStageBytes;
-constexpr int kPfThreads = 192;                     // 4 softmax warps, TMA warp, MMA warp
+constexpr int kPfThreads = 256;                     // 4 softmax warps, TMA warps 4, 6, 7, MMA warp 5
 constexpr uint32_t kPfTmemCols = 256;
 constexpr uint32_t kPfQCol = 0;                     // Q: 64 columns of bf16 pairs
 constexpr uint32_t kPfSCol = 64;                    // S: columns 64-127
@@ -130,7 +130,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
   auto load_ids = [&](int w) { const int b = 32 * w + lane; return b < nblocks ? bt_row[b] : -1; };
   int ids = -1, ids_next = -1;
   uint4 qpre[16];
-  if (warp == 4) {
+  const bool producer = warp == 4 || warp >= 6;
+  const int kind = warp == 4 ? 0 : warp - 5;        // producers: K cols 0-63, K cols 64-127, V
+  if (producer) {
     ids = load_ids(0);
     ids_next = load_ids(1);
   } else if (warp < 4) {
@@ -163,8 +165,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem_raw + kTmemSlot);
 
-  if (warp == 4) {
-    // ---- TMA producer: stage j holds key blocks 4j .. 4j + 3 --------------------------------
+  if (producer) {
+    // ---- TMA producers: stage j holds key blocks 4j .. 4j + 3 -------------------------------
+    // Three warps share a stage's 12 boxes, one kind each (lanes 0-3: the four blocks): a warp's
+    // TMA instruction issues its lanes' boxes one after another, so one warp issuing all 12
+    // leaves the stage latency-bound; with three, the SM's fill rate is the limit.  The first
+    // producer announces the stage's bytes and its present mask (the others' boxes may land
+    // first: the phase cannot complete before that arrival).
     // Lane k holds the id of block 32 w + k of the current window w (-1 past the tile's
     // blocks); the next window's ids are loaded when the current one starts.
     if (lane == 0) {
@@ -187,23 +194,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
         failed = true;
         break;
       }
-      // Lane l checks block 4j + l % 4 and, for l < 12, issues one of its three boxes (K cols
-      // 0-63, K cols 64-127, V): one thread issuing every box of a stage takes longer.  Lane 0
-      // announces the stage's bytes before any box is issued.
-      const int bi = lane & (kPfKB - 1), kind = lane / kPfKB;
+      const int bi = lane & (kPfKB - 1);
       const int blk = __shfl_sync(kFullMask, ids, k + bi);
       const int b = kPfKB * j + bi;
       const bool here = b < nblocks && blk >= 0 && blk < a.num_blocks;
       const int mask = static_cast<int>(__ballot_sync(kFullMask, here) & ((1u << kPfKB) - 1));
-      if (lane < kPfKB && b < nblocks && !here) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
       const uint32_t bar = raw + kBarKvFull + 8 * st;
-      if (lane == 0) {
-        present[st] = mask;
-        if (mask) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask)) * (2 * kTileBytes));
-        else mbar_arrive(bar);
+      if (kind == 0) {
+        if (lane < kPfKB && b < nblocks && !here) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
+        if (lane == 0) {
+          present[st] = mask;
+          if (mask) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask)) * (2 * kTileBytes));
+          else mbar_arrive(bar);
+        }
       }
-      __syncwarp();
-      if (kind < 3 && here) {
+      if (lane < kPfKB && here) {
         const int y = (blk * Hkv + g) * kBlockSize;
         const uint32_t dst = stages + st * kPfStageBytes;
         if (kind < 2)
@@ -213,7 +218,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       }
       issued = j + 1;
     }
-    if (lane == 0) {
+    if (kind == 0 && lane == 0) {
       if (failed) raise_flag(a.status, PA_FLAG_TIMEOUT);
       // Copies still in flight can only be those of the last kPfStages fills: let them land
       // (immediate in a normal run, where the MMAs consumed every stage) before the CTA exits.
