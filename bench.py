@@ -27,7 +27,9 @@ The printed JSON line carries:
                        layer, the same tile gather with no attention and no merge;
   configs              every named workload's step (tiny, qwen_b1 with its 28 layers, mix64,
                        prefix32, long4 with 512-token partitions): time, GB/s, fraction of the
-                       HBM peak, decode tokens/s (--no-configs skips it);
+                       HBM peak, decode tokens/s; and mix64_x28, the mix64 layer as the attention
+                       of a 28-layer model step, 28 device copies of its caches (--no-configs
+                       skips it);
   cpu_baseline         the fp64 oracle on the host cores over a bounded sample;
   fp8_kv               the step's decode on E4M3 caches (pa_decode_fp8, pa_decode_step_fp8),
                        bandwidth counted on the E4M3 bytes, and beside it gather_floor_*:
@@ -69,9 +71,9 @@ METRIC = "paged GQA decode: KV-cache HBM GB/s (% of GB300 peak) and attention to
 # the step form and a hash of the CUDA sources it was taken on: once a kernel changes, the
 # hash no longer matches and roofline.traffic is reported as null until it is captured again.
 MEASURED_TRAFFIC = {
-    ("mix64", "fused", "579864ccac2b18c4"): 122111744 + 3003136 + 4185856,
-    ("prefix32", "fused", "579864ccac2b18c4"): 4348928 + 0 + 3823104,
-    ("long4", "fused", "579864ccac2b18c4"): 83982080 + 2082304 + 4823040,
+    ("mix64", "fused", "0e6eeebffbc0a60b"): 122107904 + 2993408 + 4185600,
+    ("prefix32", "fused", "0e6eeebffbc0a60b"): 4348672 + 0 + 3823104,
+    ("long4", "fused", "0e6eeebffbc0a60b"): 83982592 + 2084608 + 4823296,
 }
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
@@ -178,7 +180,10 @@ class ClockSampler:
 class DeviceStep:
     """A workload resident on the GPU and one step of the hot path over it."""
 
-    def __init__(self, w: W.Workload, torch, binding, fused: bool = True, early: bool = True):
+    def __init__(self, w: W.Workload, torch, binding, fused: bool = True, early: bool = True,
+                 replicate_layers: int = 0):
+        """replicate_layers > 0: run that many layers, each with its own device copy of the
+        workload's first layer (inputs and caches), instead of the workload's own layers."""
         self.w, self.torch, self.pa, self.fused, self.early = w, torch, binding, fused, early
         dev = torch.device("cuda")
 
@@ -186,24 +191,34 @@ class DeviceStep:
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
         L = w.num_layers
-        self.q = [bf(w.q[i]) for i in range(L)]
-        self.q_src = [bf(w.q[i]) for i in range(L)]
-        self.k = [bf(w.k[i]) for i in range(L)]
-        self.v = [bf(w.v[i]) for i in range(L)]
-        self.k_cache = [bf(w.k_cache[i]) for i in range(L)]
-        self.v_cache = [bf(w.v_cache[i]) for i in range(L)]
+        src = [0] * replicate_layers if replicate_layers else list(range(L))
+        self.num_layers = len(src)
+        first = {}
+
+        def layer(arr, i):
+            if i not in first.setdefault(id(arr), {}):
+                first[id(arr)][i] = bf(arr[i])
+                return first[id(arr)][i]
+            return first[id(arr)][i].clone()
+
+        self.q = [layer(w.q, i) for i in src]
+        self.q_src = [bf(w.q[i]) for i in src]
+        self.k = [layer(w.k, i) for i in src]
+        self.v = [layer(w.v, i) for i in src]
+        self.k_cache = [layer(w.k_cache, i) for i in src]
+        self.v_cache = [layer(w.v_cache, i) for i in src]
         self.positions = torch.from_numpy(w.positions).to(dev)
         self.slots = torch.from_numpy(w.slot_mapping).to(dev)
         self.cos_sin = torch.from_numpy(w.cos_sin).to(dev)
         self.block_tables = torch.from_numpy(w.block_tables).to(dev)
         self.context_lens = torch.from_numpy(w.context_lens).to(dev)
-        self.out = [torch.empty_like(self.q[i]) for i in range(L)]
+        self.out = [torch.empty_like(q) for q in self.q]
         self.P = binding.decode_partition_tokens(w.num_q_heads, w.num_kv_heads, w.num_seqs,
                                                  w.max_context_len, w.partition_tokens)
         self.workspace = binding.decode_workspace(self.q[0], self.k_cache[0], w.max_context_len, self.P)
         # per layer: the (fused) decode kernel and the merge kernel, plus the RoPE + store
         # kernel when it runs apart
-        self.launches_per_step = L * (2 if fused else 3)
+        self.launches_per_step = self.num_layers * (2 if fused else 3)
 
     def rope_store(self, i):
         self.pa.rope_kv_store(self.q[i], self.k[i], self.v[i], self.positions, self.cos_sin,
@@ -228,7 +243,7 @@ class DeviceStep:
                             early_metadata=self.early and i > 0)
 
     def step(self):
-        for i in range(self.w.num_layers):
+        for i in range(self.num_layers):
             if self.fused:
                 self.decode_step(i)
             else:
@@ -421,12 +436,20 @@ def all_configs(args, torch, binding, flush_l2, timed_loop, world):
     metadata on layers after the first, replayed as a CUDA graph), L2 flushed before each
     step: step time, KV bytes per second against the measured HBM copy peak, and decode
     tokens per second (sequences per step over the step time).  prefix32 also reports the
-    bandwidth over its unique KV bytes (the shared prefix is read once from HBM, then from L2)."""
+    bandwidth over its unique KV bytes (the shared prefix is read once from HBM, then from L2).
+
+    mix64_x28 is the batch-64 mixed-length layer run as the attention of a 28-layer model step
+    (Qwen2.5-1.5B's depth): 28 layers, each with its own copy of the layer's caches in HBM
+    (3.4 GB of KV read per step, far past L2), so that layers 2-28 resolve their work beside
+    the layer before, as in a real decode step."""
     peak, kind = hbm_peak()
     res = {}
-    for name in W.WORKLOADS:
-        w = W.make(name)
-        st = DeviceStep(w, torch, binding, fused=True, early=True)
+    runs = [(name, W.make(name), 0) for name in W.WORKLOADS]
+    runs.append(("mix64_x28", None, 28))
+    for name, w, rep in runs:
+        if w is None:
+            w = W.make("mix64")
+        st = DeviceStep(w, torch, binding, fused=True, early=True, replicate_layers=rep)
         for _ in range(3):
             st.step()
         fn = st.step
@@ -443,15 +466,20 @@ def all_configs(args, torch, binding, flush_l2, timed_loop, world):
         rc, flags = binding.get_device_status()
         if rc != 0:
             raise RuntimeError(f"device status after the {name} step: {rc} flags {flags:#x}")
-        nbytes = w.kv_bytes_per_layer() * w.num_layers
+        layers = st.num_layers
+        nbytes = w.kv_bytes_per_layer() * layers
         gbs = nbytes / (ms * 1e-3) / 1e9
-        entry = {"layers": w.num_layers, "num_seqs": w.num_seqs,
+        entry = {"layers": layers, "num_seqs": w.num_seqs,
                  "partition_tokens": st.P or "0 (even split)",
                  "step_us": round(ms * 1e3, 3), "kv_bytes_per_step": nbytes,
                  "GB/s": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
                  "decode_tokens_per_s": round(world * w.num_seqs / (ms * 1e-3), 1)}
+        if layers > 1:
+            entry["per_layer_us"] = round(ms * 1e3 / layers, 3)
+        if rep:
+            entry["layer_caches"] = f"{rep} device copies of one layer's inputs and caches"
         if w.meta.get("shared_prefix_blocks"):
-            ub = w.unique_kv_bytes_per_layer() * w.num_layers
+            ub = w.unique_kv_bytes_per_layer() * layers
             entry["unique_kv_bytes_per_step"] = ub
             entry["unique_GB/s"] = round(ub / (ms * 1e-3) / 1e9, 1)
         res[name] = entry
