@@ -121,6 +121,37 @@ def test_early_metadata_layers_back_to_back(pa, orc, P):
     check_status_clean(pa)
 
 
+@pytest.mark.parametrize("name", ["mix64", "long4"])
+def test_early_metadata_full_size_chain(pa, orc, name):
+    """Three layers of a full-size workload back to back with the flag and one shared
+    workspace: each layer's kernel resolves its work while the kernels of the layer before are
+    still running (the merge lets it launch as soon as the merge starts), and every layer must
+    still give the oracle's result."""
+    base = W.make(name)
+    L = 3
+    d_kc = [dev_bf16(base.k_cache[0]) for _ in range(L)]
+    d_vc = [dev_bf16(base.v_cache[0]) for _ in range(L)]
+    rng_inputs = [tuple(W.SplitMix64(170 + i).normal_bf16(a.size, 1.0).reshape(a.shape)
+                        for a in (base.q[0], base.k[0], base.v[0])) for i in range(L)]
+    dev_in = [tuple(dev_bf16(a) for a in t) for t in rng_inputs]
+    cos_sin, bt, ctx = dev(base.cos_sin), dev(base.block_tables), dev(base.context_lens)
+    P = base.partition_tokens
+    ws = pa.decode_workspace(dev_in[0][0], d_kc[0], base.max_context_len, P)
+    outs = [torch.empty_like(dev_in[0][0]) for _ in range(L)]
+    for i in range(L):
+        q, k, v = dev_in[i]
+        pa.decode_step(q, k, v, cos_sin, d_kc[i], d_vc[i], bt, ctx, base.max_context_len,
+                       base.scale, partition_tokens=P, workspace=ws, out=outs[i],
+                       early_metadata=i > 0)
+    torch.cuda.synchronize()
+    for i in range(L):
+        kc, vc = base.k_cache[0].copy(), base.v_cache[0].copy()
+        ref = oracle_step(orc, base, kc, vc, base.context_lens, rng_inputs[i])
+        assert_out_close(host_bits(outs[i]), ref, f"{name} layer {i}")
+        assert np.array_equal(host_bits(d_vc[i]), vc)
+    check_status_clean(pa)
+
+
 def test_early_metadata_layers_in_a_cuda_graph(pa, orc):
     """The same chain captured once and replayed: each replay appends the next token."""
     ctx0 = np.array([33, 90, 517, 1500], np.int32)
