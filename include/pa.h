@@ -51,6 +51,11 @@
  *    and must be 16-byte aligned (PA_ERR_ALIGN otherwise).  The library allocates nothing.
  *    Its only global state is one 32-bit device status word per GPU, and the fixed scratch
  *    array of pa_decode_static_workspace (PA_STATIC_WORKSPACE_BYTES per GPU).
+ *  - Host-side caches: per GPU, the library looks up the device addresses of its globals (the
+ *    status word, the static scratch) and sets its kernels' shared-memory attributes once, and
+ *    keeps the TMA descriptors it encodes for each cache pointer; all live for the process.  A
+ *    cudaDeviceReset (or anything else that destroys the device's primary context) makes them
+ *    stale: do not call the library on a device after resetting it.
  *  - Asynchrony: calls enqueue work on `stream` and return at once.  Arguments the host can
  *    check are checked before anything is enqueued; on error nothing is launched.
  *  - Values only the device can see (block ids, positions, slots, per-sequence lengths) are
