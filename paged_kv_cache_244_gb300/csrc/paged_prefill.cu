@@ -17,31 +17,34 @@
 //   S_j (128 x 64, fp32, TMEM) = Q K_j^T   8 tcgen05.mma, M = 128, N = 64, K = 16 each
 //   softmax (one thread per row): S_j read with tcgen05.ld, causal mask, a lazy row shift in
 //   the log2 domain (it moves only when the row maximum passes it by more than 8, so P <= 2^8
-//   and O is rarely rescaled), P_j = bf16(2^(scale_log2 s - shift)) written to shared memory
-//   over K_j (dead once S_j is done; 128 rows x 64 keys is exactly its size), the fp32 values
-//   added to the row sum (exponent arguments and sums two at a time, packed f32x2)
+//   and O is rarely rescaled), P_j = bf16(2^(scale_log2 s - shift)) written to a shared-memory
+//   P buffer (128 rows x 64 keys), the fp32 values added to the row sum (exponent arguments and
+//   sums two at a time, packed f32x2)
 //   O (128 x 128, fp32, TMEM) += P_j V_j   4 tcgen05.mma (one per key block), M = N = 128, K = 16
 // Tensor memory (256 columns): Q as bf16 pairs in columns 0-63 (the A operand of S, read from
 // tensor memory: with N = 64 an A read from shared memory at every MMA would crowd shared
 // memory), S in 64-127, O in 128-255.  An MMA takes a fixed minimum time whatever its N up to
 // 64, so S runs 64 keys wide.
 //
-// Warps 0-3 load Q and run the softmax (warp w owns TMEM lanes 32w..32w+31); warp 4 issues the
-// TMA loads (lanes 0-11 one box each; its lanes read 32 block ids at a time, a window ahead);
-// warp 5 runs the MMA loop, one elected lane issuing.  The softmax frees the S columns as soon
-// as it has loaded S_j, and the MMA warp then issues S_{j+1} at once, so the tensor core
-// computes the next scores (and P_{j-1} V_{j-1}) while the softmax works on stage j.  Shared
-// memory is ~97 KB, so two CTAs share an SM.
+// Warps 0-3 load Q and run the softmax (warp w owns TMEM lanes 32w..32w+31); warps 4, 6 and 7
+// issue the TMA loads, one box kind each (K columns 0-63, K columns 64-127, V), lanes 0-3 the
+// stage's four blocks (their lanes read 32 block ids at a time, a window ahead); warp 5 runs
+// the MMA loop, one elected lane issuing.  The softmax frees the S columns as soon as it has
+// loaded S_j, and the MMA warp then issues S_{j+1} at once, so the tensor core computes the
+// next scores (and P_{j-1} V_{j-1}) while the softmax works on stage j.  K and V of a stage have
+// barriers of their own: K_j is dead once S_j is done and its slot refills for stage j + 3
+// then, while V_j waits for P_j V_j -- a K refill does not wait for the softmax of its stage.
+// Shared memory is ~113 KB (three 32 KiB stages, the 16 KiB P buffer, the barriers last), so
+// two CTAs share an SM.
 //
 // K, V and P use the 128-byte swizzle (16-byte chunk c of a 128-byte row r at c ^ (r % 8),
 // 8-row atoms of 1024 bytes).  A stage holds K half 0 of the four blocks (rows 0-63, 8 KiB), K
-// half 1 (8 KiB) -- later P, 128 rows of 64 keys -- then V of blocks 0-3 (4 KiB each, as two
-// 2 KiB halves of 16 rows).  Keys past the context in the context's last block may hold
-// anything: their scores are masked and their V rows zeroed in shared memory before P V.  A
-// block id out of range is not loaded: its keys are masked and its P V step skipped.  Every
-// wait is bounded; a timeout raises PA_FLAG_TIMEOUT and the CTA drains its copies and MMAs
-// before it exits.  Tiles are scheduled latest first over the whole grid: the last tiles of a
-// sequence see the most keys.
+// half 1 (8 KiB), then V of blocks 0-3 (4 KiB each, as two 2 KiB halves of 16 rows).  Keys
+// past the context in the context's last block may hold anything: their scores are masked and
+// their V rows zeroed in shared memory before P V.  A block id out of range is not loaded: its
+// keys are masked and its P V step skipped.  Every wait is bounded; a timeout raises
+// PA_FLAG_TIMEOUT and the CTA drains its copies and MMAs before it exits.  Tiles are scheduled
+// latest first over the whole grid: the last tiles of a sequence see the most keys.
 
 #include <mutex>
 
@@ -62,25 +65,34 @@ constexpr int kPfHalf = kBlockSize * 128;           // 16 rows x 64 bf16: 2 KiB
 constexpr int kPfKHalfBytes = kPfKB * kPfHalf;      // one K half of the stage's blocks: 8 KiB
 constexpr int kPfVOff = 2 * kPfKHalfBytes;          // V tiles after the two K halves
 constexpr int kPfStageBytes = kPfVOff + kPfKB * kTileBytes;   // 32 KiB
-static_assert(kPfRows * kPfKeys * 2 == kPfVOff, "P of a stage fills its K region");
+constexpr int kPfPBytes = kPfRows * kPfKeys * 2;    // P: 128 rows x 64 bf16 keys, 16 KiB
+constexpr int kPfPOff = kPfStages * kPfStageBytes;  // after the stages
+constexpr int kPfHdrOff = kPfPOff + kPfPBytes;      // then the header
 constexpr int kPfHeader = 256;                      // mbarriers, present masks, TMEM address
-constexpr int kPfSmem = kPfHeader + 1024 + kPfStages * kPfStageBytes;
+// Two CTAs per SM: 2 x (this + 1 KiB reserved per CTA) fits the SM's 228 KiB exactly.  The
+// layout wants a 1024-byte aligned start; up to 768 bytes of it may go to aligning.
+constexpr int kPfAlignSlack = 768;
+constexpr int kPfSmem = kPfHdrOff + kPfHeader + kPfAlignSlack;
+static_assert(2 * (kPfSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 constexpr int kPfThreads = 256;                     // 4 softmax warps, TMA warps 4, 6, 7, MMA warp 5
 constexpr uint32_t kPfTmemCols = 256;
 constexpr uint32_t kPfQCol = 0;                     // Q: 64 columns of bf16 pairs
 constexpr uint32_t kPfSCol = 64;                    // S: columns 64-127
 constexpr uint32_t kPfOCol = 128;                   // O: columns 128-255
 
-// header layout (byte offsets)
-constexpr int kBarKvFull = 0;                       // [3] TMA -> MMA, softmax
-constexpr int kBarKvEmpty = 24;                     // [3] MMA (P V done) -> TMA, softmax (O rescale)
-constexpr int kBarSFull = 48;                       // MMA (S done) -> softmax
-constexpr int kBarSFree = 56;                       // softmax (S loaded) -> MMA, 128 arrivals
-constexpr int kBarPFull = 64;                       // [2] softmax (P written) -> MMA, 128 arrivals
-constexpr int kBarDone = 80;                        // MMA thread: its last MMAs finished
-constexpr int kBarQReady = 88;                      // softmax (Q in TMEM) -> MMA, 128 arrivals
-constexpr int kPresent = 96;                        // [3] int: bit i = block i of the stage loaded
-constexpr int kTmemSlot = 112;
+// header layout (byte offsets from the header's start)
+constexpr int kBarKFull = 0;                        // [3] K TMA -> MMA (S), softmax (mask)
+constexpr int kBarVFull = 24;                       // [3] V TMA -> MMA (P V), softmax (V rows zeroed)
+constexpr int kBarKEmpty = 48;                      // [3] MMA (S done) -> K TMA
+constexpr int kBarVEmpty = 72;                      // [3] MMA (P V done) -> V TMA, softmax (P buffer, O)
+constexpr int kBarSFull = 96;                       // MMA (S done) -> softmax
+constexpr int kBarSFree = 104;                      // softmax (S loaded) -> MMA, 128 arrivals
+constexpr int kBarPFull = 112;                      // [2] softmax (P written) -> MMA, 128 arrivals
+constexpr int kBarDone = 128;                       // MMA thread: its last MMAs finished
+constexpr int kBarQReady = 136;                     // softmax (Q in TMEM) -> MMA, 128 arrivals
+constexpr int kPresent = 144;                       // [6] int, stage j at j % 6: bit i = block i loaded
+constexpr int kPresentSlots = 2 * kPfStages;        // a refill (stage j + 3) never overwrites stage j's
+constexpr int kTmemSlot = kPresent + 4 * kPresentSlots;
 static_assert(kTmemSlot + 4 <= kPfHeader, "header");
 
 __global__ void __launch_bounds__(kPfThreads, 2)
@@ -121,8 +133,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
   const int nst = (nblocks + kPfKB - 1) / kPfKB;    // stages of kPfKB key blocks
 
   const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t stages = (raw + kPfHeader + 1023u) & ~1023u;
-  volatile int* present = reinterpret_cast<volatile int*>(smem_raw + kPresent);
+  const uint32_t stages = (raw + 1023u) & ~1023u;
+  if (stages - raw > static_cast<uint32_t>(kPfAlignSlack)) {  // never seen: the start is 1 KiB aligned
+    if (threadIdx.x == 0) raise_flag(a.status, PA_FLAG_TIMEOUT);
+    return;
+  }
+  const uint32_t hdr = stages + kPfHdrOff;
+  unsigned char* const hdr_gen = smem_raw + (hdr - raw);
+  volatile int* present = reinterpret_cast<volatile int*>(hdr_gen + kPresent);
 
   // The first global reads of each role go out before the set-up below, so their latency
   // overlaps it: the softmax threads' Q rows, the TMA warp's first two windows of block ids.
@@ -145,39 +163,44 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPfStages; ++i) {
-      mbar_init(raw + kBarKvFull + 8 * i, 1);
-      mbar_init(raw + kBarKvEmpty + 8 * i, 1);
+      mbar_init(hdr + kBarKFull + 8 * i, 1);
+      mbar_init(hdr + kBarVFull + 8 * i, 1);
+      mbar_init(hdr + kBarKEmpty + 8 * i, 1);
+      mbar_init(hdr + kBarVEmpty + 8 * i, 1);
     }
-    mbar_init(raw + kBarSFull, 1);
-    mbar_init(raw + kBarSFree, 128);
-    mbar_init(raw + kBarPFull, 128);
-    mbar_init(raw + kBarPFull + 8, 128);
-    mbar_init(raw + kBarDone, 1);
-    mbar_init(raw + kBarQReady, 128);
+    mbar_init(hdr + kBarSFull, 1);
+    mbar_init(hdr + kBarSFree, 128);
+    mbar_init(hdr + kBarPFull, 128);
+    mbar_init(hdr + kBarPFull + 8, 128);
+    mbar_init(hdr + kBarDone, 1);
+    mbar_init(hdr + kBarQReady, 128);
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(raw + kTmemSlot, kPfTmemCols);
+    tmem_alloc(hdr + kTmemSlot, kPfTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem_raw + kTmemSlot);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(hdr_gen + kTmemSlot);
 
   if (producer) {
     // ---- TMA producers: stage j holds key blocks 4j .. 4j + 3 -------------------------------
     // Three warps share a stage's 12 boxes, one kind each (lanes 0-3: the four blocks): a warp's
     // TMA instruction issues its lanes' boxes one after another, so one warp issuing all 12
-    // leaves the stage latency-bound; with three, the SM's fill rate is the limit.  The first
-    // producer announces the stage's bytes and its present mask (the others' boxes may land
-    // first: the phase cannot complete before that arrival).
+    // leaves the stage latency-bound; with three, the SM's fill rate is the limit.  The K warps
+    // refill a slot once S of its last stage is done, the V warp once P V is.  The first K warp
+    // announces the K bytes and the stage's present mask, the V warp the V bytes (the other K
+    // warp's boxes may land first: the phase cannot complete before that arrival).
     // Lane k holds the id of block 32 w + k of the current window w (-1 past the tile's
     // blocks); the next window's ids are loaded when the current one starts.
     if (lane == 0) {
       prefetch_tensor_map(&tm_kh);
       prefetch_tensor_map(&tm_v);
     }
+    const uint32_t full = hdr + (kind < 2 ? kBarKFull : kBarVFull);
+    const uint32_t empty = hdr + (kind < 2 ? kBarKEmpty : kBarVEmpty);
     int issued = 0;
     bool failed = false;
     for (int j = 0; j < nst; ++j) {
@@ -188,8 +211,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
         ids_next = load_ids((kPfKB * j) / 32 + 1);
       }
       bool ok = true;
-      if (lane == 0 && j >= kPfStages)
-        ok = mbar_wait_bounded(raw + kBarKvEmpty + 8 * st, ((j / kPfStages) - 1) & 1);
+      if (lane == 0 && j >= kPfStages) ok = mbar_wait_bounded(empty + 8 * st, ((j / kPfStages) - 1) & 1);
       if (!__shfl_sync(kFullMask, ok, 0)) {
         failed = true;
         break;
@@ -199,15 +221,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       const int b = kPfKB * j + bi;
       const bool here = b < nblocks && blk >= 0 && blk < a.num_blocks;
       const int mask = static_cast<int>(__ballot_sync(kFullMask, here) & ((1u << kPfKB) - 1));
-      const uint32_t bar = raw + kBarKvFull + 8 * st;
-      if (kind == 0) {
-        if (lane < kPfKB && b < nblocks && !here) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
-        if (lane == 0) {
-          present[st] = mask;
-          if (mask) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask)) * (2 * kTileBytes));
-          else mbar_arrive(bar);
-        }
+      const uint32_t bar = full + 8 * st;
+      if (kind != 1 && lane == 0) {
+        if (kind == 0) present[j % kPresentSlots] = mask;
+        // K: both halves of each block; V: the whole tile
+        if (mask) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(__popc(mask)) * kTileBytes);
+        else mbar_arrive(bar);
       }
+      if (kind == 0 && lane < kPfKB && b < nblocks && !here) raise_flag(a.status, PA_FLAG_BLOCK_ID_OOB);
       if (lane < kPfKB && here) {
         const int y = (blk * Hkv + g) * kBlockSize;
         const uint32_t dst = stages + st * kPfStageBytes;
@@ -218,12 +239,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       }
       issued = j + 1;
     }
-    if (kind == 0 && lane == 0) {
+    if (lane == 0) {
       if (failed) raise_flag(a.status, PA_FLAG_TIMEOUT);
-      // Copies still in flight can only be those of the last kPfStages fills: let them land
-      // (immediate in a normal run, where the MMAs consumed every stage) before the CTA exits.
+      // Copies still in flight can only be those of this warp's last kPfStages fills: let them
+      // land (immediate in a normal run, where the MMAs consumed every stage) before the CTA exits.
       for (int j = max(0, issued - kPfStages); j < issued; ++j)
-        mbar_wait_bounded(raw + kBarKvFull + 8 * (j % kPfStages), (j / kPfStages) & 1, 10000000ull);
+        mbar_wait_bounded(full + 8 * (j % kPfStages), (j / kPfStages) & 1, 10000000ull);
     }
   } else if (warp == 5) {
     // ---- MMA issuer: the whole warp runs the loop, one elected lane issues ----------------------
@@ -232,18 +253,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
     // descriptors of stage 0; a stage, a k step or a block moves the start address field by
     // (byte offset) / 16, which never carries out of its 14 bits (shared memory < 256 KiB)
     const uint64_t k_desc0 = umma_smem_desc(stages, 16, 1024);
-    const uint64_t p_desc0 = umma_smem_desc(stages, 16, 1024);   // P over K: 128-byte rows
+    const uint64_t p_desc = umma_smem_desc(stages + kPfPOff, 16, 1024);   // P: 128-byte rows
     const uint64_t v_desc0 = umma_smem_desc(stages + kPfVOff, kPfHalf, 1024);
     bool o_started = false;
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(kFullMask, mbar_wait_bounded(bar, parity));
     };
-    // S_j = Q K_j^T into the S columns, once the softmax has loaded S_{j-1}
-    auto issue_s = [&](int j) -> bool {
+    // S_j = Q K_j^T into the S columns, once K_j has landed and the softmax has loaded S_{j-1};
+    // its completion frees K_j's slot as well.  Returns the stage's present mask (-1: timeout),
+    // read while the slot cannot be refilled.
+    auto issue_s = [&](int j) -> int {
       const int st = j % kPfStages;
-      if (!wait_all(raw + kBarKvFull + 8 * st, (j / kPfStages) & 1)) return false;
-      if (j > 0 && !wait_all(raw + kBarSFree, (j - 1) & 1)) return false;
+      if (!wait_all(hdr + kBarKFull + 8 * st, (j / kPfStages) & 1)) return -1;
+      if (j > 0 && !wait_all(hdr + kBarSFree, (j - 1) & 1)) return -1;
       tc_fence_after();
+      const int mask = present[j % kPresentSlots];
       const uint64_t kd = k_desc0 + static_cast<uint64_t>((st * kPfStageBytes) >> 4);
       if (elect_one()) {
 #pragma unroll
@@ -251,52 +275,60 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
           umma_bf16_tmem_a(tmem + kPfSCol, tmem + kPfQCol + 8 * kk,
                            kd + static_cast<uint64_t>(((kk >> 2) * kPfKHalfBytes + (kk & 3) * 32) >> 4), id_s,
                            kk > 0);
-        umma_commit(raw + kBarSFull);
+        umma_commit(hdr + kBarSFull);
+        umma_commit(hdr + kBarKEmpty + 8 * st);
       }
       __syncwarp();
-      return true;
+      return mask;
     };
-    bool failed = !wait_all(raw + kBarQReady, 0);
+    bool failed = !wait_all(hdr + kBarQReady, 0);
+    int mask_cur = 0;
     if (!failed) {
       tc_fence_after();
-      failed = !issue_s(0);
+      mask_cur = issue_s(0);
+      failed = mask_cur < 0;
     }
     for (int j = 0; j < nst && !failed; ++j) {
-      if (j + 1 < nst && !issue_s(j + 1)) {
-        failed = true;
-        break;
+      int mask_next = 0;
+      if (j + 1 < nst) {
+        mask_next = issue_s(j + 1);
+        if (mask_next < 0) {
+          failed = true;
+          break;
+        }
       }
       // P_j: two barriers alternate, so the softmax of stage j + 1 (which may run while this
       // warp still waits here) arrives on the other one
-      if (!wait_all(raw + kBarPFull + 8 * (j & 1), (j >> 1) & 1)) {
+      const int st = j % kPfStages;
+      if (!wait_all(hdr + kBarPFull + 8 * (j & 1), (j >> 1) & 1) ||
+          !wait_all(hdr + kBarVFull + 8 * st, (j / kPfStages) & 1)) {
         failed = true;
         break;
       }
       tc_fence_after();
-      const int st = j % kPfStages;
-      const int mask = present[st];
-      const uint64_t pd = p_desc0 + static_cast<uint64_t>((st * kPfStageBytes) >> 4);
       const uint64_t vd = v_desc0 + static_cast<uint64_t>((st * kPfStageBytes) >> 4);
       if (elect_one()) {
         bool acc = o_started;                       // the first P V of the tile overwrites O
 #pragma unroll
         for (int i = 0; i < kPfKB; ++i) {
-          if (!(mask & (1 << i))) continue;
-          umma_bf16(tmem + kPfOCol, pd + static_cast<uint64_t>((32 * i) >> 4),
+          if (!(mask_cur & (1 << i))) continue;
+          umma_bf16(tmem + kPfOCol, p_desc + static_cast<uint64_t>((32 * i) >> 4),
                     vd + static_cast<uint64_t>((i * kTileBytes) >> 4), id_pv, acc);
           acc = true;
         }
-        // P V of stage j done: the TMA warp may refill the stage, the softmax may rescale O
-        umma_commit(raw + kBarKvEmpty + 8 * st);
+        // P V of stage j done: the V warp may refill the stage, the softmax may write P_{j+1}
+        // and rescale O
+        umma_commit(hdr + kBarVEmpty + 8 * st);
       }
       __syncwarp();
-      o_started = o_started || mask != 0;
+      o_started = o_started || mask_cur != 0;
+      mask_cur = mask_next;
     }
     if (lane == 0) {
       if (failed) raise_flag(a.status, PA_FLAG_TIMEOUT);
       // Every MMA issued has finished before the CTA frees TMEM and exits.
-      umma_commit(raw + kBarDone);
-      mbar_wait_bounded(raw + kBarDone, 0);
+      umma_commit(hdr + kBarDone);
+      mbar_wait_bounded(hdr + kBarDone, 0);
     }
     __syncwarp();
   } else {
@@ -322,7 +354,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(raw + kBarQReady);
+      mbar_arrive(hdr + kBarQReady);
     }
     const float sl = a.scale_log2;
     // the context's last block, if partial: its V rows valid_last..15 are zeroed before P V
@@ -334,14 +366,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
     for (int j = 0; j < nst; ++j) {
       const int st = j % kPfStages;
       // tcgen05.ld / st are warp-collective: a warp goes on only if all its lanes saw the phase
-      const bool ok = mbar_wait_bounded(raw + kBarSFull, j & 1) &&
-                      mbar_wait_bounded(raw + kBarKvFull + 8 * st, (j / kPfStages) & 1);
+      // (K_j's barrier: the stage's present mask, written before it was armed)
+      const bool ok = mbar_wait_bounded(hdr + kBarSFull, j & 1) &&
+                      mbar_wait_bounded(hdr + kBarKFull + 8 * st, (j / kPfStages) & 1);
       if (!__all_sync(kFullMask, ok)) {
         failed = true;
         break;
       }
       tc_fence_after();
-      const int mask = present[st];
+      const int mask = present[j % kPresentSlots];
       float sc[kPfKeys];
       {
         uint32_t sv[32];
@@ -356,7 +389,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       }
       // S_j is in registers: the MMA warp may compute S_{j+1} over it
       tc_fence_before();
-      mbar_arrive(raw + kBarSFree);
+      mbar_arrive(hdr + kBarSFree);
       // Scores stay unscaled until the exponent (scale > 0, so the row maxima are the same).
       // Causal mask and missing blocks -> -inf, only on a stage that reaches past the tile's
       // first query or lacks a block; the others lie wholly before every query of the tile.
@@ -406,17 +439,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
         ps = t0 + t1;
       }
       l = fmaf(l, alpha, ps);
-      // O *= alpha once P V of stage j - 1 has landed (warp-collective TMEM access).  It completes
-      // use (j - 1) / kPfStages of its stage's kv_empty barrier; the use before is complete (it
-      // preceded S_j) and the next one needs this stage's P, so the parity is unambiguous.
-      if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
+      // P V of stage j - 1 must be done before P_j overwrites the P buffer it reads and before O
+      // is rescaled.  It completes use (j - 1) / kPfStages of its stage's V-empty barrier; the
+      // next completion needs P_{j+2}, so the parity is unambiguous.
+      if (j > 0) {
         const int pj = j - 1;
-        if (!__all_sync(kFullMask, mbar_wait_bounded(raw + kBarKvEmpty + 8 * (pj % kPfStages),
+        if (!__all_sync(kFullMask, mbar_wait_bounded(hdr + kBarVEmpty + 8 * (pj % kPfStages),
                                                      (pj / kPfStages) & 1))) {
           failed = true;
           break;
         }
         tc_fence_after();
+      }
+      // O *= alpha (warp-collective TMEM access)
+      if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
 #pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t ov[32];
@@ -428,21 +464,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
         }
         tmem_wait_st();
       }
-      unsigned char* stage_gen = smem_raw + (stages - raw) + st * kPfStageBytes;
-      // P row r over K_j (S_j is complete, so the tensor core no longer reads K_j): 64 keys =
-      // 8 chunks of 16 bytes, chunk c at c ^ (r % 8)
+      // P row r: 64 keys = 8 chunks of 16 bytes, chunk c at c ^ (r % 8)
       {
-        unsigned char* prow = stage_gen + r * 128;
+        unsigned char* prow = smem_raw + (stages - raw) + kPfPOff + r * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
               make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
       }
-      // Keys past the context in its last block: zero their V rows (both 64-column halves).
+      // Keys past the context in its last block: zero their V rows (both 64-column halves),
+      // once V_j has landed.
       const int vb = last_blk - kPfKB * j;
       if (valid_last < kBlockSize && vb >= 0 && vb < kPfKB && ((mask >> vb) & 1)) {
+        if (!__all_sync(kFullMask, mbar_wait_bounded(hdr + kBarVFull + 8 * st, (j / kPfStages) & 1))) {
+          failed = true;
+          break;
+        }
         const int chunks = (kBlockSize - valid_last) * 16;
-        unsigned char* vt = stage_gen + kPfVOff + vb * kTileBytes;
+        unsigned char* vt = smem_raw + (stages - raw) + st * kPfStageBytes + kPfVOff + vb * kTileBytes;
         for (int x = r; x < chunks; x += 128) {
           const int row = valid_last + (x >> 4), half = (x >> 3) & 1, ch = x & 7;
           *reinterpret_cast<uint4*>(vt + half * kPfHalf + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -450,11 +489,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       }
       fence_proxy_async_smem();                     // P and zeroed V rows before the tensor core reads them
       tc_fence_before();
-      mbar_arrive(raw + kBarPFull + 8 * (j & 1));
+      mbar_arrive(hdr + kBarPFull + 8 * (j & 1));
     }
     if (failed) {
       if (lane == 0) raise_flag(a.status, PA_FLAG_TIMEOUT);
-    } else if (__all_sync(kFullMask, mbar_wait_bounded(raw + kBarDone, 0))) {
+    } else if (__all_sync(kFullMask, mbar_wait_bounded(hdr + kBarDone, 0))) {
       // ---- out = O / l for the tile's real rows (kBarDone: the MMA thread's last P V) ---------
       tc_fence_after();
       // a row whose every key was skipped (all its blocks out of range) has l = 0 and an O
@@ -513,6 +552,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     std::lock_guard<std::mutex> lock(mu);
     if (!done[dev]) {
       err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+      if (err != cudaSuccess) return err;
+      // the whole 228 KiB as shared memory: two CTAs per SM need all of it
+      err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
       if (err != cudaSuccess) return err;
       done[dev] = true;
     }
