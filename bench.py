@@ -20,7 +20,9 @@ The printed JSON line carries:
   e2e                  the same metric when every step also copies its inputs (new-token
                        q/k/v, positions, slots, block tables, lengths) from pinned host
                        memory and reads the output back, all inside the timed region (the
-                       copies and calls replayed as one CUDA graph, like the device step);
+                       copies and calls replayed as one CUDA graph, like the device step); the
+                       two copies are pa_stage_copy kernels, and e2e.copy_engine repeats the
+                       step with cudaMemcpyAsync transfers instead;
   roofline             the step's decode call (its partition kernel plus the merge kernel)
                        on one layer, timed alone with CUDA events, against the measured HBM
                        copy bandwidth; beside it gather_floor_*: pa_gather_checksum on the same
@@ -348,6 +350,7 @@ def run_gpu(args, rank, world, dist):
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, st, torch, binding, flush_l2)
+    e2e_ce = run_e2e(args, st, torch, binding, flush_l2, copy_engine=True)
     configs = None if args.no_configs else all_configs(args, torch, binding, flush_l2, timed_loop, world)
     blocks = None if args.no_block_ops else block_ops(torch, binding, flush_l2, timed_loop, w)
     fp8 = None if args.no_fp8 else fp8_kv(torch, binding, timed_loop, st, args.steps)
@@ -358,8 +361,8 @@ def run_gpu(args, rank, world, dist):
         raise RuntimeError(f"device status after timing: {rc} flags {flags:#x}")
 
     # max over ranks of the timed device time; sum of bytes
-    (total_ms_max, e2e_ms_max), (all_bytes,) = reduce_over_ranks(
-        [total_ms, e2e["ms"]], [float(bytes_step)], dist, torch.device("cuda"))
+    (total_ms_max, e2e_ms_max, e2e_ce_ms_max), (all_bytes,) = reduce_over_ranks(
+        [total_ms, e2e["ms"], e2e_ce["ms"]], [float(bytes_step)], dist, torch.device("cuda"))
     if rank != 0:
         return None
 
@@ -418,7 +421,10 @@ def run_gpu(args, rank, world, dist):
         "pa_decode_us": round(1e3 * float(np.mean(plain_ms)), 3),
         "e2e": {"value": round(all_bytes * args.steps / (e2e_ms_max * 1e-3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "ms_per_step": round(e2e_ms_max / args.steps, 6), "launch": e2e["launch"]},
+                "ms_per_step": round(e2e_ms_max / args.steps, 6), "launch": e2e["launch"],
+                "copy_engine": {"value": round(all_bytes * args.steps / (e2e_ce_ms_max * 1e-3) / 1e9, 2),
+                                "ms_per_step": round(e2e_ce_ms_max / args.steps, 6),
+                                "launch": e2e_ce["launch"]}},
         "gpu_launches": st.launches_per_step * args.steps,
         "configs": configs,
         "block_ops": blocks,
@@ -667,12 +673,13 @@ def reduce_over_ranks(maxes, sums, dist, device):
     return [float(x) for x in t.cpu()], [float(x) for x in b.cpu()]
 
 
-def run_e2e(args, st, torch, binding, flush_l2):
+def run_e2e(args, st, torch, binding, flush_l2, copy_engine=False):
     """Every step: one host -> device copy of all the step's inputs (new-token q/k/v of every
     layer, block tables, lengths, and for the split step positions and slots), packed in one
     pinned buffer, then the C-ABI calls on views of the device copy, then one device -> host
     copy of every layer's output, all between the CUDA events.  The KV caches stay resident,
-    as in a serving engine."""
+    as in a serving engine.  The two copies are pa_stage_copy kernels (the library's loads and
+    stores over the CPU-GPU link), or with copy_engine cudaMemcpyAsync transfers."""
     w = st.w
     stream = torch.cuda.current_stream()
     L = w.num_layers
@@ -703,8 +710,20 @@ def run_e2e(args, st, torch, binding, flush_l2):
     d_out = torch.empty((L,) + tuple(st.out[0].shape), dtype=torch.bfloat16, device="cuda")
     h_out = torch.empty(d_out.shape, dtype=torch.bfloat16).pin_memory()
 
+    def h2d():
+        if copy_engine:
+            d_in.copy_(h_in, non_blocking=True)
+        else:
+            binding.stage_copy(d_in, h_in)
+
+    def d2h():
+        if copy_engine:
+            h_out.copy_(d_out, non_blocking=True)
+        else:
+            binding.stage_copy(h_out, d_out)
+
     def one():
-        d_in.copy_(h_in, non_blocking=True)
+        h2d()
         for i in range(L):
             if st.fused:
                 # layers after the first follow a decode kernel, and the copy that wrote the
@@ -718,7 +737,7 @@ def run_e2e(args, st, torch, binding, flush_l2):
                                   st.v_cache[i])
             binding.decode(q[i], st.k_cache[i], st.v_cache[i], bt, ctx, w.max_context_len, w.scale,
                            partition_tokens=st.P, workspace=st.workspace, out=d_out[i])
-        h_out.copy_(d_out, non_blocking=True)
+        d2h()
 
     for _ in range(2):
         one()
@@ -734,6 +753,7 @@ def run_e2e(args, st, torch, binding, flush_l2):
             graph.replay()
             torch.cuda.synchronize()
             step_fn, how = graph.replay, "CUDA graph of the H2D copy, the calls and the D2H copy"
+            how += " (cudaMemcpyAsync)" if copy_engine else " (pa_stage_copy kernels)"
         except Exception as e:  # capture unsupported here: keep eager calls
             how = f"eager calls (graph capture failed: {type(e).__name__})"
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))

@@ -383,6 +383,23 @@ int pa_copy_blocks(const pa_dims* dims, int num_caches, const void* const* src_c
                    const int64_t* block_pairs, int num_pairs, void* stream);
 
 /*
+ * pa_stage_copy -- copy `bytes` from src to dst in one kernel, either side in this GPU's
+ * memory or in page-locked host memory (cudaHostAlloc, cudaHostRegister, PyTorch pin_memory),
+ * which the kernel reads or writes in place over the CPU-GPU link.  For staging a decode
+ * step's packed inputs (new-token q, k, v, block tables, lengths) before the step's calls and
+ * reading its outputs after them: for a few hundred KiB, one kernel's loads are all in flight
+ * at once, where a copy-engine transfer costs several microseconds of set-up.  Plumbing around
+ * the pages' method, not part of it.
+ *
+ *   dst, src  16-byte aligned; the two ranges must not overlap
+ *   bytes     a multiple of 16 (0 is a no-op)
+ * Like every call it waits for the previous kernel on the stream before reading.  Pageable
+ * host memory or another GPU's memory returns PA_ERR_MEMORY.  Returns PA_OK, PA_ERR_NULL,
+ * PA_ERR_ALIGN, PA_ERR_MEMORY or PA_ERR_CUDA (nothing launched on error).  Launches one kernel.
+ */
+int pa_stage_copy(void* dst, const void* src, size_t bytes, void* stream);
+
+/*
  * pa_get_device_status -- synchronise `stream`, then read and clear the calling thread's
  * current GPU's status word.  *flags receives the PA_FLAG_* bits raised since the last
  * read (may be NULL).  Returns PA_OK when no flag was set, PA_ERR_TIMEOUT when the timeout

@@ -86,6 +86,8 @@ def lib():
         L.pa_prefill.restype = i
         L.pa_copy_blocks.argtypes = [pd, i, p, ctypes.c_int64, p, ctypes.c_int64, p, i, p]
         L.pa_copy_blocks.restype = i
+        L.pa_stage_copy.argtypes = [p, p, ctypes.c_size_t, p]
+        L.pa_stage_copy.restype = i
         L.pa_get_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
         L.pa_get_device_status.restype = i
         L.pa_selftest_wait_timeout.argtypes = [ctypes.c_uint32, p]
@@ -432,6 +434,20 @@ def copy_blocks(src_caches, dst_caches, block_pairs, stream=None):
                               ctypes.c_void_p(block_pairs.data_ptr()), block_pairs.shape[0],
                               _stream(stream))
     _check(rc, "pa_copy_blocks")
+
+
+def stage_copy(dst, src, stream=None):
+    """One-kernel copy of a tensor's bytes (pa_stage_copy): dst and src contiguous, on the GPU
+    or in pinned host memory, the same number of bytes (a multiple of 16), 16-byte aligned.
+    For staging a step's packed inputs and reading its outputs around the step's calls."""
+    for t, nm in ((dst, "dst"), (src, "src")):
+        if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{nm} must be contiguous, on the GPU or in pinned host memory")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("dst and src differ in size")
+    _check(lib().pa_stage_copy(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()),
+                               nbytes, _stream(stream)), "pa_stage_copy")
 
 
 def selftest_wait_timeout(limit_us: int = 1000, stream=None):

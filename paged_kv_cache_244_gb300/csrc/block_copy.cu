@@ -55,7 +55,65 @@ __global__ void __launch_bounds__(kCopyWarps * 32) copy_blocks_kernel(const __gr
   }
 }
 
+// pa_stage_copy: n 16-byte words from src to dst, either of them in this GPU's memory or in
+// page-locked host memory (read and written in place over the CPU-GPU link).  Each thread
+// issues its kStageVec loads before its stores, so every word of a few hundred KiB is in flight
+// at once: one round trip over the link, where a copy-engine transfer of the same bytes costs
+// several microseconds of set-up.
+constexpr int kStageThreads = 256;
+constexpr int kStageVec = 2;
+
+__global__ void __launch_bounds__(kStageThreads) stage_copy_kernel(uint4* dst, const uint4* src, long long n) {
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+  const long long stride = static_cast<long long>(gridDim.x) * kStageThreads;
+  for (long long base = static_cast<long long>(blockIdx.x) * kStageThreads + threadIdx.x; base < n;
+       base += stride * kStageVec) {
+    uint4 v[kStageVec];
+#pragma unroll
+    for (int k = 0; k < kStageVec; ++k) {
+      const long long i = base + k * stride;
+      if (i < n) v[k] = src[i];
+    }
+#pragma unroll
+    for (int k = 0; k < kStageVec; ++k) {
+      const long long i = base + k * stride;
+      if (i < n) dst[i] = v[k];
+    }
+  }
+}
+
+int sm_count(int* out) {
+  static std::mutex mu;
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!sms[dev] && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  *out = sms[dev];
+  return 0;
+}
+
 }  // namespace
+
+cudaError_t launch_stage_copy(void* dst, const void* src, long long n16, cudaStream_t stream) {
+  if (n16 <= 0) return cudaSuccess;
+  int n_sms = 0;
+  if (sm_count(&n_sms) != 0) return cudaErrorInvalidDevice;
+  const long long per_cta = static_cast<long long>(kStageThreads) * kStageVec;
+  const long long ctas = min(static_cast<long long>(n_sms) * 8, (n16 + per_cta - 1) / per_cta);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(kStageThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, stage_copy_kernel, static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16);
+}
 
 cudaError_t launch_copy_blocks(const BlockCopyArgs& a, cudaStream_t stream) {
   static std::mutex mu;

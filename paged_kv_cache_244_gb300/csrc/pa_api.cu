@@ -478,6 +478,20 @@ int pa_copy_blocks(const pa_dims* dims, int num_caches, const void* const* src_c
                                                                                      : PA_ERR_CUDA;
 }
 
+int pa_stage_copy(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return PA_OK;
+  if (!dst || !src) return PA_ERR_NULL;
+  if (!aligned16(dst) || !aligned16(src) || bytes % 16 != 0) return PA_ERR_ALIGN;
+  const void* d = nullptr;
+  const void* s = nullptr;
+  if (const int rc = device_address(dst, &d)) return rc;
+  if (const int rc = device_address(src, &s)) return rc;
+  return pa::launch_stage_copy(const_cast<void*>(d), s, static_cast<long long>(bytes / 16),
+                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
 int pa_get_device_status(void* stream, uint32_t* flags) {
   unsigned* status = nullptr;
   if (const int rc = status_word(&status)) return rc;

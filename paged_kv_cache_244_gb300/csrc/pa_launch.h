@@ -119,6 +119,8 @@ bool cache_tensor_map(const void* cache, long long rows, bool fp8, CUtensorMap* 
 cudaError_t launch_rope_kv_store(const RopeArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const BlockCopyArgs& a, cudaStream_t stream);
+// n16 16-byte words from src to dst (device or page-locked host addresses the GPU can access)
+cudaError_t launch_stage_copy(void* dst, const void* src, long long n16, cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // The decode kernel's gather of K/V tiles alone (no attention, no merge): pa_gather_checksum,

@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
                  "pa_decode_partition_tokens", "pa_get_device_status", "pa_status_string",
                  "pa_selftest_wait_timeout", "pa_decode_static_workspace", "pa_decode_step",
                  "pa_copy_blocks", "pa_rope_kv_store_fp8", "pa_decode_fp8", "pa_decode_step_fp8",
-                 "pa_prefill", "pa_gather_checksum", "pa_gather_checksum_fp8"):
+                 "pa_prefill", "pa_gather_checksum", "pa_gather_checksum_fp8", "pa_stage_copy"):
         assert must in names
 
 
@@ -279,6 +279,22 @@ def test_selftest_rejects_bad_limits_on_the_host(L):
     from paged_kv_cache_244_gb300 import binding as b
     assert L.pa_selftest_wait_timeout(0, None) == b.PA_ERR_RANGE
     assert L.pa_selftest_wait_timeout(2000000, None) == b.PA_ERR_RANGE
+
+
+def test_stage_copy_checks_its_arguments_on_the_host(L):
+    """Null, alignment and size checks come before any CUDA call (none is made here)."""
+    import ctypes
+    from paged_kv_cache_244_gb300 import binding as b
+    buf = (ctypes.c_ubyte * 96)()
+    base = ctypes.addressof(buf)
+    a16 = base + (-base) % 16                         # a 16-byte aligned address inside buf
+    vp = ctypes.c_void_p
+    assert L.pa_stage_copy(vp(a16), vp(a16 + 32), 0, None) == b.PA_OK            # no-op
+    assert L.pa_stage_copy(None, vp(a16), 16, None) == b.PA_ERR_NULL
+    assert L.pa_stage_copy(vp(a16), None, 16, None) == b.PA_ERR_NULL
+    assert L.pa_stage_copy(vp(a16 + 8), vp(a16 + 32), 16, None) == b.PA_ERR_ALIGN
+    assert L.pa_stage_copy(vp(a16), vp(a16 + 40), 16, None) == b.PA_ERR_ALIGN
+    assert L.pa_stage_copy(vp(a16), vp(a16 + 32), 24, None) == b.PA_ERR_ALIGN
 
 
 def test_status_strings(L):
