@@ -70,10 +70,13 @@ constexpr int kPfPOff = kPfStages * kPfStageBytes;  // after the stages
 constexpr int kPfHdrOff = kPfPOff + kPfPBytes;      // then the header
 constexpr int kPfHeader = 256;                      // mbarriers, present masks, TMEM address
 // Two CTAs per SM: 2 x (this + 1 KiB reserved per CTA) fits the SM's 228 KiB exactly.  The
-// layout wants a 1024-byte aligned start; up to 768 bytes of it may go to aligning.
-constexpr int kPfAlignSlack = 768;
-constexpr int kPfSmem = kPfHdrOff + kPfHeader + kPfAlignSlack;
+// stages start on the first 1024-byte boundary; the header sits in the padding before them
+// when that is at least kPfHeader bytes, else after the P buffer.  For any 16-byte aligned
+// start (padding 0..1008) the layout ends within kPfSmem: 1008 + kPfHdrOff in the first case,
+// 255 + kPfHdrOff + kPfHeader in the second.
+constexpr int kPfSmem = kPfHdrOff + kPfHeader + 768;
 static_assert(2 * (kPfSmem + 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(1008 + kPfHdrOff <= kPfSmem && kPfHeader - 1 + kPfHdrOff + kPfHeader <= kPfSmem, "layout");
 constexpr int kPfThreads = 256;                     // 4 softmax warps, TMA warps 4, 6, 7, MMA warp 5
 constexpr uint32_t kPfTmemCols = 256;
 constexpr uint32_t kPfQCol = 0;                     // Q: 64 columns of bf16 pairs
@@ -81,7 +84,7 @@ constexpr uint32_t kPfSCol = 64;                    // S: columns 64-127
 constexpr uint32_t kPfOCol = 128;                   // O: columns 128-255
 
 // header layout (byte offsets from the header's start)
-constexpr int kBarKFull = 0;                        // [3] K TMA -> MMA (S), softmax (mask)
+constexpr int kBarKFull = 0;                        // [3] K TMA -> MMA (S)
 constexpr int kBarVFull = 24;                       // [3] V TMA -> MMA (P V), softmax (V rows zeroed)
 constexpr int kBarKEmpty = 48;                      // [3] MMA (S done) -> K TMA
 constexpr int kBarVEmpty = 72;                      // [3] MMA (P V done) -> V TMA, softmax (P buffer, O)
@@ -90,7 +93,7 @@ constexpr int kBarSFree = 104;                      // softmax (S loaded) -> MMA
 constexpr int kBarPFull = 112;                      // [2] softmax (P written) -> MMA, 128 arrivals
 constexpr int kBarDone = 128;                       // MMA thread: its last MMAs finished
 constexpr int kBarQReady = 136;                     // softmax (Q in TMEM) -> MMA, 128 arrivals
-constexpr int kPresent = 144;                       // [6] int, stage j at j % 6: bit i = block i loaded
+constexpr int kPresent = 144;                       // [6] int, stage j at j % 6: bit i = block i loaded (MMA warp)
 constexpr int kPresentSlots = 2 * kPfStages;        // a refill (stage j + 3) never overwrites stage j's
 constexpr int kTmemSlot = kPresent + 4 * kPresentSlots;
 static_assert(kTmemSlot + 4 <= kPfHeader, "header");
@@ -134,11 +137,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
 
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t stages = (raw + 1023u) & ~1023u;
-  if (stages - raw > static_cast<uint32_t>(kPfAlignSlack)) {  // never seen: the start is 1 KiB aligned
-    if (threadIdx.x == 0) raise_flag(a.status, PA_FLAG_TIMEOUT);
-    return;
-  }
-  const uint32_t hdr = stages + kPfHdrOff;
+  const uint32_t pad = stages - raw;                // 0 when the start is 1 KiB aligned
+  const uint32_t hdr = pad >= static_cast<uint32_t>(kPfHeader) ? stages - kPfHeader : stages + kPfHdrOff;
   unsigned char* const hdr_gen = smem_raw + (hdr - raw);
   volatile int* present = reinterpret_cast<volatile int*>(hdr_gen + kPresent);
 
@@ -150,10 +150,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
   uint4 qpre[16];
   const bool producer = warp == 4 || warp >= 6;
   const int kind = warp == 4 ? 0 : warp - 5;        // producers: K cols 0-63, K cols 64-127, V
-  if (producer) {
+  if (producer || warp < 4) {
     ids = load_ids(0);
     ids_next = load_ids(1);
-  } else if (warp < 4) {
+  }
+  if (warp < 4) {
     // row r = query i, head g G + h: 128 bf16 (zero past the queries)
     const int r = threadIdx.x, i = r / G, h = r - (r / G) * G;
     const uint4* src = reinterpret_cast<const uint4*>(
@@ -365,16 +366,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
     const uint32_t sbuf = trow + kPfSCol;
     for (int j = 0; j < nst; ++j) {
       const int st = j % kPfStages;
+      // The stage's present mask, from the same block ids the TMA warps test (lane k holds block
+      // 32 w + k of window w).  Not from K_j's barrier: once S_j is done the slot refills for
+      // stage j + 3, and a late look at that barrier could find it two phases on.
+      const int kw = (kPfKB * j) & 31;
+      if (j > 0 && kw == 0) {
+        ids = ids_next;
+        ids_next = load_ids((kPfKB * j) / 32 + 1);
+      }
+      const int blk = __shfl_sync(kFullMask, ids, kw + (lane & (kPfKB - 1)));
+      const int bq = kPfKB * j + (lane & (kPfKB - 1));
+      const int mask = static_cast<int>(
+          __ballot_sync(kFullMask, bq < nblocks && blk >= 0 && blk < a.num_blocks) & ((1u << kPfKB) - 1));
       // tcgen05.ld / st are warp-collective: a warp goes on only if all its lanes saw the phase
-      // (K_j's barrier: the stage's present mask, written before it was armed)
-      const bool ok = mbar_wait_bounded(hdr + kBarSFull, j & 1) &&
-                      mbar_wait_bounded(hdr + kBarKFull + 8 * st, (j / kPfStages) & 1);
-      if (!__all_sync(kFullMask, ok)) {
+      if (!__all_sync(kFullMask, mbar_wait_bounded(hdr + kBarSFull, j & 1))) {
         failed = true;
         break;
       }
       tc_fence_after();
-      const int mask = present[j % kPresentSlots];
       float sc[kPfKeys];
       {
         uint32_t sv[32];
