@@ -400,6 +400,19 @@ int pa_copy_blocks(const pa_dims* dims, int num_caches, const void* const* src_c
 int pa_stage_copy(void* dst, const void* src, size_t bytes, void* stream);
 
 /*
+ * pa_set_timing_jitter -- test hook for the pipelined kernels' barriers: from the next launch
+ * on, every role of the pa_prefill kernel (softmax warps, TMA warps, MMA warp) sleeps a
+ * pseudo-random time below max_ns (the same for the whole warp, a function of seed, the CTA,
+ * the role and the step) at each step of its pipeline loop, so that tests can drive the
+ * barriers through orders of arrival that undisturbed runs rarely take.  Results must not
+ * change: the arithmetic does not depend on timing.  max_ns = 0 turns it off (the default).
+ * Applies to the calling thread's current GPU; set it only while none of this library's
+ * kernels runs there.  No counterpart in the source pages: race detection support.
+ * Returns PA_OK, PA_ERR_RANGE (max_ns > 1,000,000) or PA_ERR_CUDA.
+ */
+int pa_set_timing_jitter(uint32_t max_ns, uint32_t seed);
+
+/*
  * pa_get_device_status -- synchronise `stream`, then read and clear the calling thread's
  * current GPU's status word.  *flags receives the PA_FLAG_* bits raised since the last
  * read (may be NULL).  Returns PA_OK when no flag was set, PA_ERR_TIMEOUT when the timeout

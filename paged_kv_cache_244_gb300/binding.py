@@ -88,6 +88,8 @@ def lib():
         L.pa_copy_blocks.restype = i
         L.pa_stage_copy.argtypes = [p, p, ctypes.c_size_t, p]
         L.pa_stage_copy.restype = i
+        L.pa_set_timing_jitter.argtypes = [ctypes.c_uint32, ctypes.c_uint32]
+        L.pa_set_timing_jitter.restype = i
         L.pa_get_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
         L.pa_get_device_status.restype = i
         L.pa_selftest_wait_timeout.argtypes = [ctypes.c_uint32, p]
@@ -448,6 +450,12 @@ def stage_copy(dst, src, stream=None):
         raise ValueError("dst and src differ in size")
     _check(lib().pa_stage_copy(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()),
                                nbytes, _stream(stream)), "pa_stage_copy")
+
+
+def set_timing_jitter(max_ns: int, seed: int = 0):
+    """Test hook (pa_set_timing_jitter): pipeline roles of the prefill kernel sleep up to max_ns
+    at each step from the next launch on; 0 turns it off."""
+    _check(lib().pa_set_timing_jitter(int(max_ns), int(seed) & 0xFFFFFFFF), "pa_set_timing_jitter")
 
 
 def selftest_wait_timeout(limit_us: int = 1000, stream=None):

@@ -98,6 +98,25 @@ constexpr int kPresentSlots = 2 * kPfStages;        // a refill (stage j + 3) ne
 constexpr int kTmemSlot = kPresent + 4 * kPresentSlots;
 static_assert(kTmemSlot + 4 <= kPfHeader, "header");
 
+// Timing jitter, a test hook (pa_set_timing_jitter): {max_ns, seed}; max_ns 0 = off.  When on,
+// each role sleeps a pseudo-random time below max_ns at each step of its pipeline loop, the same
+// for the whole warp, so that tests can drive the barriers through orders of arrival that
+// undisturbed runs rarely take.
+__constant__ uint32_t c_pf_jitter[2];
+
+__device__ __forceinline__ void pf_jitter(uint32_t role, uint32_t j) {
+  const uint32_t max_ns = c_pf_jitter[0];
+  if (max_ns == 0) return;
+  uint32_t x = c_pf_jitter[1] ^ (blockIdx.x * 0x9E3779B1u) ^ (blockIdx.y * 0x85EBCA77u) ^
+               (role * 0xC2B2AE3Du) ^ (j * 0x27D4EB2Fu);
+  x ^= x >> 16;
+  x *= 0x7FEB352Du;
+  x ^= x >> 15;
+  x *= 0x846CA68Bu;
+  x ^= x >> 16;
+  __nanosleep(x % max_ns);
+}
+
 __global__ void __launch_bounds__(kPfThreads, 2)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant__ CUtensorMap tm_v,
                const PrefillArgs a) {
@@ -205,6 +224,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
     int issued = 0;
     bool failed = false;
     for (int j = 0; j < nst; ++j) {
+      pf_jitter(8 + kind, j);
       const int st = j % kPfStages;
       const int k = (kPfKB * j) & 31;               // lane holding block 4j
       if (j > 0 && k == 0) {
@@ -290,6 +310,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       failed = mask_cur < 0;
     }
     for (int j = 0; j < nst && !failed; ++j) {
+      pf_jitter(16, j);
       int mask_next = 0;
       if (j + 1 < nst) {
         mask_next = issue_s(j + 1);
@@ -365,6 +386,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
     bool failed = false;
     const uint32_t sbuf = trow + kPfSCol;
     for (int j = 0; j < nst; ++j) {
+      pf_jitter(warp, j);
       const int st = j % kPfStages;
       // The stage's present mask, from the same block ids the TMA warps test (lane k holds block
       // 32 w + k of window w).  Not from K_j's barrier: once S_j is done the slot refills for
@@ -451,6 +473,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_kh, const __grid_constant_
       // P V of stage j - 1 must be done before P_j overwrites the P buffer it reads and before O
       // is rescaled.  It completes use (j - 1) / kPfStages of its stage's V-empty barrier; the
       // next completion needs P_{j+2}, so the parity is unambiguous.
+      pf_jitter(4 + warp, j);
       if (j > 0) {
         const int pj = j - 1;
         if (!__all_sync(kFullMask, mbar_wait_bounded(hdr + kBarVEmpty + 8 * (pj % kPfStages),
@@ -584,3 +607,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace pa
+
+extern "C" int pa_set_timing_jitter(uint32_t max_ns, uint32_t seed) {
+  if (max_ns > 1000000u) return PA_ERR_RANGE;
+  const uint32_t v[2] = {max_ns, seed};
+  return cudaMemcpyToSymbol(pa::c_pf_jitter, v, sizeof v) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}

@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
                  "pa_decode_partition_tokens", "pa_get_device_status", "pa_status_string",
                  "pa_selftest_wait_timeout", "pa_decode_static_workspace", "pa_decode_step",
                  "pa_copy_blocks", "pa_rope_kv_store_fp8", "pa_decode_fp8", "pa_decode_step_fp8",
-                 "pa_prefill", "pa_gather_checksum", "pa_gather_checksum_fp8", "pa_stage_copy"):
+                 "pa_prefill", "pa_gather_checksum", "pa_gather_checksum_fp8", "pa_stage_copy",
+                 "pa_set_timing_jitter"):
         assert must in names
 
 
@@ -295,6 +296,11 @@ def test_stage_copy_checks_its_arguments_on_the_host(L):
     assert L.pa_stage_copy(vp(a16 + 8), vp(a16 + 32), 16, None) == b.PA_ERR_ALIGN
     assert L.pa_stage_copy(vp(a16), vp(a16 + 40), 16, None) == b.PA_ERR_ALIGN
     assert L.pa_stage_copy(vp(a16), vp(a16 + 32), 24, None) == b.PA_ERR_ALIGN
+
+
+def test_timing_jitter_range_is_checked_on_the_host(L):
+    from paged_kv_cache_244_gb300 import binding as b
+    assert L.pa_set_timing_jitter(1000001, 0) == b.PA_ERR_RANGE
 
 
 def test_status_strings(L):

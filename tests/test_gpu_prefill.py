@@ -176,3 +176,26 @@ def test_prefill_long_contexts_every_row(pa, orc, hq, hkv, ctx, ql):
     ref, _ = orc.prefill(w.q, w.q_start, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale)
     assert_out_close(run_prefill(pa, w), ref, f"{hq}/{hkv}")
     check_status_clean(pa)
+
+
+@pytest.mark.parametrize("name,seed,max_ns", [("chunked16", 11, 3000), ("prefill4x2048", 12, 3000),
+                                              ("pf_long", 13, 8000), ("pf_long", 14, 500)])
+def test_prefill_under_timing_jitter_gives_the_same_bits(pa, name, seed, max_ns):
+    """Race check: with pseudo-random sleeps at every pipeline step of every role (TMA warps,
+    MMA warp, softmax warps), the barriers see orders of arrival that undisturbed runs rarely
+    take; the output must be bit-identical (the arithmetic does not depend on timing) and no
+    wait may time out.  A wait that a late look can find two phases on fails here."""
+    if name == "pf_long":
+        ctx, ql = [9000, 777, 4100], [150, 40, 300]
+        w = W.build_prefill("pf_long", ctx, ql, sum((c + 15) // 16 for c in ctx) + 9, 109)
+    else:
+        w = W.make_prefill(name)
+    want = run_prefill(pa, w)
+    check_status_clean(pa)
+    pa.set_timing_jitter(max_ns, seed)
+    try:
+        got = run_prefill(pa, w)
+    finally:
+        pa.set_timing_jitter(0)
+    check_status_clean(pa)
+    assert np.array_equal(got, want)
