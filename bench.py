@@ -463,7 +463,8 @@ def all_configs(args, torch, binding, flush_l2, timed_loop, world):
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph):
                 st.step()
-            graph.replay()
+            for _ in range(max(3, args.warmup)):   # untimed replays, as the main step's warm-up
+                graph.replay()
             torch.cuda.synchronize()
             fn = graph.replay
         except Exception:

@@ -807,13 +807,19 @@ constexpr int kWideGroups = 4;   // piece groups per (sequence, query head) in t
 
 // Every merge warp waits for the partition kernel before it exits, so that the merge grid
 // completes after it and a following launch's own wait (which waits for this grid) orders it
-// after the partition kernel's writes too.  The next grid on the stream may launch as soon as
-// every merge CTA has started: a decode step with early metadata then resolves its work on
-// the SMs that this layer's partition kernel has left, reading only lengths and block tables
-// before its wait.  (Each grid is released only once all CTAs of the grid before it are
-// resident or done, so every wait chain ends in grids that are wholly resident.)
+// after the partition kernel's writes too.  The narrow form lets the next grid on the stream
+// launch as soon as every merge CTA has started: a decode step with early metadata then
+// resolves its work on the SMs that this layer's partition kernel has left, reading only
+// lengths and block tables before its wait.  The wide form lets it launch only after its wait:
+// its CTAs (16 warps, ~60 K registers) cannot sit beside a partition CTA, and merges of later
+// layers launched early would hold SMs that the partition kernels need (measured: a 28-layer
+// batch-1 step 187.5 -> 197.4 us with the early release in both forms).  (Each grid is released
+// only once all CTAs of the grid before it are resident or done, so every wait chain ends in
+// grids that are wholly resident.)
+template <int kGroups>
 __device__ __forceinline__ void wait_for_partitions() {
   pdl_wait_prior_grid();
+  if constexpr (kGroups > 1) pdl_allow_next_grid();
 }
 
 // kGroups == 1 (narrow): CTAs of 8 (or 4) warps, 4 warps per (sequence, query head).
@@ -823,7 +829,7 @@ __device__ __forceinline__ void wait_for_partitions() {
 template <int kGroups>
 __global__ void __launch_bounds__(kGroups == 1 ? kMergeWarps * 32 : kGroups * kMergeSplit * 32, kGroups == 1 ? 2 : 1)
 decode_merge_kernel(const DecodeArgs a) {
-  pdl_allow_next_grid();
+  if constexpr (kGroups == 1) pdl_allow_next_grid();
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * static_cast<int>(blockDim.x >> 5) + static_cast<int>(threadIdx.x >> 5);
   const int w = gw / (kGroups * kMergeSplit);          // (sequence, query head)
@@ -832,7 +838,7 @@ decode_merge_kernel(const DecodeArgs a) {
   const int S = a.num_seqs;
   // Every exit below depends on w alone, which is one per CTA in the wide form.
   if (w >= S * a.num_q_heads) {
-    wait_for_partitions();
+    wait_for_partitions<kGroups>();
     return;
   }
   const int Hkv = a.num_kv_heads;
@@ -857,7 +863,7 @@ decode_merge_kernel(const DecodeArgs a) {
   const int dim = quarter * 32 + lane;
   __nv_bfloat16* orow = a.out + static_cast<size_t>(w) * kHeadDim + dim;
   if (ns == 0) {  // empty context: zero row (after the partition kernel, which may read `out`)
-    wait_for_partitions();
+    wait_for_partitions<kGroups>();
     if (grp == 0) *orow = __float2bfloat16_rn(0.f);
     return;
   }
@@ -870,7 +876,7 @@ decode_merge_kernel(const DecodeArgs a) {
   const int part_last = chunk ? (ns - 1) / chunk : 0;
   const int npieces = v_last - v_first + part_last + 1;
   if (npieces == 1) {
-    wait_for_partitions();  // one piece: written directly by the partition kernel
+    wait_for_partitions<kGroups>();  // one piece: written directly by the partition kernel
     return;
   }
   const int seg = s * Hkv + g;
@@ -880,7 +886,7 @@ decode_merge_kernel(const DecodeArgs a) {
   const float2* ml = a.ws_ml + row_base;
   const float* rows = a.ws_o + row_base * kHeadDim + dim;
   const size_t stride = static_cast<size_t>(G) * kHeadDim;
-  wait_for_partitions();
+  wait_for_partitions<kGroups>();
 
   // One round trip per batch: this lane's (m, l) of the batch's piece `lane`, and its dim of
   // every piece row of the batch, combined into (M, L, acc) in piece order.  A gap (m = -inf,
