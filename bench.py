@@ -73,9 +73,9 @@ METRIC = "paged GQA decode: KV-cache HBM GB/s (% of GB300 peak) and attention to
 # the step form and a hash of the CUDA sources it was taken on: once a kernel changes, the
 # hash no longer matches and roofline.traffic is reported as null until it is captured again.
 MEASURED_TRAFFIC = {
-    ("mix64", "fused", "e84127f4068f2602"): 122106112 + 2958848 + 4185600,
-    ("prefix32", "fused", "e84127f4068f2602"): 4348928 + 0 + 3823104,
-    ("long4", "fused", "e84127f4068f2602"): 83982848 + 2096128 + 4823040,
+    ("mix64", "fused", "a9bdfc08606bc4a5"): 122108160 + 2971136 + 4185856,
+    ("prefix32", "fused", "a9bdfc08606bc4a5"): 4348928 + 0 + 3823104,
+    ("long4", "fused", "a9bdfc08606bc4a5"): 83982336 + 2106880 + 4823808,
 }
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
