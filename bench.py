@@ -35,7 +35,8 @@ The printed JSON line carries:
   cpu_baseline         the fp64 oracle on the host cores over a bounded sample;
   fp8_kv               the step's decode on E4M3 caches (pa_decode_fp8, pa_decode_step_fp8),
                        bandwidth counted on the E4M3 bytes, and beside it gather_floor_*:
-                       pa_gather_checksum_fp8, the same tile gather alone (--no-fp8 skips it);
+                       pa_gather_checksum_fp8, the same tile gather alone; fp8_kv.x28: the
+                       layer as the attention of a 28-layer step (--no-fp8 skips it);
   prefill              pa_prefill on two prefill workloads, TFLOP/s against the measured bf16
                        dense peak, and pa_rope_kv_store of their new tokens against the HBM
                        copy bandwidth (--no-prefill skips it);
@@ -584,6 +585,39 @@ def fp8_kv(torch, binding, timed_loop, st, steps):
     nbytes = w.kv_bytes_per_layer() // 2
     peak, _ = hbm_peak()
     gbs = nbytes / (dec_ms * 1e-3) / 1e9
+
+    # The same layer as the attention of a 28-layer step: 28 device copies of its E4M3 caches
+    # (each layer's kernel resolves its work beside the layer before), one CUDA graph per step.
+    L28 = 28
+    k8s = [k8] + [k8.clone() for _ in range(L28 - 1)]
+    v8s = [v8] + [v8.clone() for _ in range(L28 - 1)]
+    outs = [torch.empty_like(st.q[0]) for _ in range(L28)]
+
+    def chain():
+        for i in range(L28):
+            binding.decode_step_fp8(st.q[0], st.k[0], st.v[0], st.cos_sin, k8s[i], v8s[i], ks, vs,
+                                    st.block_tables, st.context_lens, w.max_context_len, w.scale,
+                                    partition_tokens=st.P, workspace=st.workspace, out=outs[i],
+                                    early_metadata=i > 0)
+
+    chain()
+    x28_fn = chain
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            chain()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        x28_fn = graph.replay
+    except Exception:
+        pass
+    x28_ms = float(np.mean(timed_loop(x28_fn, max(10, steps // 4))))
+    rc, flags = binding.get_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after the 28-layer E4M3 step: {rc} flags {flags:#x}")
+    x28_gbs = L28 * nbytes / (x28_ms * 1e-3) / 1e9
+    del k8s, v8s, outs
     return {"algorithmic_bytes_per_launch": nbytes,
             "pa_decode_fp8_us": round(dec_ms * 1e3, 3), "GB/s": round(gbs, 1),
             "frac_of_hbm_copy_peak": round(gbs / peak, 4),
@@ -591,7 +625,12 @@ def fp8_kv(torch, binding, timed_loop, st, steps):
             "gather_floor_us": round(gat_ms * 1e3, 3),
             "gather_floor_frac": round(nbytes / (gat_ms * 1e-3) / 1e9 / peak, 4),
             "decode_over_floor": round(dec_ms / gat_ms, 4),
-            "context_tokens_per_s": round(int(w.context_lens.astype(np.int64).sum()) / (dec_ms * 1e-3), 1)}
+            "context_tokens_per_s": round(int(w.context_lens.astype(np.int64).sum()) / (dec_ms * 1e-3), 1),
+            "x28": {"layers": L28, "step_us": round(x28_ms * 1e3, 3),
+                    "per_layer_us": round(x28_ms * 1e3 / L28, 3), "GB/s": round(x28_gbs, 1),
+                    "frac_of_hbm_copy_peak": round(x28_gbs / peak, 4),
+                    "layer_caches": f"{L28} device copies of the layer's E4M3 caches, pa_decode_step_fp8 "
+                                    "with early metadata on layers after the first, one CUDA graph"}}
 
 
 def prefill_runs(torch, binding, timed_loop, steps):

@@ -121,6 +121,34 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const void* tenso
 }
 
 // 3-D tile at element coordinates (x, y, z); x * element size must be a multiple of 16 bytes.
+// An L2 policy for data read exactly once (the K/V tiles of a decode step): its lines are the
+// first to be evicted, so that what later kernels read again (lengths, block tables, partial
+// results) stays in L2 while tens of MB stream through it.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  return policy;
+}
+
+__device__ __forceinline__ void tma_load_2d_once(uint32_t dst_smem, const void* tensor_map, int x, int y,
+                                                 uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(dst_smem), "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_once(uint32_t dst_smem, const void* tensor_map, int x, int y,
+                                                 int z, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      ::"r"(dst_smem), "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(x), "r"(y), "r"(z), "r"(bar),
+        "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const void* tensor_map, int x, int y, int z,
                                             uint32_t bar) {
   asm volatile(
