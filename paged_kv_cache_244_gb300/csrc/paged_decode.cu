@@ -44,7 +44,7 @@
 // chunk c ^ (r % 8); the ldmatrix row addresses apply the same XOR, so all eight rows of a
 // matrix hit distinct banks.
 //
-// Variants (template <kStep, kFp8>):
+// Variants (template <kStep, kFp8, kGather, kOnce>):
 //   kStep  the fused decode step ("Pico-vLLM" §2: RoPE fused with the KV cache store): the warp
 //          whose job holds a sequence's new token (position len - 1) stages the token's k, v and
 //          cos/sin row with the tiles, rotates k, writes both rows into the staged tiles before
@@ -53,6 +53,10 @@
 //          12 warps with 2 stages; the byte tiles are read by ldmatrix as 16-bit pairs and widened exactly to
 //          f16 with cvt.f16x2.e4m3x2, the q.K k index permuted alike in both operands; f16 MMAs,
 //          the K scale folded into the softmax scale, the V scale into the output.
+//   kGather the tile gather alone (pa_gather_checksum): an XOR of the tile words instead of the
+//          attention, no merge -- the floor of this kernel's access pattern.
+//   kOnce  launched for calls with early metadata (a layer of a chain): the K/V tiles load with
+//          an evict-first L2 policy, so that what the next layers read again stays in L2.
 
 #include <cmath>
 #include <mutex>
