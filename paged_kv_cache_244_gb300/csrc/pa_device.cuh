@@ -43,11 +43,6 @@ __device__ __forceinline__ void pdl_allow_next_grid() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Barrier kId (1..15; 0 is __syncthreads) among `count` threads (a multiple of 32).
-template <int kId>
-__device__ __forceinline__ void named_bar_sync(int count) {
-  asm volatile("bar.sync %0, %1;" ::"n"(kId), "r"(count) : "memory");
-}
 
 // ---- mbarrier ------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -287,13 +282,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
   asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
                "%10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, "
                "%27, %28, %29, %30, %31, %32};" ::"r"(taddr), PA_W32(v)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
-               "%10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-               "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
                : "memory");
 }
 #undef PA_R32

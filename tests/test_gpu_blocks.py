@@ -50,10 +50,6 @@ def to_dev(a):
     return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
 
 
-def to_pinned(a):
-    return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
-
-
 def bits(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
