@@ -74,9 +74,9 @@ METRIC = "paged GQA decode: KV-cache HBM GB/s (% of GB300 peak) and attention to
 # the step form and a hash of the CUDA sources it was taken on: once a kernel changes, the
 # hash no longer matches and roofline.traffic is reported as null until it is captured again.
 MEASURED_TRAFFIC = {
-    ("mix64", "fused", "68d1e86f37a46c1b"): 122101248 + 2982400 + 4185600,
-    ("prefix32", "fused", "68d1e86f37a46c1b"): 4348928 + 0 + 3822848,
-    ("long4", "fused", "68d1e86f37a46c1b"): 83981312 + 2054656 + 4823552,
+    ("mix64", "fused", "66bc39d37e6f7fac"): 122108928 + 3006464 + 4185600,
+    ("prefix32", "fused", "66bc39d37e6f7fac"): 4348672 + 0 + 3823360,
+    ("long4", "fused", "66bc39d37e6f7fac"): 83981056 + 2105088 + 4823040,
 }
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
